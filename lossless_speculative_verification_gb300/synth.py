@@ -1,0 +1,313 @@
+"""Seeded synthetic inputs for the FastMTP verify step.
+
+This module draws the tensors that both the CUDA path and the CPU oracle
+consume.  It holds none of the method's arithmetic: no router product, no
+softmax, no selection, no expert FFN, no argmax and no acceptance rule.  What
+it does hold is input shaping:
+
+* bf16 rounding of float32 draws (round to nearest even), so that every
+  consumer sees the same bf16 bits;
+* hidden states drawn as N(0,1) rows rescaled onto the sphere of radius
+  sqrt(H) (unit mean square, the distribution of "N(0,1) after RMSNorm");
+* verifier logits N(0, std 2) with a *planted* row maximum, so that the
+  greedy token of every row is known by construction (a tie with a second
+  index is planted in a fraction of the rows);
+* draft tokens that agree with the planted greedy token with a given
+  probability per position (the pages report conditional acceptances
+  0.830 / 0.663 / 0.636 at positions 1/2/3, Table 8 of the jina-ocr-v1
+  paper as quoted by the evolve.pub review);
+* an optional per-row rejection callback for the hidden states, which the
+  tests use to enforce a minimum gap between consecutive router places
+  (the callback is supplied by the caller; this module never computes it).
+
+Randomness: numpy PCG64 streams spawned from one SeedSequence per problem,
+one stream per tensor, so that adding a tensor never shifts another one.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+# Conditional acceptance at draft positions 1/2/3 reported for K=3 on an L4
+# (jina-ocr-v1 paper, Table 8, as summarised in the evolve.pub review).
+PAGE_ACCEPT = (0.830, 0.663, 0.636)
+
+VOCAB = 129_280          # decoder vocabulary of the DeepSeek-OCR family decoder
+SWEEP_B = (1, 4, 8, 16, 32, 64)
+SWEEP_K = (1, 2, 3)
+
+
+# --------------------------------------------------------------------------- bf16 bits
+def bf16_bits(a) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); returns uint16 bits."""
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    u = f.view(np.uint32)
+    r = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + r) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_value(u) -> np.ndarray:
+    """Widen bf16 bits (uint16) to float32 exactly."""
+    u = np.ascontiguousarray(u, dtype=np.uint16)
+    return (u.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_next_up(u: np.ndarray) -> np.ndarray:
+    """The next larger bf16 value (finite inputs only)."""
+    u = np.asarray(u, dtype=np.uint16)
+    neg = (u & np.uint16(0x8000)) != 0
+    zero_neg = u == np.uint16(0x8000)
+    out = np.where(neg, u - np.uint16(1), u + np.uint16(1)).astype(np.uint16)
+    out = np.where(zero_neg, np.uint16(0x0001), out)
+    return out.astype(np.uint16)
+
+
+def streams(seed: int, n: int) -> list[np.random.Generator]:
+    ss = np.random.SeedSequence(seed)
+    return [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(n)]
+
+
+# --------------------------------------------------------------------------- shapes
+@dataclass(frozen=True)
+class MoeDims:
+    """One MoE FFN layer: T tokens of width H, E routed experts (top-k) of
+    SwiGLU intermediate I, and S always-on shared experts of intermediate I."""
+    T: int
+    H: int
+    E: int
+    k: int
+    S: int
+    I: int
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    dims: MoeDims
+    B: int = 0
+    K: int = 0
+    V: int = 0
+    hidden: str = "sphere"        # "sphere" (unit RMS rows) or "normal" (N(0, 0.02))
+    accept: tuple = PAGE_ACCEPT
+    layers: int = 1
+    zipf_s: float = 0.0
+
+
+def _verify_dims(B, K, H=1280, E=64, k=6, S=2, I=896):
+    return MoeDims(T=B * (K + 1), H=H, E=E, k=k, S=S, I=I)
+
+
+WORKLOADS = {
+    # 4 sequences x (K=3)+1 = 16 tokens, hidden 256, 8 experts top-2, 1 shared,
+    # intermediate 128, everything N(0, 0.02); acceptance over a 1024-token vocab
+    # with each draft equal to the greedy token with probability 0.8.
+    "tiny": Workload("tiny", MoeDims(16, 256, 8, 2, 1, 128), B=4, K=3, V=1024,
+                     hidden="normal", accept=(0.8, 0.8, 0.8)),
+    # 32 sequences x (K=3)+1 = 128 tokens through the decoder MoE layer shape
+    # (64 routed experts top-6 + 2 shared, hidden 1280, intermediate 896),
+    # then greedy acceptance over the 129,280-token vocabulary.
+    "decode": Workload("decode", _verify_dims(32, 3), B=32, K=3, V=VOCAB),
+    # 8 pages x (1,156 visual + 64 prompt tokens) = 9,760 tokens, same layer.
+    "prefill": Workload("prefill", MoeDims(9760, 1280, 64, 6, 2, 896)),
+    # 11 layers of the decode layer shape at 64 x (K=3)+1 = 256 tokens, router
+    # popularity skewed Zipf(1.2) over the experts, then K=3 acceptance.
+    "stack": Workload("stack", _verify_dims(64, 3), B=64, K=3, V=VOCAB, layers=11,
+                      zipf_s=1.2),
+}
+
+
+def sweep_workload(B: int, K: int) -> Workload:
+    """One point of the (batch, K) verify sweep through the decode layer."""
+    return Workload(f"sweep_b{B}_k{K}", _verify_dims(B, K), B=B, K=K, V=VOCAB,
+                    accept=PAGE_ACCEPT[:K])
+
+
+def sweep_seed(B: int, K: int) -> int:
+    return 1000 * B + K
+
+
+# --------------------------------------------------------------------------- MoE tensors
+@dataclass
+class MoeProblem:
+    dims: MoeDims
+    x: np.ndarray            # [T,H] bf16 bits
+    w_router: np.ndarray     # [E,H]
+    w_gate_up: np.ndarray    # [E,2I,H]: rows 0..I-1 gate, I..2I-1 up
+    w_down: np.ndarray       # [E,H,I]
+    ws_gate_up: np.ndarray   # [2*S*I,H]: rows 0..S*I-1 gates of the S shared experts, then their ups
+    ws_down: np.ndarray      # [H,S*I]
+    resampled: int = 0
+    extra: dict = field(default_factory=dict)
+
+
+def _normal_bf16(rng, shape, std):
+    return bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(std))
+
+
+def moe_weights(d: MoeDims, rngs, std=0.02):
+    """Router, routed-expert and shared-expert weights, N(0, std) in bf16."""
+    r_router, r_gu, r_dn, r_sgu, r_sdn = rngs
+    w_router = _normal_bf16(r_router, (d.E, d.H), std)
+    w_gate_up = np.empty((d.E, 2 * d.I, d.H), dtype=np.uint16)
+    w_down = np.empty((d.E, d.H, d.I), dtype=np.uint16)
+    for e in range(d.E):                     # per expert keeps the float32 temporaries small
+        w_gate_up[e] = _normal_bf16(r_gu, (2 * d.I, d.H), std)
+        w_down[e] = _normal_bf16(r_dn, (d.H, d.I), std)
+    ws_gate_up = _normal_bf16(r_sgu, (2 * d.S * d.I, d.H), std)
+    ws_down = _normal_bf16(r_sdn, (d.H, d.S * d.I), std)
+    return w_router, w_gate_up, w_down, ws_gate_up, ws_down
+
+
+def hidden_rows(rng, n, H, kind) -> np.ndarray:
+    if kind == "normal":
+        return _normal_bf16(rng, (n, H), 0.02)
+    z = rng.standard_normal((n, H), dtype=np.float32).astype(np.float64)
+    z *= math.sqrt(H) / np.sqrt((z * z).sum(axis=1, keepdims=True))
+    return bf16_bits(z.astype(np.float32))
+
+
+def _resample(x, rng, row_ok, draw, max_rounds):
+    """Redraw rows of x that the caller's predicate rejects (deterministic in the seed)."""
+    total = 0
+    for _ in range(max_rounds):
+        ok = np.asarray(row_ok(x), dtype=bool)
+        bad = np.nonzero(~ok)[0]
+        if bad.size == 0:
+            return total
+        x[bad] = draw(rng, bad.size)
+        total += int(bad.size)
+    raise RuntimeError("row predicate still failing after %d rounds" % max_rounds)
+
+
+def moe_problem(w: Workload | MoeDims, seed: int = 0, row_ok=None, hidden: str | None = None,
+                max_rounds: int = 200) -> MoeProblem:
+    """One MoE layer's weights and hidden states.
+
+    row_ok(x_bits, w_router_bits) -> bool[T] (optional) rejects hidden rows;
+    rejected rows are redrawn from the hidden-state stream until all pass.
+    """
+    d = w.dims if isinstance(w, Workload) else w
+    kind = hidden or (w.hidden if isinstance(w, Workload) else "sphere")
+    rs = streams(seed, 6)
+    w_router, w_gate_up, w_down, ws_gate_up, ws_down = moe_weights(d, rs[:5])
+    x = hidden_rows(rs[5], d.T, d.H, kind)
+    n = 0
+    if row_ok is not None:
+        n = _resample(x, rs[5], lambda xx: row_ok(xx, w_router),
+                      lambda rng, m: hidden_rows(rng, m, d.H, kind), max_rounds)
+    return MoeProblem(d, x, w_router, w_gate_up, w_down, ws_gate_up, ws_down, n)
+
+
+# --------------------------------------------------------------------------- stack
+def zipf_shares(E: int, s: float) -> np.ndarray:
+    r = np.arange(1, E + 1, dtype=np.float64)
+    z = r ** (-s)
+    return z / z.sum()
+
+
+def stack_problem(w: Workload, seed: int = 0, row_ok=None, max_rounds: int = 200):
+    """Per-layer weights for the layer stack plus the residual stream x0 and the
+    first layer input h0.
+
+    Popularity skew: every hidden row carries a DC component of 1 (x0 = z + 1),
+    and router row e of every layer gets a constant added, chosen so that the
+    constant shifts expert e's router score by ln(zipf share of its rank); the
+    rank of each expert is a seeded permutation per layer.  This tilts the
+    softmax gate towards a Zipf(s) popularity without touching the selection
+    rule itself.
+    """
+    d = w.dims
+    rs = streams(seed, 2 + 6 * w.layers)
+    r_x, r_perm = rs[0], rs[1]
+
+    def draw(rng, m):
+        z = rng.standard_normal((m, d.H), dtype=np.float32).astype(np.float64) + 1.0
+        return z
+
+    x0f = draw(r_x, d.T)
+
+    def to_h(xf):
+        # rows rescaled to unit mean square (the normalised layer input)
+        return bf16_bits((xf * np.sqrt(d.H / (xf * xf).sum(axis=1, keepdims=True))).astype(np.float32))
+
+    shares = zipf_shares(d.E, w.zipf_s)
+    beta = np.log(shares)
+    layers = []
+    for l in range(w.layers):
+        w_router, w_gate_up, w_down, ws_gate_up, ws_down = moe_weights(d, rs[2 + 6 * l: 7 + 6 * l])
+        layers.append(dict(w_router=w_router, w_gate_up=w_gate_up, w_down=w_down,
+                           ws_gate_up=ws_gate_up, ws_down=ws_down))
+    h0 = to_h(x0f)
+    mean_h = float(bf16_value(h0).astype(np.float64).mean())
+    for l in range(w.layers):
+        rank = r_perm.permutation(d.E)              # expert e gets zipf rank rank[e]
+        shift = beta[rank] / (d.H * mean_h)
+        wr = bf16_value(layers[l]["w_router"]).astype(np.float64) + shift[:, None]
+        layers[l]["w_router"] = bf16_bits(wr.astype(np.float32))
+        layers[l]["zipf_rank"] = rank
+    n = 0
+    if row_ok is not None:
+        wr0 = layers[0]["w_router"]
+        for _ in range(max_rounds):
+            ok = np.asarray(row_ok(h0, wr0), dtype=bool)
+            bad = np.nonzero(~ok)[0]
+            if bad.size == 0:
+                break
+            x0f[bad] = draw(r_x, bad.size)
+            h0 = to_h(x0f)
+            n += int(bad.size)
+        else:
+            raise RuntimeError("row predicate still failing")
+    x0 = bf16_bits(x0f.astype(np.float32))
+    return dict(dims=d, x0=x0, h0=h0, layers=layers, resampled=n)
+
+
+# --------------------------------------------------------------------------- verify logits
+def verify_logits(B: int, K: int, V: int, seed: int, std: float = 2.0, tie_frac: float = 0.25):
+    """Verifier logits [B, K+1, V] in bf16 bits with a planted greedy token per row.
+
+    Every row is drawn N(0, std) and rounded to bf16; one uniformly chosen
+    index g is then raised to the next bf16 above the row's largest value, so
+    g is the unique maximum.  In about tie_frac of the rows a second uniformly
+    chosen index h != g is set to the same value; the greedy token with ties
+    going to the lower index is then min(g, h).  Returns (logits, planted).
+    """
+    r_val, r_g, r_tie = streams(seed, 3)
+    R = B * (K + 1)
+    logits = np.empty((R, V), dtype=np.uint16)
+    chunk = max(1, (1 << 24) // max(V, 1))
+    for r0 in range(0, R, chunk):
+        r1 = min(R, r0 + chunk)
+        logits[r0:r1] = _normal_bf16(r_val, (r1 - r0, V), std)
+    g = r_g.integers(0, V, size=R)
+    top = bf16_bits(bf16_value(logits).max(axis=1))
+    logits[np.arange(R), g] = bf16_next_up(top)
+    planted = g.copy()
+    if V > 1:
+        tie = r_tie.random(R) < tie_frac
+        h = (g + 1 + r_tie.integers(0, V - 1, size=R)) % V
+        rows = np.nonzero(tie)[0]
+        logits[rows, h[rows]] = logits[rows, g[rows]]
+        planted[rows] = np.minimum(g[rows], h[rows])
+    return logits.reshape(B, K + 1, V), planted.reshape(B, K + 1).astype(np.int32)
+
+
+def draft_tokens(planted: np.ndarray, V: int, probs, seed: int) -> np.ndarray:
+    """Drafts [B, K]: draft j equals planted[b, j] with probability probs[j],
+    independently per position, else a uniform token among the other V-1."""
+    B, K1 = planted.shape
+    K = K1 - 1
+    (rng,) = streams(seed + 0x5EED, 1)
+    p = np.asarray(probs, dtype=np.float64)[:K]
+    hit = rng.random((B, K)) < p[None, :]
+    other = (planted[:, :K] + 1 + rng.integers(0, max(V - 1, 1), size=(B, K))) % V
+    return np.where(hit, planted[:, :K], other).astype(np.int32)
+
+
+def verify_problem(w: Workload, seed: int = 0):
+    """Logits, planted greedy tokens and drafts for w's (B, K, V)."""
+    logits, planted = verify_logits(w.B, w.K, w.V, seed)
+    drafts = draft_tokens(planted, w.V, w.accept, seed)
+    return logits, planted, drafts

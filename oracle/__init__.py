@@ -1,0 +1,191 @@
+"""CPU oracle for the FastMTP verification step (TEST INFRASTRUCTURE ONLY).
+
+Plain, slow C loops (oracle.c) behind a ctypes wrapper.  Only the tests, the
+smoke check and the benchmark's CPU-baseline leg may import this package; the
+CUDA library never links, loads or calls it, and the two share no code.
+
+Pins (checked by tests marked "not gpu"):
+  route      -- torch.softmax / torch.topk special cases, planted one-hot
+                routing, exact-tie order, brute force on tiny inputs
+  route_gaps -- brute-force fp64 sort on tiny inputs
+  permute    -- bincount / cumsum, bijection and sort-order invariants
+  experts    -- closed form with H = I = 1, identical-expert invariant
+                (k = E gives one dense SwiGLU FFN), dense brute force in
+                torch fp64 with a different formulation (all experts masked)
+  combine    -- closed form on hand-built inputs
+  layer      -- the two above composed; shared-only and single-expert cases
+  accept     -- exhaustive brute force on tiny vocabularies, planted greedy
+                tokens, torch.argmax, greedy-decoding equivalence on a toy
+                model, closed form of tokens per step vs the pages' 2.73
+  rmsnorm    -- closed form on constant rows, torch rms_norm in fp64
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library next to it (gcc, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+                               "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i = ctypes.c_int
+            sig = {
+                "oracle_route": [P, P, i, i, i, i, P, P, P],
+                "oracle_route_gaps": [P, P, i, i, i, i, P],
+                "oracle_permute": [P, i, i, i, P, P, P, P],
+                "oracle_expert_rows": [P, P, P, i, i, i, P, P, i, P],
+                "oracle_shared_rows": [P, P, P, i, i, i, P, i, P],
+                "oracle_combine": [P, P, P, P, i, i, i, P],
+                "oracle_moe_layer": [P, P, P, P, P, P, i, i, i, i, i, i, P, i, P, P, P],
+                "oracle_rmsnorm_residual": [P, P, i, i, ctypes.c_double, P, P],
+                "oracle_accept": [P, P, i, i, i, P, P, P],
+            }
+            for name, args in sig.items():
+                f = getattr(_lib, name)
+                f.argtypes = args
+                f.restype = ctypes.c_int
+    return _lib
+
+
+def _p(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise ValueError("%s failed with code %d" % (name, rc))
+
+
+def route(x, w_router, k, return_logits=False):
+    """Top-k routing of every token row of x (bf16 bits [T,H]) by w_router ([E,H])."""
+    x = _c(x, np.uint16); w = _c(w_router, np.uint16)
+    T, H = x.shape
+    E = w.shape[0]
+    idx = np.zeros((T, k), np.int32)
+    p = np.zeros((T, k), np.float64)
+    logits = np.zeros((T, E), np.float32) if return_logits else None
+    _check(_load().oracle_route(_p(x), _p(w), T, H, E, k, _p(idx), _p(p), _p(logits)), "route")
+    return (idx, p, logits) if return_logits else (idx, p)
+
+
+def route_gaps(x, w_router, k):
+    x = _c(x, np.uint16); w = _c(w_router, np.uint16)
+    T, H = x.shape
+    gap = np.zeros(T, np.float64)
+    _check(_load().oracle_route_gaps(_p(x), _p(w), T, H, w.shape[0], k, _p(gap)), "route_gaps")
+    return gap
+
+
+def gap_ok(k, min_gap=1e-3):
+    """Row predicate for the input generator: consecutive router places >= min_gap apart."""
+    return lambda x, w_router: route_gaps(x, w_router, k) >= min_gap
+
+
+def permute(topk_idx, E):
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    perm = np.zeros(T * k, np.int32)
+    inv = np.zeros(T * k, np.int32)
+    _check(_load().oracle_permute(_p(idx), T, k, E, _p(counts), _p(offsets), _p(perm), _p(inv)), "permute")
+    return counts, offsets, perm, inv
+
+
+def expert_rows(x, w_gate_up, w_down, token, expert):
+    x = _c(x, np.uint16); wgu = _c(w_gate_up, np.uint16); wd = _c(w_down, np.uint16)
+    token = _c(token, np.int32); expert = _c(expert, np.int32)
+    E, I2, H = wgu.shape
+    y = np.zeros((token.size, H), np.float64)
+    _check(_load().oracle_expert_rows(_p(x), _p(wgu), _p(wd), H, I2 // 2, E, _p(token), _p(expert),
+                                      token.size, _p(y)), "expert_rows")
+    return y
+
+
+def shared_rows(x, ws_gate_up, ws_down, S, token=None):
+    x = _c(x, np.uint16); wgu = _c(ws_gate_up, np.uint16); wd = _c(ws_down, np.uint16)
+    T, H = x.shape
+    token = np.arange(T, dtype=np.int32) if token is None else _c(token, np.int32)
+    I = wgu.shape[0] // (2 * S) if S > 0 else 1
+    y = np.zeros((token.size, H), np.float64)
+    _check(_load().oracle_shared_rows(_p(x), _p(wgu), _p(wd), H, I, S, _p(token), token.size, _p(y)),
+           "shared_rows")
+    return y
+
+
+def combine(y_perm, inv, topk_w, y_shared, T, k):
+    yp = _c(y_perm, np.float32); inv = _c(inv, np.int32); w = _c(topk_w, np.float32)
+    ys = None if y_shared is None else _c(y_shared, np.float32)
+    H = yp.shape[1]
+    out = np.zeros((T, H), np.float64)
+    _check(_load().oracle_combine(_p(yp), _p(inv), _p(w), _p(ys), T, k, H, _p(out)), "combine")
+    return out
+
+
+def moe_layer(x, w_router, w_gate_up, w_down, ws_gate_up, ws_down, k, S, tokens=None):
+    """MoE layer output (double) for the listed tokens (all when None), plus routing."""
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    E = w_router.shape[0]
+    I = w_gate_up.shape[1] // 2
+    tok = None if tokens is None else _c(tokens, np.int32)
+    n = T if tok is None else tok.size
+    out = np.zeros((n, H), np.float64)
+    idx = np.zeros((n, k), np.int32)
+    w = np.zeros((n, k), np.float64)
+    wsg = _c(ws_gate_up, np.uint16) if S > 0 else np.zeros(1, np.uint16)
+    wsd = _c(ws_down, np.uint16) if S > 0 else np.zeros(1, np.uint16)
+    _check(_load().oracle_moe_layer(_p(x), _p(_c(w_router, np.uint16)), _p(_c(w_gate_up, np.uint16)),
+                                    _p(_c(w_down, np.uint16)), _p(wsg), _p(wsd), T, H, E, k, S, I,
+                                    _p(tok), n, _p(out), _p(idx), _p(w)), "moe_layer")
+    return out, idx, w
+
+
+def rmsnorm_residual(x, y, eps=1e-6):
+    x = _c(x, np.uint16); y = _c(y, np.uint16)
+    T, H = x.shape
+    xn = np.zeros((T, H), np.float64)
+    hn = np.zeros((T, H), np.float64)
+    _check(_load().oracle_rmsnorm_residual(_p(x), _p(y), T, H, eps, _p(xn), _p(hn)), "rmsnorm_residual")
+    return xn, hn
+
+
+def accept(logits, drafts):
+    """Greedy verification: logits [B,K+1,V] bf16 bits, drafts [B,K] int32."""
+    lg = _c(logits, np.uint16); d = _c(drafts, np.int32)
+    B, K1, V = lg.shape
+    K = K1 - 1
+    if d.shape != (B, K):
+        raise ValueError("drafts must be [B,K]")
+    argmax = np.zeros((B, K1), np.int32)
+    alen = np.zeros(B, np.int32)
+    committed = np.zeros((B, K1), np.int32)
+    _check(_load().oracle_accept(_p(lg), _p(d), B, K, V, _p(argmax), _p(alen), _p(committed)), "accept")
+    return argmax, alen, committed

@@ -1,0 +1,365 @@
+"""Pins for the CPU oracle: every check ties it to something other than itself
+(page numbers, closed forms, invariants, library special cases, brute force
+in a different formulation).  CPU only."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from lossless_speculative_verification_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bits(a):
+    return synth.bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+def val64(u):
+    return synth.bf16_value(u).astype(np.float64)
+
+
+def tiny_problem(T=12, H=32, E=8, k=2, S=1, I=16, seed=0, std=0.3):
+    """Small layer with bigger weights than the workloads so that outputs are O(1)."""
+    rs = synth.streams(seed, 6)
+    d = synth.MoeDims(T, H, E, k, S, I)
+    w = [bits(r.standard_normal(s) * std) for r, s in zip(
+        rs[:5], [(E, H), (E, 2 * I, H), (E, H, I), (2 * S * I, H), (H, S * I)])]
+    x = bits(rs[5].standard_normal((T, H)))
+    return d, x, w
+
+
+# ----------------------------------------------------------------------------- router
+def test_route_matches_torch_softmax_and_topk():
+    d, x, (wr, *_rest) = tiny_problem(T=64, E=16, k=4)
+    gaps = oracle.route_gaps(x, wr, d.k)
+    keep = gaps >= 1e-3
+    idx, p = oracle.route(x, wr, d.k)
+    logits = torch.from_numpy(val64(x)) @ torch.from_numpy(val64(wr)).T
+    prob = torch.softmax(logits, dim=-1)
+    tv, ti = torch.topk(logits, d.k, dim=-1)
+    assert keep.sum() > 40
+    np.testing.assert_array_equal(idx[keep], ti.numpy()[keep])
+    ref_p = torch.gather(prob, 1, torch.from_numpy(idx).long()).numpy()
+    np.testing.assert_allclose(p, ref_p, rtol=1e-5, atol=1e-7)
+
+
+def test_route_planted_one_hot():
+    # x = unit vector at column c, so the router score of expert e is W_r[e, c].
+    E, H, k, c = 10, 24, 4, 7
+    order = np.array([3, 8, 0, 5, 9, 1, 2, 4, 6, 7])          # planted ranking
+    wr = np.zeros((E, H), np.float32)
+    wr[order, c] = 2.25 - 0.25 * np.arange(E)                  # bf16-exact steps of 0.25
+    wr[:, (c + 1) % H] = 5.0                                   # decoy column: a transposed product would see it
+    x = np.zeros((1, H), np.float32)
+    x[0, c] = 1.0
+    idx, p = oracle.route(bits(x), bits(wr), k)
+    np.testing.assert_array_equal(idx[0], order[:k])
+    s = 2.25 - 0.25 * np.arange(E)
+    z = np.exp(s - s.max())
+    np.testing.assert_allclose(p[0], (z / z.sum())[:k], rtol=1e-12)
+
+
+def test_route_ties_go_to_lower_index_and_softmax_sums_to_one():
+    E, H = 8, 16
+    rs = np.random.default_rng(3)
+    row = rs.standard_normal(H)
+    wr = np.tile(row, (E, 1))                                  # all experts identical: all scores tie
+    x = bits(rs.standard_normal((5, H)))
+    idx, p = oracle.route(x, bits(wr), E)
+    np.testing.assert_array_equal(idx, np.tile(np.arange(E), (5, 1)))
+    np.testing.assert_allclose(p, 1.0 / E, rtol=1e-12)
+    # two duplicated rows among distinct ones: the lower index comes first
+    wr2 = rs.standard_normal((E, H))
+    wr2[6] = wr2[2]
+    x1 = np.zeros((1, H)); x1[0] = wr2[2]                      # makes expert 2 (and 6) the largest score
+    idx2, p2 = oracle.route(bits(x1), bits(wr2), 3)
+    assert list(idx2[0][:2]) == [2, 6]
+    assert p2[0][0] == p2[0][1]
+    # with k = E the selected probabilities are the whole softmax
+    _, xx, (wr3, *_r) = tiny_problem(T=9, E=8, k=8)
+    _, p3 = oracle.route(xx, wr3, 8)
+    np.testing.assert_allclose(p3.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(np.diff(p3, axis=1) <= 0)
+
+
+def test_route_gaps_brute_force():
+    d, x, (wr, *_r) = tiny_problem(T=20, E=9, k=3)
+    got = oracle.route_gaps(x, wr, d.k)
+    for t in range(d.T):
+        v = sorted((float(np.dot(val64(x[t]), val64(wr[e]))) for e in range(d.E)), reverse=True)
+        want = min(v[p] - v[p + 1] for p in range(d.k))
+        assert got[t] == pytest.approx(want, rel=1e-12, abs=1e-15)
+
+
+# ----------------------------------------------------------------------------- permutation
+@pytest.mark.parametrize("T,k,E", [(16, 2, 8), (128, 6, 64), (1, 1, 1), (0, 3, 4), (37, 5, 7)])
+def test_permute_invariants(T, k, E):
+    rs = np.random.default_rng(T * 31 + k)
+    idx = np.array([rs.permutation(E)[:k] for _ in range(T)], dtype=np.int32).reshape(T, k)
+    counts, offsets, perm, inv = oracle.permute(idx, E)
+    flat = idx.reshape(-1)
+    np.testing.assert_array_equal(counts, np.bincount(flat, minlength=E))
+    np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+    assert sorted(perm.tolist()) == list(range(T * k))
+    np.testing.assert_array_equal(inv[perm], np.arange(T * k))
+    # expert-major, then token-ascending: the stable sort of entries by expert
+    np.testing.assert_array_equal(perm, np.argsort(flat, kind="stable"))
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert np.all(flat[seg] == e)
+        assert np.all(np.diff(seg // max(k, 1)) > 0)
+
+
+def test_permute_rejects_out_of_range():
+    with pytest.raises(ValueError):
+        oracle.permute(np.array([[0, 4]], np.int32), 4)
+
+
+# ----------------------------------------------------------------------------- experts
+SIGMOID_2 = 0.8807970779778823   # 1/(1+e^-2)
+SIGMOID_HALF = 0.6224593312018546  # 1/(1+e^-0.5)
+
+
+def test_expert_closed_form_scalar():
+    # H = I = 1: E(x) = d * silu(g*x) * (u*x); gate and up swapped would give a different number
+    a, g, u, dd = 1.0, 2.0, 0.5, -1.5
+    wgu = bits(np.array([[[g], [u]]]))
+    wd = bits(np.array([[[dd]]]))
+    y = oracle.expert_rows(bits([[a]]), wgu, wd, [0], [0])
+    want = dd * (g * a * SIGMOID_2) * (u * a)
+    assert y[0, 0] == pytest.approx(want, rel=1e-15)
+    assert want == pytest.approx(-1.3211956169668235, rel=1e-15)
+    swapped = dd * (u * a * SIGMOID_HALF) * (g * a)
+    assert abs(y[0, 0] - swapped) > 0.1
+
+
+def dense_ffn(x64, wg, wu, wd):
+    """SwiGLU FFN in torch fp64: (silu(x Wg^T) * (x Wu^T)) Wd^T."""
+    return (F.silu(x64 @ wg.T) * (x64 @ wu.T)) @ wd.T
+
+
+def torch_layer(x, wr, wgu, wd, wsgu, wsd, k, S):
+    """The layer evaluated densely: every expert on every token, masked by the
+    top-k set; a different formulation from the oracle's per-token routing."""
+    X = torch.from_numpy(val64(x))
+    Wr = torch.from_numpy(val64(wr))
+    E = wr.shape[0]
+    I = wgu.shape[1] // 2
+    logits = X @ Wr.T
+    P = torch.softmax(logits, dim=-1)
+    mask = torch.zeros_like(P)
+    if k > 0:
+        mask.scatter_(1, torch.topk(logits, k, dim=-1).indices, 1.0)
+    out = torch.zeros_like(X)
+    for e in range(E):
+        G = torch.from_numpy(val64(wgu[e]))
+        Y = dense_ffn(X, G[:I], G[I:], torch.from_numpy(val64(wd[e])))
+        out += (mask[:, e] * P[:, e])[:, None] * Y
+    if S > 0:
+        G = torch.from_numpy(val64(wsgu))
+        D = torch.from_numpy(val64(wsd))
+        for s in range(S):
+            out += dense_ffn(X, G[s * I:(s + 1) * I], G[S * I + s * I:S * I + (s + 1) * I], D[:, s * I:(s + 1) * I])
+    return out.numpy()
+
+
+@pytest.mark.parametrize("shape", [dict(T=12, H=32, E=8, k=2, S=1, I=16),
+                                   dict(T=9, H=24, E=6, k=3, S=2, I=8),
+                                   dict(T=5, H=16, E=4, k=4, S=0, I=32)])
+def test_layer_vs_dense_torch(shape):
+    d, x, (wr, wgu, wd, wsgu, wsd) = tiny_problem(**shape, seed=11)
+    gaps = oracle.route_gaps(x, wr, d.k)
+    out, idx, p = oracle.moe_layer(x, wr, wgu, wd, wsgu, wsd, d.k, d.S)
+    ref = torch_layer(x, wr, wgu, wd, wsgu, wsd, d.k, d.S)
+    keep = gaps >= 1e-3
+    assert keep.sum() >= d.T // 2
+    # the oracle's gate uses float router scores (the kernel's precision); torch's are fp64
+    np.testing.assert_allclose(out[keep], ref[keep], rtol=1e-5, atol=1e-6)
+
+
+def test_layer_identical_experts_reduces_to_dense_ffn():
+    d, x, (wr, wgu, wd, wsgu, wsd) = tiny_problem(T=10, H=32, E=6, k=6, S=1, I=16, seed=5)
+    wgu[:] = wgu[0]
+    wd[:] = wd[0]
+    X = torch.from_numpy(val64(x))
+    G = torch.from_numpy(val64(wgu[0]))
+    f = dense_ffn(X, G[:16], G[16:], torch.from_numpy(val64(wd[0]))).numpy()
+    sh = oracle.shared_rows(x, wsgu, wsd, 1)
+    # k = E: the gate probabilities sum to one, so the routed part is exactly the dense FFN
+    out, _, _ = oracle.moe_layer(x, wr, wgu, wd, wsgu, wsd, 6, 1)
+    np.testing.assert_allclose(out - sh, f, rtol=1e-9, atol=1e-12)
+    # k < E: the routed part is (sum of the selected probabilities) x the dense FFN (no renormalisation)
+    out2, _, p2 = oracle.moe_layer(x, wr, wgu, wd, wsgu, wsd, 2, 1)
+    np.testing.assert_allclose(out2 - sh, p2.sum(axis=1)[:, None] * f, rtol=1e-9, atol=1e-12)
+    assert np.all(p2.sum(axis=1) < 1.0)
+
+
+def test_layer_special_cases():
+    d, x, (wr, wgu, wd, wsgu, wsd) = tiny_problem(T=6, H=16, E=1, k=1, S=2, I=8, seed=9)
+    # a single routed expert always has gate probability 1
+    out, idx, p = oracle.moe_layer(x, wr, wgu, wd, wsgu, wsd, 1, 2)
+    assert np.all(idx == 0) and np.allclose(p, 1.0)
+    routed = oracle.expert_rows(x, wgu, wd, np.arange(6), np.zeros(6, np.int32))
+    shared = oracle.shared_rows(x, wsgu, wsd, 2)
+    np.testing.assert_allclose(out, routed + shared, rtol=1e-12)
+    # no routed slot: the layer is its shared experts
+    out0, _, _ = oracle.moe_layer(x, wr, wgu, wd, wsgu, wsd, 0, 2)
+    np.testing.assert_allclose(out0, shared, rtol=1e-12)
+    # two shared experts of intermediate I equal one SwiGLU of intermediate 2I built by concatenation
+    X = torch.from_numpy(val64(x))
+    G = torch.from_numpy(val64(wsgu))
+    D = torch.from_numpy(val64(wsd))
+    cat = dense_ffn(X, G[:16], G[16:], D).numpy()
+    np.testing.assert_allclose(shared, cat, rtol=1e-9, atol=1e-12)
+
+
+def test_combine_closed_form():
+    T, k, H = 3, 2, 4
+    y_perm = np.arange(T * k * H, dtype=np.float32).reshape(T * k, H) / 8
+    inv = np.array([5, 0, 3, 1, 4, 2], np.int32)
+    w = np.array([[0.5, 0.25], [1.0, 0.0], [0.125, 2.0]], np.float32)
+    ysh = np.full((T, H), 10.0, np.float32)
+    out = oracle.combine(y_perm, inv, w, ysh, T, k)
+    want = np.stack([0.5 * y_perm[5] + 0.25 * y_perm[0] + 10,
+                     1.0 * y_perm[3] + 0.0 * y_perm[1] + 10,
+                     0.125 * y_perm[4] + 2.0 * y_perm[2] + 10])
+    np.testing.assert_array_equal(out, want)
+
+
+# ----------------------------------------------------------------------------- acceptance
+def brute_accept(logits, drafts):
+    """Committed tokens as greedy decoding writes them: g_0 .. g_L where L is the
+    longest prefix of drafts equal to the greedy tokens (np.argmax: first maximum)."""
+    g = np.argmax(synth.bf16_value(logits), axis=-1)
+    B, K = drafts.shape
+    alen = np.zeros(B, np.int32)
+    comm = -np.ones((B, K + 1), np.int32)
+    for b in range(B):
+        L = next(L for L in range(K, -1, -1) if all(drafts[b, i] == g[b, i] for i in range(L)))
+        alen[b] = L
+        comm[b, :L + 1] = g[b, :L + 1]
+    return g, alen, comm
+
+
+@pytest.mark.parametrize("K", [0, 1, 2, 3])
+def test_accept_exhaustive_tiny_vocab(K):
+    V = 4
+    rs = np.random.default_rng(K)
+    # values from a 3-level grid so that exact ties are common
+    lg = bits(rs.integers(-1, 2, size=(1, K + 1, V)).astype(np.float32))
+    tuples = list(itertools.product(range(-1, V + 1), repeat=K))      # includes ids outside [0,V)
+    drafts = np.array(tuples, np.int32).reshape(len(tuples), K)
+    logits = np.repeat(lg, len(tuples), axis=0)
+    g, alen, comm = oracle.accept(logits, drafts)
+    g2, alen2, comm2 = brute_accept(logits, drafts)
+    np.testing.assert_array_equal(g, g2)
+    np.testing.assert_array_equal(alen, alen2)
+    np.testing.assert_array_equal(comm, comm2)
+
+
+def test_accept_planted_greedy_tokens_and_torch_argmax():
+    for B, K, V, seed in [(4, 3, 1024, 0), (8, 2, 7, 1), (3, 1, 129_280, 2), (16, 3, 2, 3)]:
+        logits, planted = synth.verify_logits(B, K, V, seed)
+        g, _, _ = oracle.accept(logits, np.zeros((B, K), np.int32))
+        np.testing.assert_array_equal(g, planted)
+        t = torch.from_numpy(synth.bf16_value(logits).astype(np.float32))
+        np.testing.assert_array_equal(g, torch.argmax(t, dim=-1).numpy())
+
+
+def test_accept_all_match_gives_bonus_and_first_miss_gives_correction():
+    B, K, V = 5, 3, 50
+    logits, planted = synth.verify_logits(B, K, V, 7)
+    g, alen, comm = oracle.accept(logits, planted[:, :K])
+    assert np.all(alen == K)
+    np.testing.assert_array_equal(comm, planted)                     # K drafts + the bonus token
+    bad = planted[:, :K].copy()
+    bad[:, 0] = (bad[:, 0] + 1) % V
+    g, alen, comm = oracle.accept(logits, bad)
+    assert np.all(alen == 0)
+    np.testing.assert_array_equal(comm[:, 0], planted[:, 0])          # the correction token
+    assert np.all(comm[:, 1:] == -1)
+
+
+def toy_logits(prev2, prev1, V, table):
+    """Deterministic toy language model: logits depend on the last two tokens."""
+    return table[(prev2 * 131 + prev1 * 7) % table.shape[0]]
+
+
+@pytest.mark.parametrize("K", [1, 2, 3])
+def test_speculative_loop_equals_greedy_decoding(K):
+    """The pages' lossless claim: the committed text equals plain greedy decoding."""
+    V, n_tok = 13, 60
+    for seed in range(12):
+        rs = np.random.default_rng(100 * K + seed)
+        table = bits(rs.integers(-2, 3, size=(97, V)).astype(np.float32))    # many exact ties
+        # plain greedy decoding (first maximum)
+        seq = [1, 2]
+        while len(seq) < n_tok + 2:
+            row = synth.bf16_value(toy_logits(seq[-2], seq[-1], V, table))
+            seq.append(int(np.argmax(row)))
+        greedy = seq[2:]
+        # speculative: a corrupted greedy drafter proposes K tokens, the verifier scores K+1 positions
+        out = [1, 2]
+        steps = 0
+        while len(out) < n_tok + 2:
+            ctx = list(out)
+            drafts = []
+            for _ in range(K):
+                row = synth.bf16_value(toy_logits(ctx[-2], ctx[-1], V, table))
+                tok = int(np.argmax(row))
+                if rs.random() < 0.3:
+                    tok = int(rs.integers(0, V))
+                drafts.append(tok)
+                ctx.append(tok)
+            inputs = out[-2:] + drafts
+            lg = np.stack([toy_logits(inputs[j], inputs[j + 1], V, table) for j in range(K + 1)])[None]
+            _, alen, comm = oracle.accept(lg, np.array([drafts], np.int32))
+            out.extend(int(c) for c in comm[0, :alen[0] + 1])
+            steps += 1
+        assert out[2:2 + n_tok] == greedy[:n_tok]
+        assert steps < n_tok
+
+
+def test_tokens_per_step_closed_form_matches_pages():
+    with open(os.path.join(GOLDEN, "page_numbers.json")) as f:
+        pages = json.load(f)
+    a = pages["conditional_accept_k3"]["value"]
+    tau = 1 + a[0] + a[0] * a[1] + a[0] * a[1] * a[2]
+    assert tau == pytest.approx(pages["tau_k3"]["value"], abs=0.005)
+    assert (tau - 1) / 3 == pytest.approx(pages["acceptance_rate_k3"]["value"], abs=0.002)
+    # Monte Carlo through the oracle with the workload's draft generator
+    B, K, V = 200_000, 3, 8
+    logits, planted = synth.verify_logits(B, K, V, 1234)
+    drafts = synth.draft_tokens(planted, V, a, 1234)
+    _, alen, _ = oracle.accept(logits, drafts)
+    committed = alen + 1
+    sigma = committed.std()
+    assert committed.mean() == pytest.approx(tau, abs=4 * sigma / math.sqrt(B))
+    # committed-count distribution: P(n) = prod a_{<n-1} (1 - a_{n-1}), P(K+1) = prod a
+    pn = [1 - a[0], a[0] * (1 - a[1]), a[0] * a[1] * (1 - a[2]), a[0] * a[1] * a[2]]
+    hist = np.bincount(committed, minlength=5)[1:] / B
+    np.testing.assert_allclose(hist, pn, atol=0.005)
+
+
+# ----------------------------------------------------------------------------- rmsnorm
+def test_rmsnorm_residual_closed_form_and_torch():
+    T, H = 4, 64
+    x = bits(np.full((T, H), 1.5))
+    y = bits(np.full((T, H), 0.5))
+    xn, hn = oracle.rmsnorm_residual(x, y, eps=1e-6)
+    assert np.all(xn == 2.0)
+    np.testing.assert_allclose(hn, 2.0 / math.sqrt(4.0 + 1e-6), rtol=1e-14)
+    rs = np.random.default_rng(0)
+    x = bits(rs.standard_normal((T, H)))
+    y = bits(rs.standard_normal((T, H)) * 0.1)
+    xn, hn = oracle.rmsnorm_residual(x, y, eps=1e-6)
+    np.testing.assert_allclose(xn, val64(bits(val64(x) + val64(y))), rtol=0, atol=0)
+    ref = F.rms_norm(torch.from_numpy(xn), (H,), eps=1e-6).numpy()
+    np.testing.assert_allclose(hn, ref, rtol=1e-12)
