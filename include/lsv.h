@@ -1,0 +1,178 @@
+/*
+ * lsv.h -- C ABI of the GB300 (sm_103a) FastMTP verification step.
+ *
+ * The method (jina-ocr-v1; kg.zhiyong.dev "Jina AI's jina-ocr-v1 Is Selling
+ * Throughput", section "The speed comes from three layers working together";
+ * evolve.pub review "Summary", "Scope & Claims" (Section 3.1, Eq. 2)):
+ * B sequences each carry K drafted tokens; the decoder verifies all B*(K+1)
+ * positions in one pass.  Every decoder layer's FFN is a DeepSeek-style MoE
+ * (64 routed experts, top-6 routing, 2 shared experts), and a greedy rule then
+ * commits the longest draft prefix that matches the verifier's greedy tokens
+ * plus one correction (or, when every draft matches, a bonus) token, so the
+ * committed text equals plain greedy decoding.
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers (memory the caller allocated on
+ *     the current CUDA device), contiguous, row-major, 16-byte aligned unless a
+ *     pointer is documented as optional and passed as NULL.
+ *   - bf16 tensors are passed as `const void*` / `void*` holding IEEE bfloat16.
+ *   - The caller owns all memory.  The library allocates no device memory; it
+ *     keeps one device error word per device and nothing else.
+ *   - Work is enqueued asynchronously on `stream` (NULL = the legacy default
+ *     stream).  Argument errors are returned synchronously BEFORE any launch,
+ *     with outputs untouched.  Errors found by kernels (an index out of range,
+ *     a bounded wait that ran out) are written to the device error word; read
+ *     it with lsv_get_device_error.
+ *   - Entry points are thread-compatible: concurrent calls must use distinct
+ *     workspaces.
+ */
+#ifndef LSV_H_
+#define LSV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *lsv_stream;
+
+typedef enum {
+  LSV_OK = 0,
+  LSV_ERR_INVALID_ARG = 1,  /* NULL pointer, negative or inconsistent size */
+  LSV_ERR_UNSUPPORTED = 2,  /* shape outside the supported set (see each call) */
+  LSV_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+  LSV_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the queried size */
+  LSV_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+  LSV_ERR_TIMEOUT = 6,      /* device: a bounded wait ran out (kernel unwound, outputs undefined) */
+  LSV_ERR_DEVICE_INDEX = 7  /* device: an index read from memory was out of range (outputs undefined) */
+} lsv_status;
+
+/* One MoE FFN layer: T tokens of width H; E routed experts of which each token
+ * uses the top k; S shared experts; every expert is a SwiGLU of intermediate I.
+ * Supported: T >= 0; H % 64 == 0, 64 <= H <= 16384; I % 64 == 0, 64 <= I;
+ * S*I <= 16384; 1 <= E <= 256; 0 <= k <= min(E, 8); 0 <= S <= 8. */
+typedef struct {
+  int32_t T, H, E, k, S, I;
+} lsv_moe_shape;
+
+/* Expert weights (bf16, device).
+ *   w_router   [E, H]
+ *   w_gate_up  [E, 2I, H]  rows 0..I-1 of expert e: gate projection, rows I..2I-1: up projection
+ *   w_down     [E, H, I]
+ *   ws_gate_up [2*S*I, H]  rows s*I..s*I+I-1: gate of shared expert s; rows S*I+s*I..: its up
+ *   ws_down    [H, S*I]    columns s*I..s*I+I-1: down projection of shared expert s
+ * Expert e computes  y = W_down,e (silu(W_gate,e x) * (W_up,e x)),
+ * silu(z) = z / (1 + exp(-z)); no biases. */
+typedef struct {
+  const void *w_router;
+  const void *w_gate_up;
+  const void *w_down;
+  const void *ws_gate_up;
+  const void *ws_down;
+} lsv_moe_weights;
+
+/* Bytes of workspace moe_verify_layer / moe_grouped_ffn / moe_permute need for
+ * `shape` (a multiple of 256).  Returns 0 for an unsupported shape. */
+size_t lsv_workspace_size(const lsv_moe_shape *shape);
+
+/* Router: logits[t,e] = sum_h x[t,h] W_r[e,h] (fp32 accumulation in increasing
+ * h); gate p = softmax over all E experts in fp32 (NOT renormalised over the
+ * selection); the k experts with the largest logits in descending order, ties
+ * to the lower expert index.
+ * (kg.zhiyong.dev, "The speed comes from three layers working together":
+ *  64 routed experts, top-6 routing.)
+ *   x         [T, H] bf16          in
+ *   w_router  [E, H] bf16          in
+ *   topk_idx  [T, k] int32         out
+ *   topk_w    [T, k] fp32          out  p of the selected experts
+ *   logits_opt[T, E] fp32 or NULL  out */
+lsv_status moe_route(const void *x, const void *w_router, const lsv_moe_shape *shape, int32_t *topk_idx,
+                     float *topk_w, float *logits_opt, lsv_stream stream);
+
+/* Expert-contiguous order of the T*k (token, slot) pairs (entry i = t*k + s):
+ *   counts [E]     pairs per expert
+ *   offsets[E+1]   exclusive prefix sum, offsets[E] = T*k
+ *   perm_src[T*k]  entries grouped by expert, each group in increasing token order
+ *   inv   [T*k]    inverse: inv[perm_src[r]] = r
+ * Deterministic (no atomics decide any position).  An index outside [0,E)
+ * sets LSV_ERR_DEVICE_INDEX on the device.  ws: lsv_workspace_size(shape). */
+lsv_status moe_permute(const int32_t *topk_idx, const lsv_moe_shape *shape, int32_t *counts, int32_t *offsets,
+                       int32_t *perm_src, int32_t *inv, void *ws, size_t ws_bytes, lsv_stream stream);
+
+/* Grouped SwiGLU experts on the permuted pairs plus the shared experts:
+ *   y_perm  [T*k, H] fp32  y_perm[r] = E_e(x[perm_src[r] / k]) for r in expert e's segment
+ *   y_shared[T, H]   fp32  sum over shared experts s of S_s(x[t])  (ignored when S == 0; may be NULL then)
+ * bf16 tensor-core products with fp32 accumulation; the SwiGLU activation is
+ * rounded to bf16 before the down projection.  counts/offsets as from
+ * moe_permute.  ws: lsv_workspace_size(shape). */
+lsv_status moe_grouped_ffn(const void *x, const int32_t *perm_src, const int32_t *offsets, const int32_t *counts,
+                           const lsv_moe_weights *weights, const lsv_moe_shape *shape, float *y_perm,
+                           float *y_shared, void *ws, size_t ws_bytes, lsv_stream stream);
+
+/* Gate-weighted combine:
+ *   out[t,:] = sum_{s<k} topk_w[t,s] * y_perm[inv[t*k+s],:] + y_shared[t,:]   (bf16 out)
+ * summed in fp32 in slot order, then the shared term; y_shared may be NULL
+ * (no shared experts). */
+lsv_status moe_combine(const float *y_perm, const int32_t *inv, const float *topk_w, const float *y_shared,
+                       const lsv_moe_shape *shape, void *out, lsv_stream stream);
+
+/* The whole MoE layer: route, permute, grouped experts, combine.
+ *   x   [T, H] bf16 in;  out [T, H] bf16 out
+ *   topk_idx_opt [T, k] int32 and counts_opt [E] int32: optional copies of the routing.
+ * ws: lsv_workspace_size(shape). */
+lsv_status moe_verify_layer(const void *x, const lsv_moe_weights *weights, const lsv_moe_shape *shape, void *out,
+                            int32_t *topk_idx_opt, int32_t *counts_opt, void *ws, size_t ws_bytes,
+                            lsv_stream stream);
+
+/* Bytes of workspace spec_verify_accept needs (a multiple of 256). */
+size_t spec_verify_workspace_size(int32_t B, int32_t K, int32_t V);
+
+/* Greedy verification (kg.zhiyong.dev, "Why FastMTP fits OCR particularly
+ * well": bonus token when all drafts match; committed text matches ordinary
+ * greedy decoding; evolve.pub review, Section 3.1 / Eq. 2).
+ *   logits [B, K+1, V] bf16: row j is the verifier's prediction for the
+ *          position after input j (input 0 = last committed token, input j = draft j)
+ *   drafts [B, K] int32
+ *   g[b,j]        = the smallest index attaining the row maximum (finite logits assumed)
+ *   accept_len[b] = largest L <= K with drafts[b,i] == g[b,i] for all i < L
+ *   committed[b]  = drafts[b,0..L-1], g[b,L], then -1 (K+1 entries)
+ *   argmax_opt [B, K+1] int32 or NULL: g
+ * A draft outside [0,V) is a mismatch, not an error.  1 <= K+1 <= 64,
+ * 1 <= V < 2^31, B >= 0.  ws: spec_verify_workspace_size(B,K,V). */
+lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t B, int32_t K, int32_t V,
+                              int32_t *argmax_opt, int32_t *accept_len, int32_t *committed, void *ws,
+                              size_t ws_bytes, lsv_stream stream);
+
+/* Residual update and normalisation between stacked layers:
+ *   x[t,:] <- bf16(x[t,:] + y[t,:]);   h[t,:] = bf16(x[t,:] / sqrt(mean(x[t,:]^2) + eps))
+ * x [T,H] bf16 in/out, y [T,H] bf16 in, h [T,H] bf16 out; fp32 arithmetic;
+ * unit norm weight. */
+lsv_status rmsnorm_residual(void *x, const void *y, void *h, int32_t T, int32_t H, float eps,
+                            lsv_stream stream);
+
+/* Synchronise `stream`, return the current device's error word in *code_out
+ * (an lsv_status value, 0 if none) and clear it. */
+lsv_status lsv_get_device_error(int32_t *code_out, lsv_stream stream);
+
+/* Upper bound, in nanoseconds, of every bounded wait inside the kernels
+ * (default 2e9).  Process-wide; takes effect for launches after the call. */
+lsv_status lsv_set_wait_limit_ns(uint64_t ns);
+
+/* Launch one CTA that waits on a flag nothing ever sets, using the same
+ * bounded wait as the kernels; it must end by writing LSV_ERR_TIMEOUT to the
+ * error word.  For testing the failure path without faulting the GPU. */
+lsv_status lsv_selftest_wait_timeout(uint64_t limit_ns, lsv_stream stream);
+
+const char *lsv_status_string(lsv_status status);
+
+/* 100 * major + minor. */
+int32_t lsv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSV_H_ */

@@ -1,0 +1,156 @@
+"""Python surface of the C ABI: the same entry points, taking torch CUDA tensors.
+
+Each function checks dtypes/devices, passes data pointers and the current
+CUDA stream to liblsv.so, and returns the output tensors.  Every step of the
+computation runs in the library's kernels.  Workspaces are passed explicitly
+(the library allocates nothing); `workspace(...)` sizes one.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _ffi
+from ._ffi import MoeShape, MoeWeights, check
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def shape(T, H, E, k, S, I) -> MoeShape:
+    return MoeShape(T, H, E, k, S, I)
+
+
+def weights(w_router, w_gate_up, w_down, ws_gate_up=None, ws_down=None) -> MoeWeights:
+    for n, t in (("w_router", w_router), ("w_gate_up", w_gate_up), ("w_down", w_down),
+                 ("ws_gate_up", ws_gate_up), ("ws_down", ws_down)):
+        _need(t, torch.bfloat16, n)
+    return MoeWeights(*(t.data_ptr() if t is not None else None
+                        for t in (w_router, w_gate_up, w_down, ws_gate_up, ws_down)))
+
+
+def workspace_size(sh: MoeShape) -> int:
+    n = _ffi.load().lsv_workspace_size(ctypes.byref(sh))
+    if n == 0:
+        raise ValueError("unsupported MoE shape")
+    return int(n)
+
+
+def workspace(sh: MoeShape, device=None) -> torch.Tensor:
+    return torch.empty(workspace_size(sh), dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_route(x, w_router, k, topk_idx=None, topk_w=None, logits=None, stream=None):
+    _need(x, torch.bfloat16, "x"); _need(w_router, torch.bfloat16, "w_router")
+    T, H = x.shape
+    E = w_router.shape[0]
+    sh = MoeShape(T, H, E, k, 0, 64)
+    topk_idx = torch.empty((T, k), dtype=torch.int32, device=x.device) if topk_idx is None else topk_idx
+    topk_w = torch.empty((T, k), dtype=torch.float32, device=x.device) if topk_w is None else topk_w
+    check("moe_route", _ffi.load().moe_route(_ptr(x), _ptr(w_router), ctypes.byref(sh), _ptr(topk_idx),
+                                             _ptr(topk_w), _ptr(logits), _stream(stream)))
+    return topk_idx, topk_w
+
+
+def moe_permute(topk_idx, E, ws, H=64, S=0, I=64, stream=None):
+    _need(topk_idx, torch.int32, "topk_idx")
+    T, k = topk_idx.shape
+    sh = MoeShape(T, H, E, k, S, I)
+    dev = topk_idx.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    check("moe_permute", _ffi.load().moe_permute(_ptr(topk_idx), ctypes.byref(sh), _ptr(counts), _ptr(offsets),
+                                                 _ptr(perm), _ptr(inv), _ptr(ws), ws.numel(), _stream(stream)))
+    return counts, offsets, perm, inv
+
+
+def moe_grouped_ffn(x, perm, offsets, counts, w: MoeWeights, sh: MoeShape, ws, y_perm=None, y_shared=None,
+                    stream=None):
+    _need(x, torch.bfloat16, "x")
+    dev = x.device
+    if y_perm is None:
+        y_perm = torch.empty((sh.T * sh.k, sh.H), dtype=torch.float32, device=dev)
+    if y_shared is None and sh.S > 0:
+        y_shared = torch.empty((sh.T, sh.H), dtype=torch.float32, device=dev)
+    check("moe_grouped_ffn", _ffi.load().moe_grouped_ffn(
+        _ptr(x), _ptr(perm), _ptr(offsets), _ptr(counts), ctypes.byref(w), ctypes.byref(sh), _ptr(y_perm),
+        _ptr(y_shared), _ptr(ws), ws.numel(), _stream(stream)))
+    return y_perm, y_shared
+
+
+def moe_combine(y_perm, inv, topk_w, y_shared, sh: MoeShape, out=None, stream=None):
+    out = torch.empty((sh.T, sh.H), dtype=torch.bfloat16, device=y_perm.device) if out is None else out
+    check("moe_combine", _ffi.load().moe_combine(_ptr(y_perm), _ptr(inv), _ptr(topk_w), _ptr(y_shared),
+                                                 ctypes.byref(sh), _ptr(out), _stream(stream)))
+    return out
+
+
+def moe_verify_layer(x, w: MoeWeights, sh: MoeShape, ws, out=None, topk_idx=None, counts=None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    out = torch.empty((sh.T, sh.H), dtype=torch.bfloat16, device=x.device) if out is None else out
+    check("moe_verify_layer", _ffi.load().moe_verify_layer(
+        _ptr(x), ctypes.byref(w), ctypes.byref(sh), _ptr(out), _ptr(topk_idx), _ptr(counts), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out
+
+
+def spec_verify_workspace(B, K, V, device=None) -> torch.Tensor:
+    n = _ffi.load().spec_verify_workspace_size(B, K, V)
+    if n == 0:
+        raise ValueError("unsupported verify shape")
+    return torch.empty(int(n), dtype=torch.uint8, device=device or "cuda")
+
+
+def spec_verify_accept(logits, drafts, ws, argmax=None, accept_len=None, committed=None, stream=None):
+    _need(logits, torch.bfloat16, "logits"); _need(drafts, torch.int32, "drafts")
+    B, K1, V = logits.shape
+    K = K1 - 1
+    dev = logits.device
+    accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
+    committed = torch.empty((B, K1), dtype=torch.int32, device=dev) if committed is None else committed
+    check("spec_verify_accept", _ffi.load().spec_verify_accept(
+        _ptr(logits), _ptr(drafts), B, K, V, _ptr(argmax), _ptr(accept_len), _ptr(committed), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return accept_len, committed
+
+
+def rmsnorm_residual(x, y, h=None, eps=1e-6, stream=None):
+    _need(x, torch.bfloat16, "x"); _need(y, torch.bfloat16, "y")
+    T, H = x.shape
+    h = torch.empty_like(x) if h is None else h
+    check("rmsnorm_residual", _ffi.load().rmsnorm_residual(_ptr(x), _ptr(y), _ptr(h), T, H, eps, _stream(stream)))
+    return h
+
+
+def get_device_error(stream=None) -> int:
+    v = ctypes.c_int32(0)
+    check("lsv_get_device_error", _ffi.load().lsv_get_device_error(ctypes.byref(v), _stream(stream)))
+    return int(v.value)
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    check("lsv_set_wait_limit_ns", _ffi.load().lsv_set_wait_limit_ns(ns))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    check("lsv_selftest_wait_timeout", _ffi.load().lsv_selftest_wait_timeout(limit_ns, _stream(stream)))

@@ -1,0 +1,186 @@
+// accept.cu -- vocabulary-wide greedy token and prefix acceptance.
+//
+// For every verified row (b, j) the greedy token g[b,j] is the smallest index
+// attaining the row maximum.  accept_len[b] is the length of the longest
+// prefix of drafts that equals g[b,0..]; the committed tokens are that prefix
+// followed by g[b, accept_len] -- the correction at the first mismatch, or the
+// bonus token when every draft matched.  This makes the committed text
+// identical to greedy decoding (kg.zhiyong.dev, "Why FastMTP fits OCR
+// particularly well"; evolve.pub review, Section 3.1 / Eq. 2).
+//
+// Phase 1 streams the logits once: each CTA owns a chunk of one row, loads it
+// with 16-byte non-allocating loads (8 bf16 each, several in flight per
+// thread) and writes the chunk's (max, first index).  Phase 2 (one warp per
+// sequence) reduces the chunk partials in index order and applies the rule.
+// No atomics decide anything, so the result is deterministic.
+#include <limits.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lsv {
+namespace {
+
+constexpr int kAccThreads = 256;
+constexpr int kUnroll = 4;
+constexpr int kChunkQuantum = kAccThreads * 8;  // elements covered by one 16-B load per thread
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// (value desc, index asc) maximum
+__device__ __forceinline__ void better(float v, int i, float& bv, int& bi) {
+  if (v > bv || (v == bv && i < bi)) {
+    bv = v;
+    bi = i;
+  }
+}
+
+__device__ __forceinline__ void scan8(const uint4& q, int base, float& bv, int& bi) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16);
+    const float hi = __uint_as_float(w[i] & 0xFFFF0000u);
+    if (lo > bv) { bv = lo; bi = base + 2 * i; }      // increasing index: strict > keeps the first
+    if (hi > bv) { bv = hi; bi = base + 2 * i + 1; }
+  }
+}
+
+__global__ void __launch_bounds__(kAccThreads) argmax_partial_kernel(const bf16* __restrict__ logits, int V,
+                                                                     int chunk, int nchunk, int vec_ok,
+                                                                     float* __restrict__ pv,
+                                                                     int* __restrict__ pi) {
+  const int r = blockIdx.x, c = blockIdx.y;
+  const bf16* row = logits + (size_t)r * V;
+  const int begin = c * chunk;
+  const int end = min(V, begin + chunk);
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  if (vec_ok) {
+    // every thread walks its vectors in increasing index order
+    const int n8 = (end - begin) >> 3;
+    const uint4* p = reinterpret_cast<const uint4*>(row + begin);
+    int j = threadIdx.x;
+    for (; j + (kUnroll - 1) * kAccThreads < n8; j += kUnroll * kAccThreads) {
+      uint4 q[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) q[u] = ld_stream_v4(p + j + u * kAccThreads);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) scan8(q[u], begin + 8 * (j + u * kAccThreads), bv, bi);
+    }
+    for (; j < n8; j += kAccThreads) scan8(ld_stream_v4(p + j), begin + 8 * j, bv, bi);
+    for (int e = begin + 8 * n8 + threadIdx.x; e < end; e += kAccThreads)
+      better(__bfloat162float(row[e]), e, bv, bi);
+  } else {
+    for (int e = begin + threadIdx.x; e < end; e += kAccThreads) {
+      const float f = __bfloat162float(row[e]);
+      if (f > bv) { bv = f; bi = e; }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    better(ov, oi, bv, bi);
+  }
+  __shared__ float sv[kAccThreads / 32];
+  __shared__ int si[kAccThreads / 32];
+  if ((threadIdx.x & 31) == 0) {
+    sv[threadIdx.x >> 5] = bv;
+    si[threadIdx.x >> 5] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kAccThreads / 32; ++w) better(sv[w], si[w], bv, bi);
+    pv[(size_t)r * nchunk + c] = bv;
+    pi[(size_t)r * nchunk + c] = bi;
+  }
+}
+
+constexpr int kFinWarps = 4;
+
+__global__ void __launch_bounds__(kFinWarps * 32) accept_finalize_kernel(
+    const float* __restrict__ pv, const int* __restrict__ pi, int nchunk, const int32_t* __restrict__ drafts,
+    int B, int K, int32_t* __restrict__ argmax, int32_t* __restrict__ accept_len,
+    int32_t* __restrict__ committed) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kFinWarps + (threadIdx.x >> 5);
+  if (b >= B) return;
+  __shared__ int g[kFinWarps][kMaxVerifyRows];
+  int* gb = g[threadIdx.x >> 5];
+  for (int j = 0; j <= K; ++j) {
+    const size_t r = (size_t)b * (K + 1) + j;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int c = lane; c < nchunk; c += 32) better(pv[r * nchunk + c], pi[r * nchunk + c], bv, bi);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      better(ov, oi, bv, bi);
+    }
+    if (lane == 0) {
+      gb[j] = bi;
+      if (argmax) argmax[r] = bi;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    int L = 0;
+    while (L < K && drafts[(size_t)b * K + L] == gb[L]) ++L;
+    accept_len[b] = L;
+    int32_t* cm = committed + (size_t)b * (K + 1);
+    for (int i = 0; i < L; ++i) cm[i] = drafts[(size_t)b * K + i];
+    cm[L] = gb[L];
+    for (int i = L + 1; i <= K; ++i) cm[i] = -1;
+  }
+}
+
+int chunk_elems(int R, int V, int num_sms) {
+  // aim for about 8 resident CTAs per SM in one wave; at least one quantum per CTA
+  const long long target = (long long)num_sms * 8;
+  long long per = ((long long)V * R + target - 1) / target;
+  per = ((per + kChunkQuantum - 1) / kChunkQuantum) * kChunkQuantum;
+  if (per < kChunkQuantum) per = kChunkQuantum;
+  if (per > V) per = ((V + 7) / 8) * 8;
+  if (per < 8) per = 8;
+  return (int)per;
+}
+
+}  // namespace
+
+size_t accept_ws_bytes(int B, int K, int V, int num_sms) {
+  const int R = B * (K + 1);
+  if (R == 0) return 256;
+  const int chunk = chunk_elems(R, V, num_sms);
+  const size_t nchunk = (V + chunk - 1) / chunk;
+  const size_t one = ((size_t)R * nchunk * 4 + 255) / 256 * 256;
+  return 2 * one;
+}
+
+cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int K, int V, int32_t* argmax,
+                          int32_t* accept_len, int32_t* committed, void* ws, const DeviceCtx& dc,
+                          cudaStream_t s) {
+  const int R = B * (K + 1);
+  if (R == 0) return cudaSuccess;
+  const int chunk = chunk_elems(R, V, dc.num_sms);
+  const int nchunk = (V + chunk - 1) / chunk;
+  const size_t one = ((size_t)R * nchunk * 4 + 255) / 256 * 256;
+  float* pv = reinterpret_cast<float*>(ws);
+  int* pi = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + one);
+  const int vec_ok = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+  argmax_partial_kernel<<<dim3(R, nchunk), kAccThreads, 0, s>>>(logits, V, chunk, nchunk, vec_ok, pv, pi);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  accept_finalize_kernel<<<(B + kFinWarps - 1) / kFinWarps, kFinWarps * 32, 0, s>>>(pv, pi, nchunk, drafts, B, K,
+                                                                                     argmax, accept_len, committed);
+  return cudaGetLastError();
+}
+
+}  // namespace lsv

@@ -1,0 +1,572 @@
+// ffn.cu -- grouped SwiGLU experts (routed + shared) on tcgen05 tensor cores.
+//
+// Expert e:  y = W_down,e ( silu(W_gate,e x) * (W_up,e x) ),  silu(z) = z / (1 + e^-z)
+// (DeepSeek-style MoE FFN of the jina-ocr-v1 decoder: 64 routed experts, top-6,
+// two shared experts; kg.zhiyong.dev, section "The speed comes from three
+// layers working together").
+//
+// Groups: g < E is routed expert g, fed by its segment of the permuted token
+// rows; g == E (when S > 0) is the S shared experts taken together as one
+// SwiGLU of intermediate S*I (gate rows and up rows are concatenated in the
+// weight layout, and the S down matrices sit side by side), fed by every token.
+//
+// Orientation ("swap AB"): the MMA's M side is 128 weight rows and its N side
+// is up to BN tokens, so one weight tile is streamed from HBM exactly once per
+// token tile; at decode sizes (about 12 tokens per expert) every expert's
+// weights are read once in total.  Both operands are K-major in shared memory
+// with the 128-byte swizzle, loaded by TMA.
+//
+//   gate/up item (g, token tile, 64 features f0..f0+63):
+//     A = [gate rows f0..f0+63 ; up rows f0..f0+63]  (two 64-row TMA boxes)
+//     D[128 x n] in TMEM: lanes 0-63 gate, lanes 64-127 up
+//     epilogue: act[row, f] = bf16( silu(gate) * up )
+//   down item (g, token tile, 128 outputs h0..h0+127):
+//     A = W_down rows h0..h0+127, B = act rows;  y[row, h] = D (fp32)
+//
+// One persistent CTA per SM, warp-specialised: warp 0 issues TMA, warp 1
+// allocates TMEM and issues tcgen05.mma (one thread), warps 2-5 drain TMEM.
+// A STAGES-deep shared-memory ring decouples loads from MMAs, and two TMEM
+// accumulators decouple MMAs from the epilogue.  Items are dealt round-robin:
+// every gate/up item precedes every down item in the global order, and a down
+// item waits (bounded) on a per-group counter of finished gate/up items, so
+// the wait always ends: a CTA finishes all of its gate/up items before it
+// reaches any down item.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lsv {
+namespace {
+
+constexpr int kFfnThreads = 192;         // 6 warps
+constexpr int kEpiThreads = 128;         // warps 2..5
+constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
+constexpr int kXchStride = 17;           // padded row of the gate/up exchange buffer
+
+struct FfnParams {
+  int T, H, E, k, S, I, G;
+  const int32_t* offsets;  // [E+1]
+  const int32_t* table;    // tile table (see internal.h)
+  int* done;               // [G]
+  bf16* act;               // [T*k, I]
+  bf16* act_sh;            // [T, S*I]
+  float* y_perm;           // [T*k, H]
+  float* y_sh;             // [T, H]
+  int* err;
+  uint64_t wait_ns;
+};
+
+struct FfnMaps {
+  CUtensorMap wgu;     // [E*2I, H]   box 64 x 64
+  CUtensorMap wsgu;    // [2SI, H]    box 64 x 64
+  CUtensorMap wd;      // [E*H, I]    box 64 x 128
+  CUtensorMap wsd;     // [H, SI]     box 64 x 128
+  CUtensorMap xperm;   // [T*k, H]    box 64 x BN
+  CUtensorMap x;       // [T, H]      box 64 x BN
+  CUtensorMap act;     // [T*k, I]    box 64 x BN
+  CUtensorMap act_sh;  // [T, SI]     box 64 x BN
+};
+
+struct Item {
+  int gu;    // 1: gate/up, 0: down
+  int g;     // group
+  int ft;    // feature tile (64 features for gate/up, 128 outputs for down)
+  int row0;  // first token row of the tile in the group's row space
+  int cnt;   // valid token rows in the tile (1..BN)
+  int nk;    // 64-wide K chunks
+  int need;  // gate/up items of group g (for a down item's dependency)
+};
+
+template <int BN>
+__device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
+  const int* tb = p.table;
+  const int G = p.G;
+  const int n_gu = tb[0];
+  Item m;
+  m.gu = it < n_gu;
+  const int* starts = m.gu ? tb + 8 : tb + 8 + G + 1;
+  const int local_it = m.gu ? it : it - n_gu;
+  int lo = 0, hi = G - 1;  // largest g with starts[g] <= local_it
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (starts[mid] <= local_it) lo = mid; else hi = mid - 1;
+  }
+  m.g = lo;
+  const bool routed = m.g < p.E;
+  const int inter = routed ? p.I : p.S * p.I;
+  const int nft = m.gu ? inter / 64 : (p.H + 127) / 128;
+  const int local = local_it - starts[m.g];
+  const int tt = local / nft;
+  m.ft = local - tt * nft;
+  int seg0, segn;
+  if (routed) {
+    seg0 = p.offsets[m.g];
+    segn = p.offsets[m.g + 1] - seg0;
+  } else {
+    seg0 = 0;
+    segn = p.T;
+  }
+  m.row0 = seg0 + tt * BN;
+  m.cnt = min(BN, segn - tt * BN);
+  m.nk = m.gu ? p.H / 64 : inter / 64;
+  m.need = tb[8 + m.g + 1] - tb[8 + m.g];
+  return m;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+template <int BN, int STAGES>
+struct Smem {
+  static constexpr int kStageBytes = kATileBytes + BN * 128;
+  static constexpr int kRing = STAGES * kStageBytes;
+  static constexpr int kXch = 64 * kXchStride * 4;
+  static constexpr int kBars = (2 * STAGES + 5) * 8;
+  static constexpr int kTotal = 1024 /*alignment slack*/ + kRing + kXch + kBars + 16;
+  static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256) ? 256 : 512;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_constant__ FfnMaps maps,
+                                                              const FfnParams p) {
+  using SM = Smem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* xch = reinterpret_cast<float*>(smem + SM::kRing);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kRing + SM::kXch);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* final_bar = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiThreads);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, SM::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_items = p.table[0] + p.table[1];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const Item m = decode_item<BN>(it, p);
+        const bool routed = m.g < p.E;
+        if (!m.gu) {
+          if (!wait_counter_geq(&p.done[m.g], m.need, p.wait_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        const CUtensorMap* amap = m.gu ? (routed ? &maps.wgu : &maps.wsgu) : (routed ? &maps.wd : &maps.wsd);
+        const CUtensorMap* bmap = m.gu ? (routed ? &maps.xperm : &maps.x) : (routed ? &maps.act : &maps.act_sh);
+        int arow0, arow1 = 0;
+        if (m.gu) {
+          const int inter = routed ? p.I : p.S * p.I;
+          const int gbase = routed ? m.g * 2 * p.I : 0;
+          arow0 = gbase + m.ft * 64;
+          arow1 = gbase + inter + m.ft * 64;
+        } else {
+          arow0 = (routed ? m.g * p.H : 0) + m.ft * 128;
+        }
+        for (int kc = 0; kc < m.nk; ++kc) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          uint8_t* a_s = smem + stage * SM::kStageBytes;
+          uint8_t* b_s = a_s + kATileBytes;
+          mbar_arrive_expect_tx(&full[stage], kATileBytes + BN * 128);
+          if (m.gu) {
+            tma_load_2d(a_s, amap, &full[stage], kc * 64, arow0, pol_w);
+            tma_load_2d(a_s + kATileBytes / 2, amap, &full[stage], kc * 64, arow1, pol_w);
+          } else {
+            tma_load_2d(a_s, amap, &full[stage], kc * 64, arow0, pol_w);
+          }
+          tma_load_2d(b_s, bmap, &full[stage], kc * 64, m.row0, pol_x);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        __threadfence_block();
+        mbar_arrive(&full[stage]);  // wake the MMA issuer so that it sees the abort
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const Item m = decode_item<BN>(it, p);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_ns)) {
+          set_error(p.err, kErrTimeout);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const int n_mma = max(16, (m.cnt + 15) & ~15);
+        const uint32_t idesc = idesc_bf16_f32(128, n_mma);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kc = 0; kc < m.nk; ++kc) {
+          if (!mbar_wait(&full[stage], phase, p.wait_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_s = smem_u32(smem + stage * SM::kStageBytes);
+          const uint32_t b_s = a_s + kATileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d_tmem, sdesc_kmajor_sw128(a_s + kk * 32), sdesc_kmajor_sw128(b_s + kk * 32), idesc,
+                      (kc | kk) ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        __threadfence_block();
+        mbar_arrive(&tfull[acc]);  // wake the epilogue so that it sees the abort
+      }
+      // every MMA issued by this thread has completed before TMEM is released
+      umma_commit(final_bar);
+      if (!mbar_wait(final_bar, 0, p.wait_ns)) set_error(p.err, kErrTimeout);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const Item m = decode_item<BN>(it, p);
+      const bool got = mbar_wait(&tfull[acc], acc_phase, p.wait_ns);
+      if (!got) set_error(p.err, kErrTimeout);
+      // all four epilogue warps take the same decision, so their named barriers stay matched
+      if (named_bar_red_or(1, kEpiThreads, !got || *abort_flag)) break;
+      tc_fence_after_sync();
+      const bool routed = m.g < p.E;
+      const int nrows_out = routed ? p.T * p.k : p.T;
+      const int n_mma = max(16, (m.cnt + 15) & ~15);
+      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      if (m.gu) {
+        bf16* out = routed ? p.act : p.act_sh;
+        const int ld = routed ? p.I : p.S * p.I;
+        const int f = m.ft * 64 + (q & 1) * 32 + lane;
+        float* xrow = xch + ((q & 1) * 32 + lane) * kXchStride;
+        for (int c0 = 0; c0 < n_mma; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(t_row + c0, r);
+          tmem_ld_wait();
+          if (q >= 2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xrow[j] = __uint_as_float(r[j]);
+          }
+          named_bar_sync(1, kEpiThreads);
+          if (q < 2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < m.cnt && m.row0 + col < nrows_out) {
+                const float hv = silu(__uint_as_float(r[j])) * xrow[j];
+                out[(size_t)(m.row0 + col) * ld + f] = __float2bfloat16_rn(hv);
+              }
+            }
+          }
+          named_bar_sync(1, kEpiThreads);
+        }
+      } else {
+        float* out = routed ? p.y_perm : p.y_sh;
+        const int h = m.ft * 128 + q * 32 + lane;
+        for (int c0 = 0; c0 < n_mma; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(t_row + c0, r);
+          tmem_ld_wait();
+          if (h < p.H) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < m.cnt && m.row0 + col < nrows_out) out[(size_t)(m.row0 + col) * p.H + h] = __uint_as_float(r[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&tempty[acc]);
+      if (m.gu) {
+        // publish this gate/up item to the down items of its group
+        named_bar_sync(1, kEpiThreads);
+        if (threadIdx.x == 64) {
+          fence_proxy_async_global();
+          __threadfence();
+          atomicAdd(&p.done[m.g], 1);
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, SM::kTmemCols);
+  }
+}
+
+// Gathers the routed token rows into expert order (x_perm[r] = x[perm[r] / k])
+// and builds the tile table from the expert offsets.
+template <int BN>
+__global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ perm,
+                                                       const int32_t* __restrict__ offsets, int T, int H, int E,
+                                                       int k, int S, int I, bf16* __restrict__ xperm,
+                                                       int32_t* __restrict__ table, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int nrows = T * k;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row < nrows) {
+    const int src = perm[row];
+    if (src < 0 || src >= nrows) {
+      set_error(err, kErrDeviceIndex);
+    } else {
+      const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)(src / k) * H);
+      uint4* d = reinterpret_cast<uint4*>(xperm + (size_t)row * H);
+      for (int c = lane; c < H / 8; c += 32) d[c] = __ldg(s + c);
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x < 32) {
+    const int G = E + (S > 0 ? 1 : 0);
+    const int nft_dn = (H + 127) / 128;
+    // 9 groups per lane covers G <= 257 + 31
+    constexpr int PER = (kMaxExperts + 1 + 31) / 32;
+    int gu_loc[PER], dn_loc[PER];
+    int gu_sum = 0, dn_sum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int g = lane * PER + j;
+      int ntt = 0, nft_gu = 0;
+      if (g < E) {
+        const int c = offsets[g + 1] - offsets[g];
+        ntt = (c + BN - 1) / BN;
+        nft_gu = I / 64;
+      } else if (g < G) {
+        ntt = (T + BN - 1) / BN;
+        nft_gu = S * I / 64;
+      }
+      gu_loc[j] = ntt * nft_gu;
+      dn_loc[j] = ntt * nft_dn;
+      gu_sum += gu_loc[j];
+      dn_sum += dn_loc[j];
+    }
+    // the offsets must describe a partition of [0, T*k); otherwise no item is scheduled
+    int bad = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int g = lane * PER + j;
+      if (g < E && (offsets[g] > offsets[g + 1])) bad = 1;
+    }
+    if (lane == 0 && (offsets[0] != 0 || offsets[E] != nrows)) bad = 1;
+    bad = __any_sync(0xffffffffu, bad);
+    if (bad) {
+      gu_sum = dn_sum = 0;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) gu_loc[j] = dn_loc[j] = 0;
+      if (lane == 0) set_error(err, kErrDeviceIndex);
+    }
+    int gu_incl = gu_sum, dn_incl = dn_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, gu_incl, o);
+      const int b = __shfl_up_sync(0xffffffffu, dn_incl, o);
+      if (lane >= o) {
+        gu_incl += a;
+        dn_incl += b;
+      }
+    }
+    int gu_run = gu_incl - gu_sum, dn_run = dn_incl - dn_sum;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int g = lane * PER + j;
+      if (g <= G) {
+        table[8 + g] = gu_run;
+        table[8 + G + 1 + g] = dn_run;
+      }
+      if (g < G) table[8 + 2 * G + 2 + g] = 0;
+      gu_run += gu_loc[j];
+      dn_run += dn_loc[j];
+    }
+    if (lane == 31) {
+      table[0] = gu_incl;
+      table[1] = dn_incl;
+      table[2] = G;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box = box_cols x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  if (rows == 0) rows = 1;  // an empty tensor still needs a valid map; nothing reads it
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
+                    const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E, int k,
+                    int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
+                    const DeviceCtx& dc, cudaStream_t s) {
+  using SM = Smem<BN, STAGES>;
+  static int attr_done[64] = {0};
+  if (dc.device >= 0 && dc.device < 64 && !attr_done[dc.device]) {
+    cudaError_t e = cudaFuncSetAttribute(ffn_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SM::kTotal);
+    if (e != cudaSuccess) return e;
+    attr_done[dc.device] = 1;
+  }
+  int32_t* table = reinterpret_cast<int32_t*>(ws + L.table);
+  bf16* xperm = reinterpret_cast<bf16*>(ws + L.xperm);
+  bf16* act = reinterpret_cast<bf16*>(ws + L.act);
+  bf16* act_sh = reinterpret_cast<bf16*>(ws + L.act_sh);
+  const int G = E + (S > 0 ? 1 : 0);
+  const int nrows = T * k;
+
+  const int prep_blocks = max(1, (nrows + 7) / 8);
+  ffn_prep_kernel<BN><<<prep_blocks, 256, 0, s>>>(x, perm, offsets, T, H, E, k, S, I, xperm, table, dc.err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  FfnMaps maps;
+  const int SI = S > 0 ? S * I : 64;
+  const bool ok = make_map(&maps.wgu, w_gate_up, (uint64_t)E * 2 * I, H, 64) &&
+                  make_map(&maps.wsgu, S > 0 ? ws_gate_up : w_gate_up, S > 0 ? (uint64_t)2 * S * I : 1, H, 64) &&
+                  make_map(&maps.wd, w_down, (uint64_t)E * H, I, 128) &&
+                  make_map(&maps.wsd, S > 0 ? ws_down : w_down, S > 0 ? (uint64_t)H : 1, S > 0 ? SI : I, 128) &&
+                  make_map(&maps.xperm, xperm, nrows, H, BN) && make_map(&maps.x, x, T, H, BN) &&
+                  make_map(&maps.act, act, nrows, I, BN) &&
+                  make_map(&maps.act_sh, S > 0 ? (const void*)act_sh : (const void*)act, S > 0 ? T : 1,
+                           S > 0 ? SI : I, BN);
+  if (!ok) return cudaErrorInvalidValue;
+
+  FfnParams p;
+  p.T = T; p.H = H; p.E = E; p.k = k; p.S = S; p.I = I; p.G = G;
+  p.offsets = offsets;
+  p.table = table;
+  p.done = table + 8 + 2 * G + 2;
+  p.act = act;
+  p.act_sh = act_sh;
+  p.y_perm = y_perm;
+  p.y_sh = y_sh;
+  p.err = dc.err;
+  p.wait_ns = wait_limit_ns();
+  ffn_kernel<BN, STAGES><<<dc.num_sms, kFfnThreads, SM::kTotal, s>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Token tile: the smallest of 32/64/128/256 that holds the mean rows per expert
+// with room for the spread of a multinomial draw.
+int ffn_token_tile(int T, int k, int E) {
+  const double mean = E > 0 ? (double)T * k / E : 0.0;
+  if (mean <= 20.0) return 32;
+  if (mean <= 44.0) return 64;
+  if (mean <= 96.0) return 128;
+  return 256;
+}
+
+cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
+                       const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
+                       int k, int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
+                       const DeviceCtx& dc, cudaStream_t s) {
+  switch (ffn_token_tile(T, k, E)) {
+    case 32:
+      return run_ffn<32, 10>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
+                             y_sh, ws, L, dc, s);
+    case 64:
+      return run_ffn<64, 8>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
+                            y_sh, ws, L, dc, s);
+    case 128:
+      return run_ffn<128, 6>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
+                             y_sh, ws, L, dc, s);
+    default:
+      return run_ffn<256, 4>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
+                             y_sh, ws, L, dc, s);
+  }
+}
+
+}  // namespace lsv

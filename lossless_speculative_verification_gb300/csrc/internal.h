@@ -1,0 +1,79 @@
+// internal.h -- launchers and shared host-side declarations of the library
+// (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace lsv {
+
+typedef __nv_bfloat16 bf16;
+
+// Limits shared by validation and kernels.
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kMaxShared = 8;
+constexpr int kMaxHidden = 16384;
+constexpr int kMaxVerifyRows = 64;  // K + 1 per sequence
+
+// Per-device state: the error word's device address and the SM count.
+struct DeviceCtx {
+  int device = -1;
+  int num_sms = 0;
+  int* err = nullptr;
+};
+cudaError_t device_ctx(DeviceCtx** out);
+uint64_t wait_limit_ns();
+
+// ---------------------------------------------------------------- FFN tile table
+// int32 table in the workspace, written by the prep kernel, read by the FFN kernel.
+//   [0] gate/up items  [1] down items  [2] groups G
+//   [8 .. 8+G]             gate/up item start per group (exclusive scan, G+1 entries)
+//   [8+G+1 .. 8+2G+1]      down item start per group (G+1 entries)
+//   [8+2G+2 .. 8+3G+1]     completed gate/up items per group (zeroed by the prep kernel)
+inline int table_ints(int G) { return 8 + 3 * G + 2; }
+
+struct FfnGeom {
+  int T, H, E, k, S, I, G, BN;
+};
+
+// Workspace layout (byte offsets, each region 256-byte aligned).
+struct WsLayout {
+  size_t topk_idx, topk_w, counts, offsets, perm, inv, blk_counts, table, xperm, act, act_sh, y_perm, y_sh;
+  size_t total;
+  int nblk;  // permutation blocks
+};
+WsLayout ws_layout(int T, int H, int E, int k, int S, int I);
+
+constexpr int kPermChunk = 8192;  // (token, slot) entries per permutation block
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int k, int32_t* idx, float* w,
+                         float* logits, cudaStream_t s);
+
+cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* perm, int32_t* inv, int32_t* blk_counts, int nblk, int* err,
+                           cudaStream_t s);
+
+int ffn_token_tile(int T, int k, int E);
+cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
+                       const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
+                       int k, int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
+                       const DeviceCtx& dc, cudaStream_t s);
+
+cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_sh,
+                           int T, int H, int k, bf16* out, int* err, cudaStream_t s);
+
+cudaError_t launch_rmsnorm_residual(bf16* x, const bf16* y, bf16* h, int T, int H, float eps, cudaStream_t s);
+
+size_t accept_ws_bytes(int B, int K, int V, int num_sms);
+cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int K, int V, int32_t* argmax,
+                          int32_t* accept_len, int32_t* committed, void* ws, const DeviceCtx& dc,
+                          cudaStream_t s);
+
+cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace lsv

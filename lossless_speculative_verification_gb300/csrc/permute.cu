@@ -1,0 +1,167 @@
+// permute.cu -- expert histogram, exclusive scan and stable permutation of the
+// (token, slot) pairs into expert-contiguous order.
+//
+// Entry i = t*k + s carries expert idx[i].  counts[e] = #entries of e,
+// offsets = exclusive scan, and perm_src lists the entries of expert 0, then
+// expert 1, ..., each expert's entries in increasing i (= increasing token,
+// since a token picks an expert at most once).  Positions are computed from
+// ranks, never from the order in which atomics land, so the result is unique
+// and run-to-run identical.
+//
+// Blocks own contiguous ranges of kPermChunk entries.  With more than one
+// block a count kernel first writes per-block histograms; the scatter kernel
+// derives every block's base per expert from them.  Inside a block, entries
+// are ranked a round of 1024 at a time: __match_any_sync groups equal experts
+// within a warp, and a per-expert scan over the 32 warps orders the warps.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lsv {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+__global__ void __launch_bounds__(kThreads) permute_count_kernel(const int32_t* __restrict__ idx, int n, int E,
+                                                                 int32_t* __restrict__ blk_counts, int* err) {
+  __shared__ int cnt[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += kThreads) cnt[e] = 0;
+  __syncthreads();
+  const int begin = blockIdx.x * kPermChunk;
+  const int end = min(n, begin + kPermChunk);
+  for (int i = begin + threadIdx.x; i < end; i += kThreads) {
+    const int e = idx[i];
+    if (e < 0 || e >= E)
+      set_error(err, kErrDeviceIndex);
+    else
+      atomicAdd(&cnt[e], 1);  // integer counts: the result does not depend on the order
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kThreads) blk_counts[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// Exclusive scan of v[0..E) into out[0..E] by warp 0 (E <= 256: 8 per lane).
+__device__ void warp_exclusive_scan(const int* v, int* out, int E) {
+  const int lane = threadIdx.x & 31;
+  constexpr int PER = kMaxExperts / 32;
+  int loc[PER];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane * PER + j;
+    loc[j] = e < E ? v[e] : 0;
+    sum += loc[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane * PER + j;
+    if (e < E) out[e] = run;
+    run += loc[j];
+  }
+  if (lane == 31) out[E] = incl;
+}
+
+__global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
+    const int32_t* __restrict__ idx, int n, int E, int nblk, const int32_t* __restrict__ blk_counts,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, int* err) {
+  __shared__ int tot[kMaxExperts];
+  __shared__ int off[kMaxExperts + 1];
+  __shared__ int base[kMaxExperts];
+  __shared__ int wcnt[kWarps][kMaxExperts];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int begin = blockIdx.x * kPermChunk;
+  const int end = min(n, begin + kPermChunk);
+
+  // totals per expert and this block's share of earlier blocks
+  if (nblk == 1) {
+    for (int e = tid; e < E; e += kThreads) tot[e] = 0;
+    __syncthreads();
+    for (int i = begin + tid; i < end; i += kThreads) {
+      const int e = idx[i];
+      if (e >= 0 && e < E) atomicAdd(&tot[e], 1);
+      else set_error(err, kErrDeviceIndex);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) base[e] = 0;
+  } else {
+    for (int e = tid; e < E; e += kThreads) {
+      int t = 0, pre = 0;
+      for (int b = 0; b < nblk; ++b) {
+        const int c = blk_counts[(size_t)b * E + e];
+        if (b < blockIdx.x) pre += c;
+        t += c;
+      }
+      tot[e] = t;
+      base[e] = pre;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) warp_exclusive_scan(tot, off, E);
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = tid; e < E; e += kThreads) {
+      counts[e] = tot[e];
+      offsets[e] = off[e];
+    }
+    if (tid == 0) offsets[E] = off[E];
+  }
+  for (int e = tid; e < E; e += kThreads) base[e] += off[e];
+  __syncthreads();
+
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r0 = begin; r0 < end; r0 += kThreads) {
+    for (int q = tid; q < kWarps * E; q += kThreads) (&wcnt[0][0])[(q / E) * kMaxExperts + q % E] = 0;
+    __syncthreads();
+    const int i = r0 + tid;
+    int e = (i < end) ? idx[i] : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += kThreads) {
+      int acc = base[ee];
+#pragma unroll 4
+      for (int w = 0; w < kWarps; ++w) {
+        const int c = wcnt[w][ee];
+        wcnt[w][ee] = acc;
+        acc += c;
+      }
+      base[ee] = acc;
+    }
+    __syncthreads();
+    if (e >= 0) {
+      const int pos = wcnt[warp][e] + rank;
+      perm[pos] = i;
+      inv[i] = pos;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* perm, int32_t* inv, int32_t* blk_counts, int nblk, int* err,
+                           cudaStream_t s) {
+  const int n = T * k;
+  if (nblk > 1) {
+    permute_count_kernel<<<nblk, kThreads, 0, s>>>(idx, n, E, blk_counts, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  permute_scatter_kernel<<<nblk, kThreads, 0, s>>>(idx, n, E, nblk, blk_counts, counts, offsets, perm, inv,
+                                                   err);
+  return cudaGetLastError();
+}
+
+}  // namespace lsv
