@@ -85,6 +85,16 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def wait_first_sample(self, timeout=3.0):
+        """Block until nvidia-smi has printed its first sample (it takes a moment to start)."""
+        self._first = None
+        if self.proc is None:
+            return
+        import select
+        r, _, _ = select.select([self.proc.stdout], [], [], timeout)
+        if r:
+            self._first = self.proc.stdout.readline()
+
     def __exit__(self, *a):
         if self.proc is not None:
             self.proc.terminate()
@@ -93,7 +103,8 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            first = [self._first] if getattr(self, "_first", None) else []
+            self.lines = [l for l in first + out.splitlines() if l.strip()]
         else:
             self.lines = []
 
@@ -189,17 +200,18 @@ def cpu_baseline_sample(seconds=12.0, seed=0):
     logits, planted, drafts = synth.verify_problem(w, seed=seed)
     n = 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds and n < d.T:
+    while time.perf_counter() - t0 < seconds:
+        t = n % d.T
         oracle.moe_layer(prob.x, prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up, prob.ws_down,
-                         d.k, d.S, tokens=np.array([n], np.int32))
-        b = n // (w.K + 1)
-        if n % (w.K + 1) == 0:
+                         d.k, d.S, tokens=np.array([t], np.int32))
+        b = t // (w.K + 1)
+        if t % (w.K + 1) == 0:
             oracle.accept(logits[b:b + 1], drafts[b:b + 1])
         n += 1
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of the 128 tokens through the oracle layer (route, 6 routed + 2 shared experts, combine) "
-                      "plus the acceptance of their sequences, %.1f s" % (n, dt)}
+            "sample": "%d token passes (cycling over the 128 tokens) through the oracle layer (route, 6 routed "
+                      "+ 2 shared experts, combine) plus the acceptance of their sequences, %.1f s" % (n, dt)}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -250,25 +262,46 @@ def run_ours(args, rank, world, local):
     comm = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
     lib = api._ffi.load()
     stream = torch.cuda.current_stream(dev)
-    ffn_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     launches_per_step = 7   # route, permute, ffn prep, ffn, combine, argmax partials, accept
 
-    def step(time_ffn=False):
-        # the same launches moe_verify_layer makes, called one by one so that the FFN span can be timed
+    def part_a():
+        # the launches moe_verify_layer makes, called one by one so that the FFN span can be timed
         api.moe_route(x, W[0], k, topk_idx=idx, topk_w=tw)
         api._ffi.check("moe_permute", lib.moe_permute(api._ptr(idx), api.ctypes.byref(sh), api._ptr(counts),
                                                       api._ptr(offsets), api._ptr(perm), api._ptr(inv),
                                                       api._ptr(ws), ws.numel(), api._stream()))
-        if time_ffn:
-            ffn_ev[0].record(stream)
+
+    def part_b():
         api.moe_grouped_ffn(x, perm, offsets, counts, wts, sh, ws, y_perm=y_perm, y_shared=y_sh)
-        if time_ffn:
-            ffn_ev[1].record(stream)
+
+    def part_c():
         api.moe_combine(y_perm, inv, tw, y_sh, sh, out=out)
         api.spec_verify_accept(logits, drafts, aws, accept_len=alen, committed=comm)
 
     for _ in range(max(args.warmup, 0)):
-        step()
+        part_a(); part_b(); part_c()
+    torch.cuda.synchronize()
+    assert api.get_device_error() == 0
+
+    # eager launches, for context
+    eager_ms = []
+    for i in range(min(args.steps, 10)):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        part_a(); part_b(); part_c()
+        b.record(stream)
+        b.synchronize()
+        eager_ms.append(a.elapsed_time(b))
+
+    # the step as three CUDA graphs (routing | grouped experts | combine + acceptance)
+    graphs = [torch.cuda.CUDAGraph() for _ in range(3)]
+    for g, fn in zip(graphs, (part_a, part_b, part_c)):
+        with torch.cuda.graph(g):
+            fn()
+    for _ in range(max(args.warmup, 0)):
+        for g in graphs:
+            g.replay()
     torch.cuda.synchronize()
     assert api.get_device_error() == 0
 
@@ -280,20 +313,36 @@ def run_ours(args, rank, world, local):
 
     # timed region: per step, flush L2 (untimed), then events around the step
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    ffn_ms = []
+    fevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # the sampler polls every 100 ms: keep the GPU in the same back-to-back load for a
+        # moment before and after the timed steps so that its samples describe them
+        clk.wait_first_sample()
+        t_end = time.perf_counter() + 0.3
+        while time.perf_counter() < t_end:
+            flush.fill_(0)
+            for g in graphs:
+                g.replay()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             evs[i][0].record(stream)
-            step(time_ffn=True)
+            graphs[0].replay()
+            fevs[i][0].record(stream)
+            graphs[1].replay()
+            fevs[i][1].record(stream)
+            graphs[2].replay()
             evs[i][1].record(stream)
-            evs[i][1].synchronize()
-            ffn_ms.append(ffn_ev[0].elapsed_time(ffn_ev[1]))
+        t_end = time.perf_counter() + 0.3
+        while time.perf_counter() < t_end:
+            flush.fill_(0)
+            for g in graphs:
+                g.replay()
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in evs]
+    ffn_ms = [a.elapsed_time(b) for a, b in fevs]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -363,7 +412,9 @@ def run_ours(args, rank, world, local):
                                "then greedy acceptance over [32,4,129280] bf16 logits",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (256 MB write, outside the events)",
-                   "timing": "eager launches, CUDA events per step"},
+                   "timing": "step replayed as 3 CUDA graphs, CUDA events per step",
+                   "clocks_window": "nvidia-smi every 100 ms over back-to-back steps around the timed ones",
+                   "eager_ms_per_step": sum(eager_ms) / len(eager_ms)},
         "roofline": {"bound": "hbm", "kernel": "ffn_kernel (grouped SwiGLU experts, tcgen05) incl. its gather prep",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_kind, "traffic": traffic, "algorithmic_bytes": ffn_bytes,

@@ -39,9 +39,13 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags: list[str] | None = None) -> str:
+def build(verbose: bool = False, force: bool = False, extra_flags: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    """Compile into out_dir (default: the package's _lib/) and return the library path."""
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    odir = out_dir or OUT_DIR
+    lib_path = os.path.join(odir, "liblsv.so")
+    os.makedirs(odir, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "lsv.h"))
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
@@ -51,7 +55,7 @@ def build(verbose: bool = False, force: bool = False, extra_flags: list[str] | N
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(odir, src.replace(".cu", ".o"))
         if force or _stale(o, [s] + headers):
             cmd = [nvcc, "-c", s, "-o", o + ".tmp.o"] + flags
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -64,16 +68,16 @@ def build(verbose: bool = False, force: bool = False, extra_flags: list[str] | N
 
     with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if force or _stale(LIB, objs):
+    if force or _stale(lib_path, objs):
         lib64 = os.path.join(_cuda_home(nvcc), "lib64")
-        tmp = LIB + ".%d.tmp" % os.getpid()
+        tmp = lib_path + ".%d.tmp" % os.getpid()
         cmd = [nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "shared", "-Xlinker",
                                                             "-rpath," + lib64]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

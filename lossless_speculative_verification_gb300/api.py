@@ -43,8 +43,11 @@ def weights(w_router, w_gate_up, w_down, ws_gate_up=None, ws_down=None) -> MoeWe
     for n, t in (("w_router", w_router), ("w_gate_up", w_gate_up), ("w_down", w_down),
                  ("ws_gate_up", ws_gate_up), ("ws_down", ws_down)):
         _need(t, torch.bfloat16, n)
-    return MoeWeights(*(t.data_ptr() if t is not None else None
-                        for t in (w_router, w_gate_up, w_down, ws_gate_up, ws_down)))
+    w = MoeWeights(*(t.data_ptr() if t is not None else None
+                     for t in (w_router, w_gate_up, w_down, ws_gate_up, ws_down)))
+    # the struct holds raw pointers: keep the tensors alive as long as the struct
+    w._tensors = (w_router, w_gate_up, w_down, ws_gate_up, ws_down)
+    return w
 
 
 def workspace_size(sh: MoeShape) -> int:

@@ -25,12 +25,16 @@
 //
 // One persistent CTA per SM, warp-specialised: warp 0 issues TMA, warp 1
 // allocates TMEM and issues tcgen05.mma (one thread), warps 2-5 drain TMEM.
-// A STAGES-deep shared-memory ring decouples loads from MMAs, and two TMEM
-// accumulators decouple MMAs from the epilogue.  Items are dealt round-robin:
-// every gate/up item precedes every down item in the global order, and a down
-// item waits (bounded) on a per-group counter of finished gate/up items, so
-// the wait always ends: a CTA finishes all of its gate/up items before it
-// reaches any down item.
+// A STAGES-deep shared-memory ring (KCH K-chunks per stage, so that the
+// neighbouring 128-byte pieces of each weight row are requested together)
+// decouples loads from MMAs, and two TMEM accumulators decouple MMAs from the
+// epilogue.  Items are dealt dynamically: the producer takes the next index
+// from a global counter and passes it to the MMA and epilogue warps through a
+// small shared-memory ring.  Every gate/up item precedes every down item in
+// the global order, and a down item waits (bounded) on a per-group counter of
+// finished gate/up items; the wait always ends, because every gate/up item of
+// that group was dealt earlier to a running CTA whose progress on it depends
+// on nothing else.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -41,6 +45,14 @@ constexpr int kFfnThreads = 192;         // 6 warps
 constexpr int kEpiThreads = 128;         // warps 2..5
 constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
 constexpr int kXchStride = 17;           // padded row of the gate/up exchange buffer
+
+// Decode-size pipeline: K chunks (64 wide) per stage and stage count.
+#ifndef LSV_FFN_KCH32
+#define LSV_FFN_KCH32 2
+#endif
+#ifndef LSV_FFN_STAGES32
+#define LSV_FFN_STAGES32 5
+#endif
 
 struct FfnParams {
   int T, H, E, k, S, I, G;
@@ -114,21 +126,25 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KCH>
 struct Smem {
-  static constexpr int kStageBytes = kATileBytes + BN * 128;
+  static constexpr int kChunkA = kATileBytes;               // one 64-wide K chunk of A
+  static constexpr int kChunkB = BN * 128;                  // one 64-wide K chunk of B
+  static constexpr int kStageBytes = KCH * (kChunkA + kChunkB);
   static constexpr int kRing = STAGES * kStageBytes;
   static constexpr int kXch = 64 * kXchStride * 4;
-  static constexpr int kBars = (2 * STAGES + 5) * 8;
-  static constexpr int kTotal = 1024 /*alignment slack*/ + kRing + kXch + kBars + 16;
+  static constexpr int kItemSlots = 4;
+  static constexpr int kBars = (2 * STAGES + 5 + 2 * kItemSlots) * 8;
+  static constexpr int kTotal = 1024 /*alignment slack*/ + kRing + kXch + kBars + 16 + kItemSlots * 4;
   static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KCH>
 __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_constant__ FfnMaps maps,
                                                               const FfnParams p) {
-  using SM = Smem<BN, STAGES>;
+  using SM = Smem<BN, STAGES, KCH>;
+  constexpr int NS = SM::kItemSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xch = reinterpret_cast<float*>(smem + SM::kRing);
@@ -138,8 +154,11 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* final_bar = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  uint64_t* item_full = final_bar + 1;
+  uint64_t* item_empty = item_full + NS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(item_empty + NS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -151,6 +170,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], kEpiThreads);
+    }
+    for (int q = 0; q < NS; ++q) {
+      mbar_init(&item_full[q], 1);
+      mbar_init(&item_empty[q], 1 + kEpiThreads);
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
@@ -165,17 +188,33 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int n_items = p.table[0] + p.table[1];
-
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer + item dealer
     if (lane == 0) {
+      const int n_items = p.table[0] + p.table[1];
+      int* counter = const_cast<int*>(p.table) + 3;
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
+      int slot = 0;
+      uint32_t slot_phase = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      while (ok) {
+        if (!mbar_wait(&item_empty[slot], slot_phase ^ 1u, p.wait_ns)) {
+          set_error(p.err, kErrTimeout);
+          ok = false;
+          break;
+        }
+        int it = atomicAdd(counter, 1);
+        if (it >= n_items) it = -1;
+        item_slot[slot] = it;
+        mbar_arrive(&item_full[slot]);  // release: the slot write is visible to the waiters
+        if (++slot == NS) {
+          slot = 0;
+          slot_phase ^= 1u;
+        }
+        if (it < 0) break;
         const Item m = decode_item<BN>(it, p);
         const bool routed = m.g < p.E;
         if (!m.gu) {
@@ -197,22 +236,26 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         } else {
           arow0 = (routed ? m.g * p.H : 0) + m.ft * 128;
         }
-        for (int kc = 0; kc < m.nk; ++kc) {
+        for (int kc0 = 0; kc0 < m.nk; kc0 += KCH) {
+          const int nch = min(KCH, m.nk - kc0);
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
             set_error(p.err, kErrTimeout);
             ok = false;
             break;
           }
           uint8_t* a_s = smem + stage * SM::kStageBytes;
-          uint8_t* b_s = a_s + kATileBytes;
-          mbar_arrive_expect_tx(&full[stage], kATileBytes + BN * 128);
-          if (m.gu) {
-            tma_load_2d(a_s, amap, &full[stage], kc * 64, arow0, pol_w);
-            tma_load_2d(a_s + kATileBytes / 2, amap, &full[stage], kc * 64, arow1, pol_w);
-          } else {
-            tma_load_2d(a_s, amap, &full[stage], kc * 64, arow0, pol_w);
-          }
-          tma_load_2d(b_s, bmap, &full[stage], kc * 64, m.row0, pol_x);
+          uint8_t* b_s = a_s + KCH * SM::kChunkA;
+          mbar_arrive_expect_tx(&full[stage], nch * (SM::kChunkA + SM::kChunkB));
+          // all K chunks of one weight row block back to back: neighbouring 128-byte pieces of
+          // every row reach the memory system together
+          for (int c = 0; c < nch; ++c)
+            tma_load_2d(a_s + c * SM::kChunkA, amap, &full[stage], (kc0 + c) * 64, arow0, pol_w);
+          if (m.gu)
+            for (int c = 0; c < nch; ++c)
+              tma_load_2d(a_s + c * SM::kChunkA + kATileBytes / 2, amap, &full[stage], (kc0 + c) * 64, arow1,
+                          pol_w);
+          for (int c = 0; c < nch; ++c)
+            tma_load_2d(b_s + c * SM::kChunkB, bmap, &full[stage], (kc0 + c) * 64, m.row0, pol_x);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -223,6 +266,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         *abort_flag = 1;
         __threadfence_block();
         mbar_arrive(&full[stage]);  // wake the MMA issuer so that it sees the abort
+        // and hand out an end marker in case the consumers wait for an item
+        item_slot[slot] = -1;
+        mbar_arrive(&item_full[slot]);
       }
     }
   } else if (warp == 1) {
@@ -232,8 +278,22 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      int slot = 0;
+      uint32_t slot_phase = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      while (ok) {
+        if (!mbar_wait(&item_full[slot], slot_phase, p.wait_ns)) {
+          set_error(p.err, kErrTimeout);
+          ok = false;
+          break;
+        }
+        const int it = item_slot[slot];
+        mbar_arrive(&item_empty[slot]);
+        if (++slot == NS) {
+          slot = 0;
+          slot_phase ^= 1u;
+        }
+        if (it < 0 || *abort_flag) break;
         const Item m = decode_item<BN>(it, p);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_ns)) {
           set_error(p.err, kErrTimeout);
@@ -244,7 +304,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         const int n_mma = max(16, (m.cnt + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(128, n_mma);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kc = 0; kc < m.nk; ++kc) {
+        for (int kc0 = 0; kc0 < m.nk; kc0 += KCH) {
+          const int nch = min(KCH, m.nk - kc0);
           if (!mbar_wait(&full[stage], phase, p.wait_ns)) {
             set_error(p.err, kErrTimeout);
             ok = false;
@@ -256,11 +317,14 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           }
           tc_fence_after_sync();
           const uint32_t a_s = smem_u32(smem + stage * SM::kStageBytes);
-          const uint32_t b_s = a_s + kATileBytes;
+          const uint32_t b_s = a_s + KCH * SM::kChunkA;
+          for (int c = 0; c < nch; ++c) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d_tmem, sdesc_kmajor_sw128(a_s + kk * 32), sdesc_kmajor_sw128(b_s + kk * 32), idesc,
-                      (kc | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(d_tmem, sdesc_kmajor_sw128(a_s + c * SM::kChunkA + kk * 32),
+                        sdesc_kmajor_sw128(b_s + c * SM::kChunkB + kk * 32), idesc,
+                        ((kc0 + c) | kk) ? 1u : 0u);
+          }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -272,11 +336,10 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok) {
-        *abort_flag = 1;
-        __threadfence_block();
-        mbar_arrive(&tfull[acc]);  // wake the epilogue so that it sees the abort
-      }
+      // tell the epilogue that no more accumulators come (end marker or abort)
+      *abort_flag = ok ? *abort_flag : 1;
+      __threadfence_block();
+      if (!ok) mbar_arrive(&tfull[acc]);
       // every MMA issued by this thread has completed before TMEM is released
       umma_commit(final_bar);
       if (!mbar_wait(final_bar, 0, p.wait_ns)) set_error(p.err, kErrTimeout);
@@ -287,11 +350,22 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    int slot = 0;
+    uint32_t slot_phase = 0;
+    while (true) {
+      const bool got_item = mbar_wait(&item_full[slot], slot_phase, p.wait_ns);
+      if (!got_item) set_error(p.err, kErrTimeout);
+      const int it = got_item ? item_slot[slot] : -1;
+      mbar_arrive(&item_empty[slot]);
+      if (++slot == NS) {
+        slot = 0;
+        slot_phase ^= 1u;
+      }
+      // the same decision in all four epilogue warps keeps their named barriers matched
+      if (named_bar_red_or(1, kEpiThreads, it < 0)) break;
       const Item m = decode_item<BN>(it, p);
       const bool got = mbar_wait(&tfull[acc], acc_phase, p.wait_ns);
       if (!got) set_error(p.err, kErrTimeout);
-      // all four epilogue warps take the same decision, so their named barriers stay matched
       if (named_bar_red_or(1, kEpiThreads, !got || *abort_flag)) break;
       tc_fence_after_sync();
       const bool routed = m.g < p.E;
@@ -335,7 +409,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int col = c0 + j;
-              if (col < m.cnt && m.row0 + col < nrows_out) out[(size_t)(m.row0 + col) * p.H + h] = __uint_as_float(r[j]);
+              if (col < m.cnt && m.row0 + col < nrows_out)
+                out[(size_t)(m.row0 + col) * p.H + h] = __uint_as_float(r[j]);
             }
           }
         }
@@ -449,6 +524,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
       table[0] = gu_incl;
       table[1] = dn_incl;
       table[2] = G;
+      table[3] = 0;  // next item to deal
     }
   }
 }
@@ -485,15 +561,16 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KCH>
 cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                     const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E, int k,
                     int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
                     const DeviceCtx& dc, cudaStream_t s) {
-  using SM = Smem<BN, STAGES>;
+  using SM = Smem<BN, STAGES, KCH>;
+  static_assert(SM::kTotal <= 232448, "shared memory budget");
   static int attr_done[64] = {0};
   if (dc.device >= 0 && dc.device < 64 && !attr_done[dc.device]) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(ffn_kernel<BN, STAGES, KCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SM::kTotal);
     if (e != cudaSuccess) return e;
     attr_done[dc.device] = 1;
@@ -533,7 +610,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.y_sh = y_sh;
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();
-  ffn_kernel<BN, STAGES><<<dc.num_sms, kFfnThreads, SM::kTotal, s>>>(maps, p);
+  ffn_kernel<BN, STAGES, KCH><<<dc.num_sms, kFfnThreads, SM::kTotal, s>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -555,17 +632,17 @@ cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offset
                        const DeviceCtx& dc, cudaStream_t s) {
   switch (ffn_token_tile(T, k, E)) {
     case 32:
-      return run_ffn<32, 10>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                             y_sh, ws, L, dc, s);
+      return run_ffn<32, LSV_FFN_STAGES32, LSV_FFN_KCH32>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down,
+                                                          T, H, E, k, S, I, y_perm, y_sh, ws, L, dc, s);
     case 64:
-      return run_ffn<64, 8>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                            y_sh, ws, L, dc, s);
+      return run_ffn<64, 4, 2>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
+                               y_sh, ws, L, dc, s);
     case 128:
-      return run_ffn<128, 6>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                             y_sh, ws, L, dc, s);
+      return run_ffn<128, 6, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
+                                y_sh, ws, L, dc, s);
     default:
-      return run_ffn<256, 4>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                             y_sh, ws, L, dc, s);
+      return run_ffn<256, 4, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
+                                y_sh, ws, L, dc, s);
   }
 }
 

@@ -30,7 +30,7 @@ uint64_t wait_limit_ns();
 
 // ---------------------------------------------------------------- FFN tile table
 // int32 table in the workspace, written by the prep kernel, read by the FFN kernel.
-//   [0] gate/up items  [1] down items  [2] groups G
+//   [0] gate/up items  [1] down items  [2] groups G  [3] next item to deal (zeroed by the prep kernel)
 //   [8 .. 8+G]             gate/up item start per group (exclusive scan, G+1 entries)
 //   [8+G+1 .. 8+2G+1]      down item start per group (G+1 entries)
 //   [8+2G+2 .. 8+3G+1]     completed gate/up items per group (zeroed by the prep kernel)

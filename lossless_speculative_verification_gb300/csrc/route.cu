@@ -1,16 +1,19 @@
-// route.cu -- router product, softmax gate and top-k selection (one warp per token).
+// route.cu -- router product, softmax gate and top-k selection.
 //
-// logits[t,e] = sum_h x[t,h] * W_r[e,h] accumulated in fp32 in increasing h
-// (each bf16 x bf16 product is exact in fp32, so an FMA chain in index order
-// gives the same bits as a multiply-then-add chain); p = softmax over all E in
-// fp32 (not renormalised over the selection); the k largest logits in
-// descending order with ties to the lower expert index.
+// logits[t,e] = sum_h x[t,h] * W_r[e,h] with fp32 accumulation; p = softmax
+// over all E in fp32 (not renormalised over the selection); the k largest
+// logits in descending order with ties to the lower expert index.
 // (jina-ocr-v1: "64 routed experts ... Top-6 routing", kg.zhiyong.dev, section
 // "The speed comes from three layers working together".)
 //
-// The router matrix is tiny (E x H bf16, 160 KB at E=64, H=1280) and is read
-// through L1/L2 by every warp; x rows are read once.  The step is latency
-// bound, not bandwidth bound.
+// One CTA takes TT tokens.  Warp w computes experts 8w..8w+7 (then 8w+64..)
+// for all TT tokens; inside a warp each lane owns a contiguous 8-element slice
+// of every 256-element block of h (16-byte loads of x and W), and the 32
+// partial sums are combined by a fixed butterfly.  The summation order is fixed, so
+// results are run-to-run identical; it differs from a sequential sum only by
+// fp32 rounding (far below the router gaps the selection depends on).  The
+// E logits of each token then go through shared memory to one warp per token
+// for the softmax and the k selection rounds.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -18,7 +21,6 @@ namespace lsv {
 namespace {
 
 constexpr int kRouteWarps = 8;
-constexpr int kMaxPerLane = kMaxExperts / 32;
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -29,82 +31,97 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
-template <int PER_LANE>
+template <int TT>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __restrict__ x,
                                                                  const bf16* __restrict__ wr, int T, int H,
                                                                  int E, int k, int32_t* __restrict__ idx,
                                                                  float* __restrict__ w,
                                                                  float* __restrict__ logits) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
+  __shared__ float lg[TT][kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * TT;
+  const int nt = min(TT, T - t0);
+  const int n8 = H / 8;  // 16-byte groups per row
 
-  float acc[PER_LANE];
+  // warp w owns experts [8w, 8w+8), [8w+64, 8w+72), ...: eight independent rows in flight per step
+  for (int e0 = warp * 8; e0 < E; e0 += kRouteWarps * 8) {
+    float acc[8][TT];
 #pragma unroll
-  for (int j = 0; j < PER_LANE; ++j) acc[j] = 0.0f;
-
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  for (int h8 = 0; h8 < H / 8; ++h8) {
-    float xf[8];
-    bf16x8_to_f32(__ldg(xr + h8), xf);
+    for (int q = 0; q < 8; ++q)
 #pragma unroll
-    for (int j = 0; j < PER_LANE; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E) {
-        float wf[8];
-        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + h8), wf);
+      for (int i = 0; i < TT; ++i) acc[q][i] = 0.0f;
+#pragma unroll 2
+    for (int c = lane; c < n8; c += 32) {
+      uint4 wv[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[j] = fmaf(xf[i], wf[i], acc[j]);
+      for (int q = 0; q < 8; ++q)
+        wv[q] = (e0 + q < E) ? __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + q) * H) + c)
+                             : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int i = 0; i < TT; ++i) {
+        if (i < nt) {
+          float xf[8];
+          bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + c), xf);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float wf[8];
+            bf16x8_to_f32(wv[q], wf);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[q][i] = fmaf(xf[j], wf[j], acc[q][i]);
+          }
+        }
       }
     }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+      for (int i = 0; i < TT; ++i) {
+        float v = acc[q][i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0 && e0 + q < E) lg[i][e0 + q] = v;
+      }
   }
+  __syncthreads();
 
-  // softmax over all E experts
-  float m = -INFINITY;
+  // softmax + top-k: one warp per token
+  for (int i = warp; i < nt; i += kRouteWarps) {
+    const int t = t0 + i;
+    float m = -INFINITY;
+    for (int e = lane; e < E; e += 32) m = fmaxf(m, lg[i][e]);
 #pragma unroll
-  for (int j = 0; j < PER_LANE; ++j)
-    if (lane + 32 * j < E) m = fmaxf(m, acc[j]);
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.0f;
+    for (int e = lane; e < E; e += 32) z += expf(lg[i][e] - m);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float z = 0.0f;
-#pragma unroll
-  for (int j = 0; j < PER_LANE; ++j)
-    if (lane + 32 * j < E) z += expf(acc[j] - m);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-
-  if (logits) {
-#pragma unroll
-    for (int j = 0; j < PER_LANE; ++j)
-      if (lane + 32 * j < E) logits[(size_t)t * E + lane + 32 * j] = acc[j];
-  }
-
-  // top-k: k rounds of a warp-wide (value desc, index asc) maximum
-  uint32_t taken = 0;
-  for (int s = 0; s < k; ++s) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < PER_LANE; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !(taken & (1u << j)) && (acc[j] > bv || (acc[j] == bv && e < be))) {
-        bv = acc[j];
-        be = e;
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (logits)
+      for (int e = lane; e < E; e += 32) logits[(size_t)t * E + e] = lg[i][e];
+    uint32_t taken = 0;  // bit j: expert lane + 32 j already selected
+    for (int s = 0; s < k; ++s) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+      for (int j = 0, e = lane; e < E; ++j, e += 32) {
+        const float v = lg[i][e];
+        if (!(taken & (1u << j)) && (v > bv || (v == bv && e < be))) {
+          bv = v;
+          be = e;
+        }
       }
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
       }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == 0) {
-      idx[(size_t)t * k + s] = be;
-      w[(size_t)t * k + s] = expf(bv - m) / z;
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == 0) {
+        idx[(size_t)t * k + s] = be;
+        w[(size_t)t * k + s] = expf(bv - m) / z;
+      }
     }
   }
 }
@@ -114,15 +131,14 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
 cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int k, int32_t* idx, float* w,
                          float* logits, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const dim3 grid((T + kRouteWarps - 1) / kRouteWarps), block(kRouteWarps * 32);
-  if (E <= 32)
-    route_kernel<1><<<grid, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
-  else if (E <= 64)
-    route_kernel<2><<<grid, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
-  else if (E <= 128)
-    route_kernel<4><<<grid, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
+  const dim3 block(kRouteWarps * 32);
+  // about one CTA per SM at decode sizes; more tokens per CTA once T is large
+  if (T <= 256)
+    route_kernel<1><<<T, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
+  else if (T <= 1024)
+    route_kernel<4><<<(T + 3) / 4, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
   else
-    route_kernel<kMaxPerLane><<<grid, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
+    route_kernel<8><<<(T + 7) / 8, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
   return cudaGetLastError();
 }
 
