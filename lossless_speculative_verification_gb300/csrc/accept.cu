@@ -10,8 +10,8 @@
 //
 // Phase 1 streams the logits once: each CTA owns a chunk of one row, loads it
 // with 16-byte non-allocating loads (8 bf16 each, several in flight per
-// thread) and writes the chunk's (max, first index).  Phase 2 (one warp per
-// sequence) reduces the chunk partials in index order and applies the rule.
+// thread) and writes the chunk's (max, first index).  Phase 2 (one CTA per
+// sequence, one warp per row) reduces the chunk partials and applies the rule.
 // No atomics decide anything, so the result is deterministic.
 #include <limits.h>
 
@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kAccThreads) argmax_partial_kernel(const bf16*
                                                                      int chunk, int nchunk, int vec_ok,
                                                                      float* __restrict__ pv,
                                                                      int* __restrict__ pi) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x, c = blockIdx.y;
   const bf16* row = logits + (size_t)r * V;
   const int begin = c * chunk;
@@ -103,18 +105,20 @@ __global__ void __launch_bounds__(kAccThreads) argmax_partial_kernel(const bf16*
   }
 }
 
-constexpr int kFinWarps = 4;
+// One CTA per sequence, one warp per verified row: each warp reduces its row's
+// chunk partials; then one thread applies the acceptance rule.
+constexpr int kFinWarps = 32;
 
 __global__ void __launch_bounds__(kFinWarps * 32) accept_finalize_kernel(
     const float* __restrict__ pv, const int* __restrict__ pi, int nchunk, const int32_t* __restrict__ drafts,
     int B, int K, int32_t* __restrict__ argmax, int32_t* __restrict__ accept_len,
     int32_t* __restrict__ committed) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kFinWarps + (threadIdx.x >> 5);
-  if (b >= B) return;
-  __shared__ int g[kFinWarps][kMaxVerifyRows];
-  int* gb = g[threadIdx.x >> 5];
-  for (int j = 0; j <= K; ++j) {
+  const int b = blockIdx.x;
+  __shared__ int g[kMaxVerifyRows];
+  for (int j = threadIdx.x >> 5; j <= K; j += blockDim.x >> 5) {
     const size_t r = (size_t)b * (K + 1) + j;
     float bv = -INFINITY;
     int bi = INT_MAX;
@@ -126,18 +130,18 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finalize_kernel(
       better(ov, oi, bv, bi);
     }
     if (lane == 0) {
-      gb[j] = bi;
+      g[j] = bi;
       if (argmax) argmax[r] = bi;
     }
   }
-  __syncwarp();
-  if (lane == 0) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
     int L = 0;
-    while (L < K && drafts[(size_t)b * K + L] == gb[L]) ++L;
+    while (L < K && drafts[(size_t)b * K + L] == g[L]) ++L;
     accept_len[b] = L;
     int32_t* cm = committed + (size_t)b * (K + 1);
     for (int i = 0; i < L; ++i) cm[i] = drafts[(size_t)b * K + i];
-    cm[L] = gb[L];
+    cm[L] = g[L];
     for (int i = L + 1; i <= K; ++i) cm[i] = -1;
   }
 }
@@ -175,12 +179,11 @@ cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int 
   float* pv = reinterpret_cast<float*>(ws);
   int* pi = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + one);
   const int vec_ok = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
-  argmax_partial_kernel<<<dim3(R, nchunk), kAccThreads, 0, s>>>(logits, V, chunk, nchunk, vec_ok, pv, pi);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(argmax_partial_kernel, dim3(R, nchunk), dim3(kAccThreads), 0, s, logits, V, chunk,
+                             nchunk, vec_ok, pv, pi);
   if (e != cudaSuccess) return e;
-  accept_finalize_kernel<<<(B + kFinWarps - 1) / kFinWarps, kFinWarps * 32, 0, s>>>(pv, pi, nchunk, drafts, B, K,
-                                                                                     argmax, accept_len, committed);
-  return cudaGetLastError();
+  return launch_pdl(accept_finalize_kernel, dim3(B), dim3(32 * min(K + 1, kFinWarps)), 0, s, (const float*)pv, (const int*)pi,
+                    nchunk, drafts, B, K, argmax, accept_len, committed);
 }
 
 }  // namespace lsv

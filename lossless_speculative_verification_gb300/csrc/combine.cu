@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const float* __re
   const int t = blockIdx.x;
   const int h4 = blockIdx.y * kCombThreads + threadIdx.x;  // group of 4 columns
   __shared__ int rows[kMaxTopK];
+  pdl_wait();
+  pdl_trigger();
   __shared__ float wts[kMaxTopK];
   if (threadIdx.x < k) {
     int r = inv[(size_t)t * k + threadIdx.x];
@@ -68,6 +70,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_residual_kernel(bf16* __
                                                                         bf16* __restrict__ h, int H,
                                                                         float eps) {
   const int t = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
   bf16* xr = x + (size_t)t * H;
   const bf16* yr = y + (size_t)t * H;
   bf16* hr = h + (size_t)t * H;
@@ -96,14 +100,12 @@ cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float*
                            int T, int H, int k, bf16* out, int* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const dim3 grid(T, (H / 4 + kCombThreads - 1) / kCombThreads);
-  combine_kernel<<<grid, kCombThreads, 0, s>>>(y_perm, inv, topk_w, y_sh, T, H, k, out, err);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(kCombThreads), 0, s, y_perm, inv, topk_w, y_sh, T, H, k, out, err);
 }
 
 cudaError_t launch_rmsnorm_residual(bf16* x, const bf16* y, bf16* h, int T, int H, float eps, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  rmsnorm_residual_kernel<<<T, kNormThreads, 0, s>>>(x, y, h, H, eps);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_residual_kernel, dim3(T), dim3(kNormThreads), 0, s, x, y, h, H, eps);
 }
 
 }  // namespace lsv

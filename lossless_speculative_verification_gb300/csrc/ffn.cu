@@ -80,6 +80,7 @@ struct FfnMaps {
 
 struct Item {
   int gu;    // 1: gate/up, 0: down
+  int slot;  // position of the group in the dealing order
   int g;     // group
   int ft;    // feature tile (64 features for gate/up, 128 outputs for down)
   int row0;  // first token row of the tile in the group's row space
@@ -87,6 +88,12 @@ struct Item {
   int nk;    // 64-wide K chunks
   int need;  // gate/up items of group g (for a down item's dependency)
 };
+
+// Dealing order of the groups: the shared group (the largest items) first, then
+// the routed experts in index order.
+__host__ __device__ __forceinline__ int slot_group(int slot, int E, int S) {
+  return S > 0 ? (slot == 0 ? E : slot - 1) : slot;
+}
 
 template <int BN>
 __device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
@@ -102,11 +109,12 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
     const int mid = (lo + hi + 1) >> 1;
     if (starts[mid] <= local_it) lo = mid; else hi = mid - 1;
   }
-  m.g = lo;
+  m.slot = lo;
+  m.g = slot_group(lo, p.E, p.S);
   const bool routed = m.g < p.E;
   const int inter = routed ? p.I : p.S * p.I;
   const int nft = m.gu ? inter / 64 : (p.H + 127) / 128;
-  const int local = local_it - starts[m.g];
+  const int local = local_it - starts[m.slot];
   const int tt = local / nft;
   m.ft = local - tt * nft;
   int seg0, segn;
@@ -120,7 +128,7 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
   m.row0 = seg0 + tt * BN;
   m.cnt = min(BN, segn - tt * BN);
   m.nk = m.gu ? p.H / 64 : inter / 64;
-  m.need = tb[8 + m.g + 1] - tb[8 + m.g];
+  m.need = tb[8 + m.slot + 1] - tb[8 + m.slot];
   return m;
 }
 
@@ -183,10 +191,19 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     tmem_alloc(tmem_slot, SM::kTmemCols);
     tmem_relinquish();
   }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&maps.wgu);
+    tma_prefetch_desc(&maps.wd);
+    tma_prefetch_desc(&maps.wsgu);
+    tma_prefetch_desc(&maps.wsd);
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // the prologue above overlaps the previous kernel; everything below reads its results
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer + item dealer
@@ -218,7 +235,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         const Item m = decode_item<BN>(it, p);
         const bool routed = m.g < p.E;
         if (!m.gu) {
-          if (!wait_counter_geq(&p.done[m.g], m.need, p.wait_ns)) {
+          if (!wait_counter_geq(&p.done[m.slot], m.need, p.wait_ns)) {
             set_error(p.err, kErrTimeout);
             ok = false;
             break;
@@ -423,7 +440,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         if (threadIdx.x == 64) {
           fence_proxy_async_global();
           __threadfence();
-          atomicAdd(&p.done[m.g], 1);
+          atomicAdd(&p.done[m.slot], 1);
         }
       }
       acc ^= 1;
@@ -446,6 +463,8 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
                                                        const int32_t* __restrict__ offsets, int T, int H, int E,
                                                        int k, int S, int I, bf16* __restrict__ xperm,
                                                        int32_t* __restrict__ table, int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int nrows = T * k;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -468,7 +487,8 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
     int gu_sum = 0, dn_sum = 0;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
-      const int g = lane * PER + j;
+      const int slot = lane * PER + j;
+      const int g = slot < G ? slot_group(slot, E, S) : G;
       int ntt = 0, nft_gu = 0;
       if (g < E) {
         const int c = offsets[g + 1] - offsets[g];
@@ -511,12 +531,12 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
     int gu_run = gu_incl - gu_sum, dn_run = dn_incl - dn_sum;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
-      const int g = lane * PER + j;
-      if (g <= G) {
-        table[8 + g] = gu_run;
-        table[8 + G + 1 + g] = dn_run;
+      const int slot = lane * PER + j;
+      if (slot <= G) {
+        table[8 + slot] = gu_run;
+        table[8 + G + 1 + slot] = dn_run;
       }
-      if (g < G) table[8 + 2 * G + 2 + g] = 0;
+      if (slot < G) table[8 + 2 * G + 2 + slot] = 0;
       gu_run += gu_loc[j];
       dn_run += dn_loc[j];
     }
@@ -583,8 +603,8 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   const int nrows = T * k;
 
   const int prep_blocks = max(1, (nrows + 7) / 8);
-  ffn_prep_kernel<BN><<<prep_blocks, 256, 0, s>>>(x, perm, offsets, T, H, E, k, S, I, xperm, table, dc.err);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(ffn_prep_kernel<BN>, dim3(prep_blocks), dim3(256), 0, s, x, perm, offsets, T, H, E, k,
+                             S, I, xperm, table, dc.err);
   if (e != cudaSuccess) return e;
 
   FfnMaps maps;
@@ -610,8 +630,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.y_sh = y_sh;
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();
-  ffn_kernel<BN, STAGES, KCH><<<dc.num_sms, kFfnThreads, SM::kTotal, s>>>(maps, p);
-  return cudaGetLastError();
+  return launch_pdl(ffn_kernel<BN, STAGES, KCH>, dim3(dc.num_sms), dim3(kFfnThreads), SM::kTotal, s, maps, p);
 }
 
 }  // namespace

@@ -8,6 +8,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace lsv {
 
 typedef __nv_bfloat16 bf16;
@@ -31,9 +33,11 @@ uint64_t wait_limit_ns();
 // ---------------------------------------------------------------- FFN tile table
 // int32 table in the workspace, written by the prep kernel, read by the FFN kernel.
 //   [0] gate/up items  [1] down items  [2] groups G  [3] next item to deal (zeroed by the prep kernel)
-//   [8 .. 8+G]             gate/up item start per group (exclusive scan, G+1 entries)
-//   [8+G+1 .. 8+2G+1]      down item start per group (G+1 entries)
-//   [8+2G+2 .. 8+3G+1]     completed gate/up items per group (zeroed by the prep kernel)
+//   [8 .. 8+G]             gate/up item start per group slot (exclusive scan, G+1 entries)
+//   [8+G+1 .. 8+2G+1]      down item start per group slot (G+1 entries)
+//   [8+2G+2 .. 8+3G+1]     completed gate/up items per group slot (zeroed by the prep kernel)
+// Group slots are the dealing order: the shared group first (when S > 0), then
+// routed experts 0..E-1.
 inline int table_ints(int G) { return 8 + 3 * G + 2; }
 
 struct FfnGeom {
@@ -49,6 +53,25 @@ struct WsLayout {
 WsLayout ws_layout(int T, int H, int E, int k, int S, int I);
 
 constexpr int kPermChunk = 8192;  // (token, slot) entries per permutation block
+
+// Launch with programmatic stream serialization: the kernel may start while its
+// predecessor in the stream finishes; it must call pdl_wait() before touching
+// memory the predecessor writes or reads.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int k, int32_t* idx, float* w,

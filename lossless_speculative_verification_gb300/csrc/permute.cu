@@ -25,6 +25,8 @@ constexpr int kWarps = kThreads / 32;
 __global__ void __launch_bounds__(kThreads) permute_count_kernel(const int32_t* __restrict__ idx, int n, int E,
                                                                  int32_t* __restrict__ blk_counts, int* err) {
   __shared__ int cnt[kMaxExperts];
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e < E; e += kThreads) cnt[e] = 0;
   __syncthreads();
   const int begin = blockIdx.x * kPermChunk;
@@ -77,6 +79,8 @@ __global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
   __shared__ int base[kMaxExperts];
   __shared__ int wcnt[kWarps][kMaxExperts];
 
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int begin = blockIdx.x * kPermChunk;
   const int end = min(n, begin + kPermChunk);
@@ -155,13 +159,11 @@ cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* cou
                            cudaStream_t s) {
   const int n = T * k;
   if (nblk > 1) {
-    permute_count_kernel<<<nblk, kThreads, 0, s>>>(idx, n, E, blk_counts, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(permute_count_kernel, dim3(nblk), dim3(kThreads), 0, s, idx, n, E, blk_counts, err);
     if (e != cudaSuccess) return e;
   }
-  permute_scatter_kernel<<<nblk, kThreads, 0, s>>>(idx, n, E, nblk, blk_counts, counts, offsets, perm, inv,
-                                                   err);
-  return cudaGetLastError();
+  return launch_pdl(permute_scatter_kernel, dim3(nblk), dim3(kThreads), 0, s, idx, n, E, nblk,
+                    (const int32_t*)blk_counts, counts, offsets, perm, inv, err);
 }
 
 }  // namespace lsv

@@ -218,6 +218,13 @@ __device__ __forceinline__ int named_bar_red_or(int id, int nthreads, int pred) 
   return r;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue now, and wait until the previous kernel has completed and its
+// memory is visible.  Both are no-ops for a kernel launched without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 }  // namespace lsv

@@ -6,7 +6,7 @@
 // (jina-ocr-v1: "64 routed experts ... Top-6 routing", kg.zhiyong.dev, section
 // "The speed comes from three layers working together".)
 //
-// One CTA takes TT tokens.  Warp w computes experts 8w..8w+7 (then 8w+64..)
+// One CTA takes TT tokens.  Warp w computes experts 4w..4w+3 (then 4w+64..)
 // for all TT tokens; inside a warp each lane owns a contiguous 8-element slice
 // of every 256-element block of h (16-byte loads of x and W), and the 32
 // partial sums are combined by a fixed butterfly.  The summation order is fixed, so
@@ -20,7 +20,8 @@
 namespace lsv {
 namespace {
 
-constexpr int kRouteWarps = 8;
+constexpr int kRouteWarps = 16;
+constexpr int kExpPerWarp = 4;
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -38,23 +39,25 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
                                                                  float* __restrict__ w,
                                                                  float* __restrict__ logits) {
   __shared__ float lg[TT][kMaxExperts];
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * TT;
   const int nt = min(TT, T - t0);
   const int n8 = H / 8;  // 16-byte groups per row
 
-  // warp w owns experts [8w, 8w+8), [8w+64, 8w+72), ...: eight independent rows in flight per step
-  for (int e0 = warp * 8; e0 < E; e0 += kRouteWarps * 8) {
-    float acc[8][TT];
+  // warp w owns experts [4w, 4w+4), [4w+64, 4w+68), ...: four independent rows in flight per step
+  for (int e0 = warp * kExpPerWarp; e0 < E; e0 += kRouteWarps * kExpPerWarp) {
+    float acc[kExpPerWarp][TT];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int q = 0; q < kExpPerWarp; ++q)
 #pragma unroll
       for (int i = 0; i < TT; ++i) acc[q][i] = 0.0f;
-#pragma unroll 2
+#pragma unroll 5
     for (int c = lane; c < n8; c += 32) {
-      uint4 wv[8];
+      uint4 wv[kExpPerWarp];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
+      for (int q = 0; q < kExpPerWarp; ++q)
         wv[q] = (e0 + q < E) ? __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + q) * H) + c)
                              : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -63,7 +66,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
           float xf[8];
           bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + c), xf);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < kExpPerWarp; ++q) {
             float wf[8];
             bf16x8_to_f32(wv[q], wf);
 #pragma unroll
@@ -73,7 +76,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
       }
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int q = 0; q < kExpPerWarp; ++q)
 #pragma unroll
       for (int i = 0; i < TT; ++i) {
         float v = acc[q][i];
@@ -133,13 +136,10 @@ cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int
   if (T == 0) return cudaSuccess;
   const dim3 block(kRouteWarps * 32);
   // about one CTA per SM at decode sizes; more tokens per CTA once T is large
-  if (T <= 256)
-    route_kernel<1><<<T, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
-  else if (T <= 1024)
-    route_kernel<4><<<(T + 3) / 4, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
-  else
-    route_kernel<8><<<(T + 7) / 8, block, 0, s>>>(x, wr, T, H, E, k, idx, w, logits);
-  return cudaGetLastError();
+  if (T <= 256) return launch_pdl(route_kernel<1>, dim3(T), block, 0, s, x, wr, T, H, E, k, idx, w, logits);
+  if (T <= 1024)
+    return launch_pdl(route_kernel<4>, dim3((T + 3) / 4), block, 0, s, x, wr, T, H, E, k, idx, w, logits);
+  return launch_pdl(route_kernel<8>, dim3((T + 7) / 8), block, 0, s, x, wr, T, H, E, k, idx, w, logits);
 }
 
 }  // namespace lsv
