@@ -17,7 +17,8 @@
  *     pointer is documented as optional and passed as NULL.
  *   - bf16 tensors are passed as `const void*` / `void*` holding IEEE bfloat16.
  *   - The caller owns all memory.  The library allocates no device memory; it
- *     keeps one device error word per device and nothing else.
+ *     keeps one device error word per device and the fixed scratch array of
+ *     spec_verify_accept_noalloc (128 KiB per device), and nothing else.
  *   - Work is enqueued asynchronously on `stream` (NULL = the legacy default
  *     stream).  Argument errors are returned synchronously BEFORE any launch,
  *     with outputs untouched.  Errors found by kernels (an index out of range,
@@ -145,6 +146,30 @@ size_t spec_verify_workspace_size(int32_t B, int32_t K, int32_t V);
 lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t B, int32_t K, int32_t V,
                               int32_t *argmax_opt, int32_t *accept_len, int32_t *committed, void *ws,
                               size_t ws_bytes, lsv_stream stream);
+
+/* spec_verify_accept without a workspace, for callers that cannot allocate
+ * device memory when they verify: code that must not call cudaMalloc inside a
+ * stream capture or a latency-critical decode loop, and plugin-style hosts
+ * that give a kernel neither an allocator nor a workspace.  The paper has no
+ * counterpart; this is a convenience of the library.
+ *   Same arguments, rule and outputs as spec_verify_accept, minus ws/ws_bytes.
+ *   The argmax partials live in one fixed device array of 128 KiB (16,384
+ *   (max, index) pairs), held by every device that loads the library until
+ *   the process exits.  A problem needing more partials returns
+ *   LSV_ERR_UNSUPPORTED before any launch; the count is B*(K+1) rows times
+ *   the chunks per row (on a 152-SM GB300 about 10 chunks per row at 128 rows
+ *   of 129,280 logits, 1 chunk per row beyond 1,216 rows, so up to 16,384 rows).
+ *   The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *   routine.  The first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress) and caches it; make that first call before
+ *   any stream capture.  All calls on a device share the array and it keeps
+ *   the previous call's contents; nothing in it needs to start at zero, since
+ *   each call writes every partial it reads.  Calls that overlap on the GPU
+ *   (different streams, no ordering between them) race on the array: order
+ *   them on one stream or with events. */
+lsv_status spec_verify_accept_noalloc(const void *logits, const int32_t *drafts, int32_t B, int32_t K, int32_t V,
+                                      int32_t *argmax_opt, int32_t *accept_len, int32_t *committed,
+                                      lsv_stream stream);
 
 /* Residual update and normalisation between stacked layers:
  *   x[t,:] <- bf16(x[t,:] + y[t,:]);   h[t,:] = bf16(x[t,:] / sqrt(mean(x[t,:]^2) + eps))

@@ -137,6 +137,19 @@ def spec_verify_accept(logits, drafts, ws, argmax=None, accept_len=None, committ
     return accept_len, committed
 
 
+def spec_verify_accept_noalloc(logits, drafts, argmax=None, accept_len=None, committed=None, stream=None):
+    """spec_verify_accept without a workspace: its scratch is a fixed array inside the library."""
+    _need(logits, torch.bfloat16, "logits"); _need(drafts, torch.int32, "drafts")
+    B, K1, V = logits.shape
+    dev = logits.device
+    accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
+    committed = torch.empty((B, K1), dtype=torch.int32, device=dev) if committed is None else committed
+    check("spec_verify_accept_noalloc", _ffi.load().spec_verify_accept_noalloc(
+        _ptr(logits), _ptr(drafts), B, K1 - 1, V, _ptr(argmax), _ptr(accept_len), _ptr(committed),
+        _stream(stream)))
+    return accept_len, committed
+
+
 def rmsnorm_residual(x, y, h=None, eps=1e-6, stream=None):
     _need(x, torch.bfloat16, "x"); _need(y, torch.bfloat16, "y")
     T, H = x.shape

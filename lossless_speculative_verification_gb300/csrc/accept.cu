@@ -15,7 +15,10 @@
 // No atomics decide anything, so the result is deterministic.
 #include <limits.h>
 
+#include <mutex>
+
 #include "internal.h"
+#include "lsv.h"
 #include "ptx.cuh"
 
 namespace lsv {
@@ -187,3 +190,60 @@ cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int 
 }
 
 }  // namespace lsv
+
+// ----------------------------------------------------------------------------- no-allocation variant
+// Some callers cannot allocate device memory at the point where they verify
+// drafts: code that must not call cudaMalloc while a stream is being captured
+// or while a latency-critical decode loop runs, and plugin-style hosts that
+// hand a kernel neither an allocator nor a workspace.  For them the chunk
+// partials of the argmax live in this fixed array instead of a caller
+// workspace.  It exists once per device that loads the library and stays
+// allocated until the process exits.
+namespace lsv {
+namespace {
+constexpr int kNoAllocPartials = 16384;  // (max, index) pairs: 128 KiB in total
+static __device__ __align__(256) unsigned char g_noalloc_scratch[2 * kNoAllocPartials * 4];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of the scratch array for the current device.  The first call
+// on a device resolves it (host code may not use the array's name as an
+// address); later calls reuse the cached value.
+cudaError_t noalloc_scratch(int device, void** out) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[device]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[device] = p;
+  }
+  *out = g_noalloc_addr[device];
+  return cudaSuccess;
+}
+}  // namespace
+}  // namespace lsv
+
+extern "C" lsv_status spec_verify_accept_noalloc(const void* logits, const int32_t* drafts, int32_t B, int32_t K,
+                                                 int32_t V, int32_t* argmax_opt, int32_t* accept_len,
+                                                 int32_t* committed, lsv_stream stream) {
+  using namespace lsv;
+  if (B < 0 || K < 0 || V <= 0) return LSV_ERR_INVALID_ARG;
+  if (K + 1 > kMaxVerifyRows || (long long)B * (K + 1) >= (1ll << 31)) return LSV_ERR_UNSUPPORTED;
+  if (B == 0) return LSV_OK;
+  if (!logits || !accept_len || !committed || (K > 0 && !drafts)) return LSV_ERR_INVALID_ARG;
+  const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (!a16(logits) || !a16(drafts) || !a16(argmax_opt) || !a16(accept_len) || !a16(committed))
+    return LSV_ERR_MISALIGNED;
+  DeviceCtx* dc = nullptr;
+  if (device_ctx(&dc) != cudaSuccess) return LSV_ERR_CUDA;
+  // problems whose partials do not fit the fixed array are refused, never truncated
+  if (accept_ws_bytes(B, K, V, dc->num_sms) > sizeof(g_noalloc_scratch)) return LSV_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (noalloc_scratch(dc->device, &scratch) != cudaSuccess) return LSV_ERR_CUDA;
+  return launch_accept(static_cast<const bf16*>(logits), drafts, B, K, V, argmax_opt, accept_len, committed, scratch,
+                       *dc, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LSV_OK
+             : LSV_ERR_CUDA;
+}
