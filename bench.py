@@ -129,24 +129,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def ffn_source_hash():
+def layer_source_hash():
     h = hashlib.sha256()
-    for f in ("ffn.cu", "ptx.cuh"):
+    for f in ("ffn.cu", "ptx.cuh", "prefetch.cu", "route.cu", "permute.cu", "combine.cu", "ffn_plan.cuh", "api.cu"):
         with open(os.path.join(ROOT, "lossless_speculative_verification_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_hash):
-    """DRAM bytes per FFN launch from the committed ncu summary, if it was taken on this kernel source."""
-    path = os.path.join(ROOT, "profiles", "ffn_decode_traffic.json")
+    """DRAM bytes of one layer (sum over its launches) from the committed ncu summary, if it was
+    taken on this source."""
+    path = os.path.join(ROOT, "profiles", "layer_decode_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     if d.get("kernel_source_hash") != kernel_hash:
         return None
-    return d.get("dram_bytes_per_launch")
+    return d.get("dram_bytes_per_layer")
 
 
 # ----------------------------------------------------------------------------- reference arm (CPU oracle)
@@ -250,36 +251,22 @@ def run_ours(args, rank, world, local):
 
     T, k = d.T, d.k
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    tw = torch.empty((T, k), dtype=torch.float32, device=dev)
     counts = torch.empty(d.E, dtype=torch.int32, device=dev)
-    offsets = torch.empty(d.E + 1, dtype=torch.int32, device=dev)
-    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
-    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
-    y_perm = torch.empty((T * k, d.H), dtype=torch.float32, device=dev)
-    y_sh = torch.empty((T, d.H), dtype=torch.float32, device=dev)
     out = torch.empty((T, d.H), dtype=torch.bfloat16, device=dev)
     alen = torch.empty(w.B, dtype=torch.int32, device=dev)
     comm = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
-    lib = api._ffi.load()
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 7   # route, permute, ffn prep, ffn, combine, argmax partials, accept
+    # launches per step: route, permute+gather, grouped experts, combine | argmax partials, accept
+    launches_per_step = 6
 
-    def part_a():
-        # the launches moe_verify_layer makes, called one by one so that the FFN span can be timed
-        api.moe_route(x, W[0], k, topk_idx=idx, topk_w=tw)
-        api._ffi.check("moe_permute", lib.moe_permute(api._ptr(idx), api.ctypes.byref(sh), api._ptr(counts),
-                                                      api._ptr(offsets), api._ptr(perm), api._ptr(inv),
-                                                      api._ptr(ws), ws.numel(), api._stream()))
+    def layer():
+        api.moe_verify_layer(x, wts, sh, ws, out=out, topk_idx=idx, counts=counts)
 
-    def part_b():
-        api.moe_grouped_ffn(x, perm, offsets, counts, wts, sh, ws, y_perm=y_perm, y_shared=y_sh)
-
-    def part_c():
-        api.moe_combine(y_perm, inv, tw, y_sh, sh, out=out)
+    def accept():
         api.spec_verify_accept(logits, drafts, aws, accept_len=alen, committed=comm)
 
     for _ in range(max(args.warmup, 0)):
-        part_a(); part_b(); part_c()
+        layer(); accept()
     torch.cuda.synchronize()
     assert api.get_device_error() == 0
 
@@ -289,14 +276,14 @@ def run_ours(args, rank, world, local):
         flush.fill_(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        part_a(); part_b(); part_c()
+        layer(); accept()
         b.record(stream)
         b.synchronize()
         eager_ms.append(a.elapsed_time(b))
 
-    # the step as three CUDA graphs (routing | grouped experts | combine + acceptance)
-    graphs = [torch.cuda.CUDAGraph() for _ in range(3)]
-    for g, fn in zip(graphs, (part_a, part_b, part_c)):
+    # the step as two CUDA graphs: the MoE layer (one PDL chain) and the acceptance
+    graphs = [torch.cuda.CUDAGraph() for _ in range(2)]
+    for g, fn in zip(graphs, (layer, accept)):
         with torch.cuda.graph(g):
             fn()
     for _ in range(max(args.warmup, 0)):
@@ -306,14 +293,13 @@ def run_ours(args, rank, world, local):
     assert api.get_device_error() == 0
 
     n_touched = int((counts > 0).sum().item())
-    H, I, S = d.H, d.I, d.S
-    w_bytes = (n_touched + S) * 3 * H * I * 2
-    tok_bytes = T * H * 2 + T * k * H * 4 + T * H * 4
-    ffn_bytes = w_bytes + tok_bytes
+    H, I, S, E = d.H, d.I, d.S, d.E
+    # algorithmic bytes of the layer: router + touched routed + shared expert weights, x in, out
+    layer_bytes = E * H * 2 + (n_touched + S) * 3 * H * I * 2 + 2 * T * H * 2
+    accept_bytes = w.B * (w.K + 1) * w.V * 2
 
-    # timed region: per step, flush L2 (untimed), then events around the step
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    fevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # timed region: per step, flush L2 (untimed), then events around the two graphs
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -330,19 +316,18 @@ def run_ours(args, rank, world, local):
             flush.fill_(i & 0xFF)
             evs[i][0].record(stream)
             graphs[0].replay()
-            fevs[i][0].record(stream)
-            graphs[1].replay()
-            fevs[i][1].record(stream)
-            graphs[2].replay()
             evs[i][1].record(stream)
+            graphs[1].replay()
+            evs[i][2].record(stream)
         t_end = time.perf_counter() + 0.3
         while time.perf_counter() < t_end:
             flush.fill_(0)
             for g in graphs:
                 g.replay()
         torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    ffn_ms = [a.elapsed_time(b) for a, b in fevs]
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    layer_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    accept_ms = [e[1].elapsed_time(e[2]) for e in evs]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -400,9 +385,10 @@ def run_ours(args, rank, world, local):
     tokens = T * world * args.steps
     value = tokens / (total_ms / 1e3)
     peak, peak_kind = peaks()
-    ffn_avg = sum(ffn_ms) / len(ffn_ms)
-    achieved = ffn_bytes / (ffn_avg / 1e3) / 1e9
-    khash = ffn_source_hash()
+    layer_avg = sum(layer_ms) / len(layer_ms)
+    accept_avg = sum(accept_ms) / len(accept_ms)
+    achieved = layer_bytes / (layer_avg / 1e3) / 1e9
+    khash = layer_source_hash()
     traffic = ncu_traffic(khash)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -412,13 +398,17 @@ def run_ours(args, rank, world, local):
                                "then greedy acceptance over [32,4,129280] bf16 logits",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (256 MB write, outside the events)",
-                   "timing": "step replayed as 3 CUDA graphs, CUDA events per step",
+                   "timing": "step replayed as 2 CUDA graphs (layer, acceptance), CUDA events per step",
                    "clocks_window": "nvidia-smi every 100 ms over back-to-back steps around the timed ones",
                    "eager_ms_per_step": sum(eager_ms) / len(eager_ms)},
-        "roofline": {"bound": "hbm", "kernel": "ffn_kernel (grouped SwiGLU experts, tcgen05) incl. its gather prep",
+        "roofline": {"bound": "hbm",
+                     "kernel": "moe_verify_layer: router, permute+gather, grouped SwiGLU experts (tcgen05), "
+                               "combine; one PDL-chained launch sequence (the experts kernel carries the HBM stream)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_kind, "traffic": traffic, "algorithmic_bytes": ffn_bytes,
-                     "touched_experts": n_touched, "ffn_ms": ffn_avg, "kernel_source_hash": khash},
+                     "peak_source": peak_kind, "traffic": traffic, "algorithmic_bytes": layer_bytes,
+                     "touched_experts": n_touched, "layer_ms": layer_avg, "kernel_source_hash": khash,
+                     "accept": {"ms": accept_avg, "algorithmic_bytes": accept_bytes,
+                                "achieved_gbs": accept_bytes / (accept_avg / 1e3) / 1e9}},
         "e2e": {"value": T * world * args.steps / (e2e_total / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

@@ -79,6 +79,16 @@ typedef struct {
  * `shape` (a multiple of 256).  Returns 0 for an unsupported shape. */
 size_t lsv_workspace_size(const lsv_moe_shape *shape);
 
+/* Start streaming expert weights into L2, in the order moe_grouped_ffn reads
+ * them (shared gate/up, routed gate/up, shared down, routed down), up to
+ * max_bytes.  Returns at once; the data arrives while later work on the stream
+ * runs.  A hint only: results never depend on it.  Useful when the caller
+ * has independent work to overlap with it (for instance the attention block
+ * before the MoE FFN); moe_verify_layer does not issue it, because its own
+ * next kernel would wait for the prefetch grid to finish. */
+lsv_status moe_prefetch_weights(const lsv_moe_weights *weights, const lsv_moe_shape *shape, size_t max_bytes,
+                                lsv_stream stream);
+
 /* Router: logits[t,e] = sum_h x[t,h] W_r[e,h] (fp32 accumulation in increasing
  * h); gate p = softmax over all E experts in fp32 (NOT renormalised over the
  * selection); the k experts with the largest logits in descending order, ties

@@ -38,6 +38,7 @@ WEIGHTS_P = ctypes.POINTER(MoeWeights)
 
 SIGNATURES = {
     "lsv_workspace_size": (SZ, [SHAPE_P]),
+    "moe_prefetch_weights": (I32, [WEIGHTS_P, SHAPE_P, SZ, P]),
     "moe_route": (I32, [P, P, SHAPE_P, P, P, P, P]),
     "moe_permute": (I32, [P, SHAPE_P, P, P, P, P, P, SZ, P]),
     "moe_grouped_ffn": (I32, [P, P, P, P, WEIGHTS_P, SHAPE_P, P, P, P, SZ, P]),

@@ -61,6 +61,11 @@ def workspace(sh: MoeShape, device=None) -> torch.Tensor:
     return torch.empty(workspace_size(sh), dtype=torch.uint8, device=device or "cuda")
 
 
+def moe_prefetch_weights(w: MoeWeights, sh: MoeShape, max_bytes: int, stream=None) -> None:
+    check("moe_prefetch_weights", _ffi.load().moe_prefetch_weights(ctypes.byref(w), ctypes.byref(sh), max_bytes,
+                                                                   _stream(stream)))
+
+
 def moe_route(x, w_router, k, topk_idx=None, topk_w=None, logits=None, stream=None):
     _need(x, torch.bfloat16, "x"); _need(w_router, torch.bfloat16, "w_router")
     T, H = x.shape

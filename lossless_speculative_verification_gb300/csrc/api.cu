@@ -44,9 +44,13 @@ cudaError_t device_ctx(DeviceCtx** out) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    int l2 = 0;
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess) return e;
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_error);
     if (e != cudaSuccess) return e;
+    c.l2_bytes = l2;
     c.num_sms = sms;
     c.err = static_cast<int*>(p);
     c.device = dev;
@@ -112,6 +116,22 @@ lsv_status check_shape(const lsv_moe_shape* s) {
 
 lsv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LSV_OK : LSV_ERR_CUDA; }
 
+// L2 prefetch budget of moe_verify_layer, as a percentage of L2.  Measured on
+// GB300 at the decode shape (T=128): 0 % gives a 101.5 us layer, 30/60/80 %
+// all give 117.9 us, because the router waits for the prefetch grid to
+// complete before it starts.  So the layer does not prefetch by default;
+// moe_prefetch_weights stays available for callers that can issue it earlier
+// (for instance before the attention block of the same decoder layer).
+#ifndef LSV_PREFETCH_L2_PCT
+#define LSV_PREFETCH_L2_PCT 0
+#endif
+uint64_t default_prefetch_bytes(const DeviceCtx& dc, int T, int E, int k, int S, int I, int H) {
+  const uint64_t shared = (uint64_t)3 * S * I * H * 2;
+  const uint64_t cap = (uint64_t)dc.l2_bytes * LSV_PREFETCH_L2_PCT / 100;
+  if ((long long)T * k >= 2ll * E) return cap;
+  return shared < cap ? shared : cap;
+}
+
 }  // namespace
 
 extern "C" {
@@ -165,6 +185,22 @@ lsv_status lsv_selftest_wait_timeout(uint64_t limit_ns, lsv_stream stream) {
   DeviceCtx* dc = nullptr;
   if (device_ctx(&dc) != cudaSuccess) return LSV_ERR_CUDA;
   return from_cuda(launch_wait_selftest(dc->err, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lsv_status moe_prefetch_weights(const lsv_moe_weights* wt, const lsv_moe_shape* shape, size_t max_bytes,
+                                lsv_stream stream) {
+  lsv_status st = check_shape(shape);
+  if (st != LSV_OK) return st;
+  if (!wt) return LSV_ERR_INVALID_ARG;
+  if (max_bytes == 0) return LSV_OK;
+  if (!aligned16(wt->w_gate_up) || !aligned16(wt->w_down) || !aligned16(wt->ws_gate_up) || !aligned16(wt->ws_down))
+    return LSV_ERR_MISALIGNED;
+  DeviceCtx* dc = nullptr;
+  if (device_ctx(&dc) != cudaSuccess) return LSV_ERR_CUDA;
+  return from_cuda(launch_weight_prefetch(static_cast<const bf16*>(wt->w_gate_up), static_cast<const bf16*>(wt->w_down),
+                                          static_cast<const bf16*>(wt->ws_gate_up), static_cast<const bf16*>(wt->ws_down),
+                                          shape->H, shape->E, shape->S, shape->I, max_bytes, *dc,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 lsv_status moe_route(const void* x, const void* w_router, const lsv_moe_shape* shape, int32_t* topk_idx,
@@ -276,15 +312,29 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   int32_t* inv = reinterpret_cast<int32_t*>(w + L.inv);
   float* y_perm = reinterpret_cast<float*>(w + L.y_perm);
   float* y_sh = reinterpret_cast<float*>(w + L.y_sh);
-  cudaError_t e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx,
-                               tw, nullptr, s);
+  const bf16* wgu = static_cast<const bf16*>(wt->w_gate_up);
+  const bf16* wdn = static_cast<const bf16*>(wt->w_down);
+  const bf16* wsgu = static_cast<const bf16*>(wt->ws_gate_up);
+  const bf16* wsdn = static_cast<const bf16*>(wt->ws_down);
+  cudaError_t e = cudaSuccess;
+  const uint64_t pf = default_prefetch_bytes(*dc, T, E, k, S, I, H);
+  if (pf) e = launch_weight_prefetch(wgu, wdn, wsgu, wsdn, H, E, S, I, pf, *dc, s);
   if (e == cudaSuccess)
-    e = launch_permute(idx, T, k, E, counts, offsets, perm, inv, reinterpret_cast<int32_t*>(w + L.blk_counts),
-                       L.nblk, dc->err, s);
+    e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,
+                     nullptr, s);
+  const bool fused = L.nblk == 1;  // up to kPermChunk pairs: permutation, gather and plan in one launch
+  if (e == cudaSuccess) {
+    if (fused)
+      e = launch_permute_gather(idx, T, k, E, H, S, I, ffn_token_tile(T, k, E), static_cast<const bf16*>(x), counts,
+                                offsets, perm, inv, reinterpret_cast<bf16*>(w + L.xperm),
+                                reinterpret_cast<int32_t*>(w + L.table), dc->err, s);
+    else
+      e = launch_permute(idx, T, k, E, counts, offsets, perm, inv, reinterpret_cast<int32_t*>(w + L.blk_counts),
+                         L.nblk, dc->err, s);
+  }
   if (e == cudaSuccess)
-    e = launch_ffn(static_cast<const bf16*>(x), perm, offsets, static_cast<const bf16*>(wt->w_gate_up),
-                   static_cast<const bf16*>(wt->w_down), static_cast<const bf16*>(wt->ws_gate_up),
-                   static_cast<const bf16*>(wt->ws_down), T, H, E, k, S, I, y_perm, y_sh, w, L, *dc, s);
+    e = launch_ffn(static_cast<const bf16*>(x), perm, offsets, wgu, wdn, wsgu, wsdn, T, H, E, k, S, I, y_perm, y_sh, w,
+                   L, *dc, s, /*with_prep=*/!fused);
   if (e == cudaSuccess)
     e = launch_combine(y_perm, inv, tw, S > 0 ? y_sh : nullptr, T, H, k, static_cast<bf16*>(out), dc->err, s);
   return from_cuda(e);

@@ -35,6 +35,7 @@
 // finished gate/up items; the wait always ends, because every gate/up item of
 // that group was dealt earlier to a running CTA whose progress on it depends
 // on nothing else.
+#include "ffn_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -88,12 +89,6 @@ struct Item {
   int nk;    // 64-wide K chunks
   int need;  // gate/up items of group g (for a down item's dependency)
 };
-
-// Dealing order of the groups: the shared group (the largest items) first, then
-// the routed experts in index order.
-__host__ __device__ __forceinline__ int slot_group(int slot, int E, int S) {
-  return S > 0 ? (slot == 0 ? E : slot - 1) : slot;
-}
 
 template <int BN>
 __device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
@@ -478,75 +473,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
       for (int c = lane; c < H / 8; c += 32) d[c] = __ldg(s + c);
     }
   }
-  if (blockIdx.x == 0 && threadIdx.x < 32) {
-    const int G = E + (S > 0 ? 1 : 0);
-    const int nft_dn = (H + 127) / 128;
-    // 9 groups per lane covers G <= 257 + 31
-    constexpr int PER = (kMaxExperts + 1 + 31) / 32;
-    int gu_loc[PER], dn_loc[PER];
-    int gu_sum = 0, dn_sum = 0;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int slot = lane * PER + j;
-      const int g = slot < G ? slot_group(slot, E, S) : G;
-      int ntt = 0, nft_gu = 0;
-      if (g < E) {
-        const int c = offsets[g + 1] - offsets[g];
-        ntt = (c + BN - 1) / BN;
-        nft_gu = I / 64;
-      } else if (g < G) {
-        ntt = (T + BN - 1) / BN;
-        nft_gu = S * I / 64;
-      }
-      gu_loc[j] = ntt * nft_gu;
-      dn_loc[j] = ntt * nft_dn;
-      gu_sum += gu_loc[j];
-      dn_sum += dn_loc[j];
-    }
-    // the offsets must describe a partition of [0, T*k); otherwise no item is scheduled
-    int bad = 0;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int g = lane * PER + j;
-      if (g < E && (offsets[g] > offsets[g + 1])) bad = 1;
-    }
-    if (lane == 0 && (offsets[0] != 0 || offsets[E] != nrows)) bad = 1;
-    bad = __any_sync(0xffffffffu, bad);
-    if (bad) {
-      gu_sum = dn_sum = 0;
-#pragma unroll
-      for (int j = 0; j < PER; ++j) gu_loc[j] = dn_loc[j] = 0;
-      if (lane == 0) set_error(err, kErrDeviceIndex);
-    }
-    int gu_incl = gu_sum, dn_incl = dn_sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, gu_incl, o);
-      const int b = __shfl_up_sync(0xffffffffu, dn_incl, o);
-      if (lane >= o) {
-        gu_incl += a;
-        dn_incl += b;
-      }
-    }
-    int gu_run = gu_incl - gu_sum, dn_run = dn_incl - dn_sum;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int slot = lane * PER + j;
-      if (slot <= G) {
-        table[8 + slot] = gu_run;
-        table[8 + G + 1 + slot] = dn_run;
-      }
-      if (slot < G) table[8 + 2 * G + 2 + slot] = 0;
-      gu_run += gu_loc[j];
-      dn_run += dn_loc[j];
-    }
-    if (lane == 31) {
-      table[0] = gu_incl;
-      table[1] = dn_incl;
-      table[2] = G;
-      table[3] = 0;  // next item to deal
-    }
-  }
+  if (blockIdx.x == 0 && threadIdx.x < 32) build_item_table(offsets, T, H, E, k, S, I, BN, table, err);
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -585,7 +512,7 @@ template <int BN, int STAGES, int KCH>
 cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                     const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E, int k,
                     int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
-                    const DeviceCtx& dc, cudaStream_t s) {
+                    const DeviceCtx& dc, cudaStream_t s, bool with_prep) {
   using SM = Smem<BN, STAGES, KCH>;
   static_assert(SM::kTotal <= 232448, "shared memory budget");
   static int attr_done[64] = {0};
@@ -602,10 +529,12 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   const int G = E + (S > 0 ? 1 : 0);
   const int nrows = T * k;
 
-  const int prep_blocks = max(1, (nrows + 7) / 8);
-  cudaError_t e = launch_pdl(ffn_prep_kernel<BN>, dim3(prep_blocks), dim3(256), 0, s, x, perm, offsets, T, H, E, k,
-                             S, I, xperm, table, dc.err);
-  if (e != cudaSuccess) return e;
+  if (with_prep) {
+    const int prep_blocks = max(1, (nrows + 7) / 8);
+    const cudaError_t e = launch_pdl(ffn_prep_kernel<BN>, dim3(prep_blocks), dim3(256), 0, s, x, perm, offsets, T,
+                                     H, E, k, S, I, xperm, table, dc.err);
+    if (e != cudaSuccess) return e;
+  }
 
   FfnMaps maps;
   const int SI = S > 0 ? S * I : 64;
@@ -648,20 +577,20 @@ int ffn_token_tile(int T, int k, int E) {
 cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                        const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
                        int k, int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
-                       const DeviceCtx& dc, cudaStream_t s) {
+                       const DeviceCtx& dc, cudaStream_t s, bool with_prep) {
   switch (ffn_token_tile(T, k, E)) {
     case 32:
       return run_ffn<32, LSV_FFN_STAGES32, LSV_FFN_KCH32>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down,
-                                                          T, H, E, k, S, I, y_perm, y_sh, ws, L, dc, s);
+                                                          T, H, E, k, S, I, y_perm, y_sh, ws, L, dc, s, with_prep);
     case 64:
       return run_ffn<64, 4, 2>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                               y_sh, ws, L, dc, s);
+                               y_sh, ws, L, dc, s, with_prep);
     case 128:
       return run_ffn<128, 6, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                                y_sh, ws, L, dc, s);
+                                y_sh, ws, L, dc, s, with_prep);
     default:
       return run_ffn<256, 4, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                                y_sh, ws, L, dc, s);
+                                y_sh, ws, L, dc, s, with_prep);
   }
 }
 

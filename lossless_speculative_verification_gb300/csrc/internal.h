@@ -25,6 +25,7 @@ constexpr int kMaxVerifyRows = 64;  // K + 1 per sequence
 struct DeviceCtx {
   int device = -1;
   int num_sms = 0;
+  int l2_bytes = 0;
   int* err = nullptr;
 };
 cudaError_t device_ctx(DeviceCtx** out);
@@ -81,11 +82,25 @@ cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* cou
                            int32_t* perm, int32_t* inv, int32_t* blk_counts, int nblk, int* err,
                            cudaStream_t s);
 
+// Permutation + row gather + item table in one launch (T*k <= kPermChunk).
+cudaError_t launch_permute_gather(const int32_t* idx, int T, int k, int E, int H, int S, int I, int BN,
+                                  const bf16* x, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                  bf16* xperm, int32_t* table, int* err, cudaStream_t s);
+
+// Bulk L2 prefetch of the expert weights in the order the grouped-expert kernel
+// consumes them (shared gate/up, routed gate/up, shared down, routed down), up
+// to `budget` bytes.
+cudaError_t launch_weight_prefetch(const bf16* w_gate_up, const bf16* w_down, const bf16* ws_gate_up,
+                                   const bf16* ws_down, int H, int E, int S, int I, uint64_t budget,
+                                   const DeviceCtx& dc, cudaStream_t s);
+
 int ffn_token_tile(int T, int k, int E);
+// Grouped experts.  with_prep: first gather the routed rows and build the item
+// table (otherwise launch_permute_gather already did).
 cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                        const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
                        int k, int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
-                       const DeviceCtx& dc, cudaStream_t s);
+                       const DeviceCtx& dc, cudaStream_t s, bool with_prep = true);
 
 cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_sh,
                            int T, int H, int k, bf16* out, int* err, cudaStream_t s);

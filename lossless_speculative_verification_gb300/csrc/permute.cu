@@ -13,6 +13,7 @@
 // derives every block's base per expert from them.  Inside a block, entries
 // are ranked a round of 1024 at a time: __match_any_sync groups equal experts
 // within a warp, and a per-expert scan over the 32 warps orders the warps.
+#include "ffn_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -152,7 +153,90 @@ __global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
   }
 }
 
+// Permutation, row gather and item table in one launch, for up to kPermChunk
+// pairs.  CTA c owns the 32 pairs [32c, 32c+32): it histograms all pairs
+// (cheap at these sizes) and, separately, the pairs before its slice, which
+// gives every expert's offset and the slice's base inside each expert segment;
+// warp 0 ranks the slice with __match_any_sync, and all warps copy the slice's
+// token rows into expert order.  CTA 0 also writes counts/offsets and the item
+// table of the grouped-expert kernel.
+constexpr int kPgThreads = 256;
+constexpr int kPgSlice = 32;
+
+__global__ void __launch_bounds__(kPgThreads) permute_gather_kernel(
+    const int32_t* __restrict__ idx, int T, int k, int E, int H, int S, int I, int BN, const bf16* __restrict__ x,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, bf16* __restrict__ xperm, int32_t* __restrict__ table, int* err) {
+  __shared__ int tot[kMaxExperts];
+  __shared__ int pre[kMaxExperts];
+  __shared__ int off[kMaxExperts + 1];
+  __shared__ int pos_s[kPgSlice];
+  pdl_wait();
+  pdl_trigger();
+  const int n = T * k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s0 = blockIdx.x * kPgSlice;
+  const int s1 = min(n, s0 + kPgSlice);
+  for (int e = tid; e < E; e += kPgThreads) {
+    tot[e] = 0;
+    pre[e] = 0;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kPgThreads) {
+    const int e = idx[i];
+    if (e < 0 || e >= E) {
+      if (blockIdx.x == 0) set_error(err, kErrDeviceIndex);
+      continue;
+    }
+    atomicAdd(&tot[e], 1);  // integer counts: independent of the order
+    if (i < s0) atomicAdd(&pre[e], 1);
+  }
+  __syncthreads();
+  if (warp == 0) warp_exclusive_scan(tot, off, E);
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = tid; e < E; e += kPgThreads) {
+      counts[e] = tot[e];
+      offsets[e] = off[e];
+    }
+    if (tid == 0) offsets[E] = off[E];
+  }
+  if (warp == 0) {
+    const int i = s0 + lane;
+    int e = i < s1 ? idx[i] : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int pos = -1;
+    if (e >= 0) {
+      pos = off[e] + pre[e] + rank;
+      perm[pos] = i;
+      inv[i] = pos;
+    }
+    pos_s[lane] = pos;
+  } else if (warp == 1 && blockIdx.x == 0) {
+    build_item_table(off, T, H, E, k, S, I, BN, table, err);
+  }
+  __syncthreads();
+  for (int j = warp; j < s1 - s0; j += kPgThreads / 32) {
+    const int pos = pos_s[j];
+    if (pos < 0) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)((s0 + j) / k) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xperm + (size_t)pos * H);
+    for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_permute_gather(const int32_t* idx, int T, int k, int E, int H, int S, int I, int BN,
+                                  const bf16* x, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                  bf16* xperm, int32_t* table, int* err, cudaStream_t s) {
+  const int n = T * k;
+  const int grid = n == 0 ? 1 : (n + kPgSlice - 1) / kPgSlice;
+  return launch_pdl(permute_gather_kernel, dim3(grid), dim3(kPgThreads), 0, s, idx, T, k, E, H, S, I, BN, x,
+                    counts, offsets, perm, inv, xperm, table, err);
+}
 
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                            int32_t* perm, int32_t* inv, int32_t* blk_counts, int nblk, int* err,
