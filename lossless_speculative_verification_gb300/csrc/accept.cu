@@ -25,7 +25,7 @@ namespace lsv {
 namespace {
 
 constexpr int kAccThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 constexpr int kChunkQuantum = kAccThreads * 8;  // elements covered by one 16-B load per thread
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -71,15 +71,19 @@ __global__ void __launch_bounds__(kAccThreads) argmax_partial_kernel(const bf16*
     // every thread walks its vectors in increasing index order
     const int n8 = (end - begin) >> 3;
     const uint4* p = reinterpret_cast<const uint4*>(row + begin);
-    int j = threadIdx.x;
-    for (; j + (kUnroll - 1) * kAccThreads < n8; j += kUnroll * kAccThreads) {
+    for (int j0 = threadIdx.x; j0 < n8; j0 += kUnroll * kAccThreads) {
       uint4 q[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) q[u] = ld_stream_v4(p + j + u * kAccThreads);
+      for (int u = 0; u < kUnroll; ++u) {
+        const int j = j0 + u * kAccThreads;
+        q[u] = j < n8 ? ld_stream_v4(p + j) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) scan8(q[u], begin + 8 * (j + u * kAccThreads), bv, bi);
+      for (int u = 0; u < kUnroll; ++u) {
+        const int j = j0 + u * kAccThreads;
+        if (j < n8) scan8(q[u], begin + 8 * j, bv, bi);
+      }
     }
-    for (; j < n8; j += kAccThreads) scan8(ld_stream_v4(p + j), begin + 8 * j, bv, bi);
     for (int e = begin + 8 * n8 + threadIdx.x; e < end; e += kAccThreads)
       better(__bfloat162float(row[e]), e, bv, bi);
   } else {
@@ -150,13 +154,15 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finalize_kernel(
 }
 
 int chunk_elems(int R, int V, int num_sms) {
-  // aim for about 8 resident CTAs per SM in one wave; at least one quantum per CTA
+  // one wave of about 8 resident CTAs per SM: pick the chunks per row first, then
+  // the chunk length (a multiple of 8 elements, so 16-byte loads stay aligned)
   const long long target = (long long)num_sms * 8;
-  long long per = ((long long)V * R + target - 1) / target;
-  per = ((per + kChunkQuantum - 1) / kChunkQuantum) * kChunkQuantum;
-  if (per < kChunkQuantum) per = kChunkQuantum;
-  if (per > V) per = ((V + 7) / 8) * 8;
-  if (per < 8) per = 8;
+  long long nchunk = target / (R > 0 ? R : 1);
+  const long long max_chunks = ((long long)V + kChunkQuantum - 1) / kChunkQuantum;  // at least one quantum each
+  if (nchunk > max_chunks) nchunk = max_chunks;
+  if (nchunk < 1) nchunk = 1;
+  long long per = ((long long)V + nchunk - 1) / nchunk;
+  per = (per + 7) / 8 * 8;
   return (int)per;
 }
 

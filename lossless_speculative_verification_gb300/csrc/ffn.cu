@@ -24,7 +24,7 @@
 //     A = W_down rows h0..h0+127, B = act rows;  y[row, h] = D (fp32)
 //
 // One persistent CTA per SM, warp-specialised: warp 0 issues TMA, warp 1
-// allocates TMEM and issues tcgen05.mma (one thread), warps 2-5 drain TMEM.
+// allocates TMEM and issues tcgen05.mma (one thread), warps 2-9 drain TMEM.
 // A STAGES-deep shared-memory ring (KCH K-chunks per stage, so that the
 // neighbouring 128-byte pieces of each weight row are requested together)
 // decouples loads from MMAs, and two TMEM accumulators decouple MMAs from the
@@ -42,10 +42,13 @@
 namespace lsv {
 namespace {
 
-constexpr int kFfnThreads = 192;         // 6 warps
-constexpr int kEpiThreads = 128;         // warps 2..5
+constexpr int kFfnThreads = 320;         // 10 warps
+constexpr int kEpiWarps = 8;             // warps 2..9: two per TMEM lane quadrant
+constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
-constexpr int kXchStride = 17;           // padded row of the gate/up exchange buffer
+constexpr int kXchStride = 9;            // padded 8-value row of the gate/up exchange buffer
+constexpr int kXchPair = 2 * 32 * kXchStride;  // floats per (pair, buffer): gate->up and up->gate halves
+constexpr int kEpiBarAll = 5;            // named barrier over all epilogue warps (ids 1..4: warp pairs)
 
 // Decode-size pipeline: K chunks (64 wide) per stage and stage count.
 #ifndef LSV_FFN_KCH32
@@ -135,7 +138,7 @@ struct Smem {
   static constexpr int kChunkB = BN * 128;                  // one 64-wide K chunk of B
   static constexpr int kStageBytes = KCH * (kChunkA + kChunkB);
   static constexpr int kRing = STAGES * kStageBytes;
-  static constexpr int kXch = 64 * kXchStride * 4;
+  static constexpr int kXch = 4 /*pairs*/ * 2 /*buffers*/ * kXchPair * 4;
   static constexpr int kItemSlots = 4;
   static constexpr int kBars = (2 * STAGES + 5 + 2 * kItemSlots) * 8;
   static constexpr int kTotal = 1024 /*alignment slack*/ + kRing + kXch + kBars + 16 + kItemSlots * 4;
@@ -358,12 +361,22 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    // Warp w may read TMEM lanes 32*(w%4)..+31.  Two warps per quadrant split the
+    // 16-column chunks of an accumulator (half h takes chunks h, h+2, ...).  For
+    // gate/up items the warp holding gate rows (quadrant 0/1) and the one holding
+    // the matching up rows (quadrant 2/3) swap half of each chunk through shared
+    // memory, so that both compute SwiGLU on eight columns.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int pair = (q & 1) + 2 * half;     // gate/up warp pair, named barrier 1 + pair
+    const bool is_gate = q < 2;
+    float* xpair = xch + pair * 2 * kXchPair;
     int acc = 0;
     uint32_t acc_phase = 0;
     int slot = 0;
     uint32_t slot_phase = 0;
+    int nx = 0;  // chunks exchanged so far (selects the buffer)
     while (true) {
       const bool got_item = mbar_wait(&item_full[slot], slot_phase, p.wait_ns);
       if (!got_item) set_error(p.err, kErrTimeout);
@@ -373,12 +386,12 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         slot = 0;
         slot_phase ^= 1u;
       }
-      // the same decision in all four epilogue warps keeps their named barriers matched
-      if (named_bar_red_or(1, kEpiThreads, it < 0)) break;
+      // the same decision in all epilogue warps keeps their named barriers matched
+      if (named_bar_red_or(kEpiBarAll, kEpiThreads, it < 0)) break;
       const Item m = decode_item<BN>(it, p);
       const bool got = mbar_wait(&tfull[acc], acc_phase, p.wait_ns);
       if (!got) set_error(p.err, kErrTimeout);
-      if (named_bar_red_or(1, kEpiThreads, !got || *abort_flag)) break;
+      if (named_bar_red_or(kEpiBarAll, kEpiThreads, !got || *abort_flag)) break;
       tc_fence_after_sync();
       const bool routed = m.g < p.E;
       const int nrows_out = routed ? p.T * p.k : p.T;
@@ -388,32 +401,36 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         bf16* out = routed ? p.act : p.act_sh;
         const int ld = routed ? p.I : p.S * p.I;
         const int f = m.ft * 64 + (q & 1) * 32 + lane;
-        float* xrow = xch + ((q & 1) * 32 + lane) * kXchStride;
-        for (int c0 = 0; c0 < n_mma; c0 += 16) {
+        for (int c0 = 16 * half; c0 < n_mma; c0 += 32) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(t_row + c0, r);
           tmem_ld_wait();
-          if (q >= 2) {
+          float* buf = xpair + (nx & 1) * kXchPair;
+          float* g2u = buf + lane * kXchStride;                 // gate values of columns 8..15
+          float* u2g = buf + (32 + lane) * kXchStride;          // up values of columns 0..7
+          if (is_gate) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) xrow[j] = __uint_as_float(r[j]);
-          }
-          named_bar_sync(1, kEpiThreads);
-          if (q < 2) {
+            for (int j = 0; j < 8; ++j) g2u[j] = __uint_as_float(r[8 + j]);
+          } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = c0 + j;
-              if (col < m.cnt && m.row0 + col < nrows_out) {
-                const float hv = silu(__uint_as_float(r[j])) * xrow[j];
-                out[(size_t)(m.row0 + col) * ld + f] = __float2bfloat16_rn(hv);
-              }
-            }
+            for (int j = 0; j < 8; ++j) u2g[j] = __uint_as_float(r[j]);
           }
-          named_bar_sync(1, kEpiThreads);
+          named_bar_sync(1 + pair, 64);
+          const int jb = is_gate ? 0 : 8;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int col = c0 + jb + j;
+            const float gv = is_gate ? __uint_as_float(r[j]) : g2u[j];
+            const float uv = is_gate ? u2g[j] : __uint_as_float(r[8 + j]);
+            if (col < m.cnt && m.row0 + col < nrows_out)
+              out[(size_t)(m.row0 + col) * ld + f] = __float2bfloat16_rn(silu(gv) * uv);
+          }
+          ++nx;
         }
       } else {
         float* out = routed ? p.y_perm : p.y_sh;
         const int h = m.ft * 128 + q * 32 + lane;
-        for (int c0 = 0; c0 < n_mma; c0 += 16) {
+        for (int c0 = 16 * half; c0 < n_mma; c0 += 32) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(t_row + c0, r);
           tmem_ld_wait();
@@ -431,7 +448,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       mbar_arrive(&tempty[acc]);
       if (m.gu) {
         // publish this gate/up item to the down items of its group
-        named_bar_sync(1, kEpiThreads);
+        named_bar_sync(kEpiBarAll, kEpiThreads);
         if (threadIdx.x == 64) {
           fence_proxy_async_global();
           __threadfence();
