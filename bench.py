@@ -1,18 +1,25 @@
 """Benchmark of the FastMTP verify step on GB300.
 
-One step = the whole hot path over one batch: the MoE FFN layer at 32
-sequences x (K=3)+1 = 128 tokens (route, permute, grouped SwiGLU experts,
-shared experts, combine) followed by greedy acceptance over the verifier's
-[32, 4, 129280] bf16 logits.
+Default workload ("decode"): one step = the whole hot path over one batch,
+i.e. the MoE FFN layer at 32 sequences x (K=3)+1 = 128 tokens (route, permute,
+grouped SwiGLU experts, shared experts, combine) followed by greedy
+acceptance over the verifier's [32, 4, 129280] bf16 logits.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|prefill|sweep|stack]
 
-Prints one JSON line (rank 0).  `value` is verified tokens/s with all inputs
-resident in HBM; `e2e` is the same through the public API with host buffers
-(pinned host -> device copies and the read-back inside the timed region).
-Between timed steps L2 is flushed by writing a 256 MB buffer (outside the
-timed events).  The `--impl reference` arm times the CPU oracle on a bounded
-sample of the same workload.
+Prints one JSON line per measured configuration (rank 0; the default run
+prints exactly one).  `value` is tokens/s with all inputs resident in HBM;
+`e2e` is the same through the public API with host buffers (pinned host ->
+device copies and the read-back inside the timed region).  Before every
+timed step L2 is flushed by writing a 256 MB buffer (outside the events).
+The `--impl reference` arm times the CPU oracle on a bounded sample of the
+same workload.
+
+Other workloads (not the default line):
+  prefill  8 pages x (1,156 visual + 64 prompt) = 9,760 tokens through the layer
+  sweep    B in {1,4,8,16,32,64} x K in {1,2,3}: layer + acceptance, one line each
+  stack    11 layers (Zipf-skewed routing, residual + RMSNorm) at 64 x 4 tokens + acceptance
 """
 from __future__ import annotations
 
@@ -30,7 +37,6 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "decode"
 METRIC = "MoE verify-step tokens/s at 32x(K+1) tokens; % of HBM / tensor-core roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -43,30 +49,29 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack"])
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
 
 def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
 def peaks():
+    """(hbm GB/s, bf16 TFLOP/s, source) from MEASURED_PEAKS.json, else the fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        hbm = d.get("hbm_gbs")
-        if hbm:
-            return float(hbm), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        if d.get("hbm_gbs"):
+            return float(d["hbm_gbs"]), float(d.get("bf16_tflops") or FALLBACK_BF16_TFLOPS), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms around the timed region."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -75,6 +80,8 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.lines = []
+        self._first = None
 
     def __enter__(self):
         try:
@@ -87,7 +94,6 @@ class ClockSampler:
 
     def wait_first_sample(self, timeout=3.0):
         """Block until nvidia-smi has printed its first sample (it takes a moment to start)."""
-        self._first = None
         if self.proc is None:
             return
         import select
@@ -103,10 +109,8 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            first = [self._first] if getattr(self, "_first", None) else []
+            first = [self._first] if self._first else []
             self.lines = [l for l in first + out.splitlines() if l.strip()]
-        else:
-            self.lines = []
 
     def summary(self):
         sm, mx, reasons = [], [], set()
@@ -131,16 +135,16 @@ class ClockSampler:
 
 def layer_source_hash():
     h = hashlib.sha256()
-    for f in ("ffn.cu", "ptx.cuh", "prefetch.cu", "route.cu", "permute.cu", "combine.cu", "ffn_plan.cuh", "api.cu"):
+    for f in ("ffn.cu", "ptx.cuh", "route.cu", "permute.cu", "combine.cu", "ffn_plan.cuh", "api.cu", "tmap.h"):
         with open(os.path.join(ROOT, "lossless_speculative_verification_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_hash):
+def ncu_traffic(workload, kernel_hash):
     """DRAM bytes of one layer (sum over its launches) from the committed ncu summary, if it was
     taken on this source."""
-    path = os.path.join(ROOT, "profiles", "layer_decode_traffic.json")
+    path = os.path.join(ROOT, "profiles", "layer_%s_traffic.json" % workload)
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -150,140 +154,151 @@ def ncu_traffic(kernel_hash):
     return d.get("dram_bytes_per_layer")
 
 
-# ----------------------------------------------------------------------------- reference arm (CPU oracle)
-def run_reference(args, rank, world):
-    if rank != 0:
-        return
-    import oracle
-    from lossless_speculative_verification_gb300 import synth
-    oracle.build()
-    w = synth.WORKLOADS[WORKLOAD]
+# ----------------------------------------------------------------------------- workloads
+def layer_bytes(d, n_touched):
+    """Algorithmic bytes of one MoE layer: router, touched routed and shared expert weights, x in, out."""
+    return d.E * d.H * 2 + (n_touched + d.S) * 3 * d.H * d.I * 2 + 2 * d.T * d.H * 2
+
+
+def layer_flops(d):
+    return 2.0 * d.T * (d.k + d.S) * 3 * d.H * d.I + 2.0 * d.T * d.E * d.H
+
+
+def describe(w, layers=1):
     d = w.dims
-    prob = synth.moe_problem(w, seed=args.seed)
-    logits, planted, drafts = synth.verify_problem(w, seed=args.seed)
-    tok_per_step = 2          # tokens of the 128-token batch the oracle takes per step
-
-    def step(i):
-        toks = np.array([(2 * i) % d.T, (2 * i + 1) % d.T], np.int32)
-        oracle.moe_layer(prob.x, prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up, prob.ws_down,
-                         d.k, d.S, tokens=toks)
-        b = (i % w.B)
-        oracle.accept(logits[b:b + 1], drafts[b:b + 1])
-
-    for i in range(args.warmup):
-        step(i)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(args.warmup + i)
-    dt = time.perf_counter() - t0
-    value = tok_per_step * args.steps / dt
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "decode verify step: MoE layer T=128 (B=32,K=3), H=1280, E=64 top-6, S=2, I=896, "
-                               "then acceptance over [32,4,129280] bf16", "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d tokens of the 128-token layer + 1 sequence's acceptance per step" % tok_per_step},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
+    s = "MoE layer T=%d, H=%d, E=%d top-%d, S=%d, I=%d" % (d.T, d.H, d.E, d.k, d.S, d.I)
+    if layers > 1:
+        s = "%d x %s, Zipf(%.1f) routing, residual + RMSNorm" % (layers, s, w.zipf_s)
+    if w.V:
+        s += "; then greedy acceptance over [%d,%d,%d] bf16 logits (B=%d, K=%d)" % (w.B, w.K + 1, w.V, w.B, w.K)
+    return s
 
 
-def cpu_baseline_sample(seconds=12.0, seed=0):
-    """The oracle as it stands, single-threaded, on a bounded sample of the same workload."""
-    import oracle
-    from lossless_speculative_verification_gb300 import synth
-    oracle.build()
-    w = synth.WORKLOADS[WORKLOAD]
-    d = w.dims
-    prob = synth.moe_problem(w, seed=seed)
-    logits, planted, drafts = synth.verify_problem(w, seed=seed)
-    n = 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds:
-        t = n % d.T
-        oracle.moe_layer(prob.x, prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up, prob.ws_down,
-                         d.k, d.S, tokens=np.array([t], np.int32))
-        b = t // (w.K + 1)
-        if t % (w.K + 1) == 0:
-            oracle.accept(logits[b:b + 1], drafts[b:b + 1])
-        n += 1
-    dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d token passes (cycling over the 128 tokens) through the oracle layer (route, 6 routed "
-                      "+ 2 shared experts, combine) plus the acceptance of their sequences, %.1f s" % (n, dt)}
+class DeviceStep:
+    """One workload on the device: `layer()` and `accept()` (each graph-capturable),
+    `e2e()` through the public API with host buffers, plus the accounting."""
+
+    def __init__(self, name, w, seed, dev):
+        import torch
+        from lossless_speculative_verification_gb300 import api, synth
+        self.name, self.w, self.dev = name, w, dev
+        self.api = api
+        d = w.dims
+        self.T = d.T
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        self.sh = api.shape(d.T, d.H, d.E, d.k, d.S, d.I)
+        self.ws = api.workspace(self.sh, dev)
+        self.layers = []
+        if w.layers > 1:
+            st = synth.stack_problem(w, seed=seed)
+            for L in st["layers"]:
+                self.layers.append(api.weights(*[t(L[n]) for n in ("w_router", "w_gate_up", "w_down",
+                                                                    "ws_gate_up", "ws_down")]))
+            self.x0, self.h0 = t(st["x0"]), t(st["h0"])
+        else:
+            prob = synth.moe_problem(w, seed=seed)
+            self.layers.append(api.weights(*[t(a) for a in (prob.w_router, prob.w_gate_up, prob.w_down,
+                                                             prob.ws_gate_up, prob.ws_down)]))
+            self.x0 = self.h0 = t(prob.x)
+        self.x = torch.empty_like(self.x0)
+        self.h = torch.empty_like(self.x0)
+        self.h2 = torch.empty_like(self.x0)
+        self.out = torch.empty_like(self.x0)
+        self.layer_counts = [torch.empty(d.E, dtype=torch.int32, device=dev) for _ in self.layers]
+        if w.V:
+            logits, planted, drafts = synth.verify_problem(w, seed=seed)
+            self.logits = t(logits)
+            self.drafts = torch.from_numpy(drafts).to(dev)
+            self.aws = api.spec_verify_workspace(w.B, w.K, w.V, dev)
+            self.alen = torch.empty(w.B, dtype=torch.int32, device=dev)
+            self.comm = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+        else:
+            self.logits = None
+        # our launches per step.  Per layer: route, fused permute+gather (<= 8192 pairs; else count,
+        # scatter and prep), experts, combine, and rmsnorm in the stack.  Acceptance: partials + finalize.
+        per_layer = 4 if d.T * d.k <= 8192 else 6
+        self.launches = len(self.layers) * (per_layer + (1 if w.layers > 1 else 0)) + (2 if w.V else 0)
+
+    def _layers(self, x_in):
+        api = self.api
+        if len(self.layers) == 1:
+            api.moe_verify_layer(x_in, self.layers[0], self.sh, self.ws, out=self.out, counts=self.layer_counts[0])
+            return
+        self.x.copy_(x_in)
+        self.h.copy_(self.h0)
+        h, h2 = self.h, self.h2
+        for L, c in zip(self.layers, self.layer_counts):
+            api.moe_verify_layer(h, L, self.sh, self.ws, out=self.out, counts=c)
+            api.rmsnorm_residual(self.x, self.out, h=h2)
+            h, h2 = h2, h
+
+    def layer(self):
+        self._layers(self.x0)
+
+    def accept(self):
+        if self.logits is not None:
+            self.api.spec_verify_accept(self.logits, self.drafts, self.aws, accept_len=self.alen, committed=self.comm)
+
+    def bytes_and_flops(self):
+        d = self.w.dims
+        byts = sum(layer_bytes(d, int((c > 0).sum().item())) for c in self.layer_counts)
+        flops = layer_flops(d) * len(self.layers)
+        acc = self.w.B * (self.w.K + 1) * self.w.V * 2 if self.logits is not None else 0
+        return byts, flops, acc
+
+    def setup_e2e(self):
+        import torch
+        self.hx = self.x0.cpu().pin_memory()
+        self.dx = torch.empty_like(self.x0)
+        self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
+        h2d, d2h = self.hx.numel() * 2, self.h_out.numel() * 2
+        if self.logits is not None:
+            self.hl = self.logits.cpu().pin_memory()
+            self.hd = self.drafts.cpu().pin_memory()
+            self.dl, self.dd = torch.empty_like(self.logits), torch.empty_like(self.drafts)
+            self.h_len = torch.empty_like(self.alen, device="cpu").pin_memory()
+            self.h_comm = torch.empty_like(self.comm, device="cpu").pin_memory()
+            h2d += self.hl.numel() * 2 + self.hd.numel() * 4
+            d2h += self.h_len.numel() * 4 + self.h_comm.numel() * 4
+        return h2d, d2h
+
+    def e2e(self):
+        self.dx.copy_(self.hx, non_blocking=True)
+        self._layers(self.dx)
+        if self.logits is not None:
+            self.dl.copy_(self.hl, non_blocking=True)
+            self.dd.copy_(self.hd, non_blocking=True)
+            self.api.spec_verify_accept(self.dl, self.dd, self.aws, accept_len=self.alen, committed=self.comm)
+            self.h_len.copy_(self.alen, non_blocking=True)
+            self.h_comm.copy_(self.comm, non_blocking=True)
+        self.h_out.copy_(self.out, non_blocking=True)
 
 
-# ----------------------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local):
+def measure(step, args, local, world, flush, dist):
+    """Warm up, time `steps` graph replays (L2 flushed before each), then the e2e path."""
     import torch
-    from lossless_speculative_verification_gb300 import _build, api, synth
-
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if rank == 0 or not os.path.exists(_build.LIB):
-        _build.build()
-    if world > 1:
-        dist.barrier()
-
-    w = synth.WORKLOADS[WORKLOAD]
-    d = w.dims
-    prob = synth.moe_problem(w, seed=args.seed + 1000 * rank)
-    logits_np, planted, drafts_np = synth.verify_problem(w, seed=args.seed + 1000 * rank)
-
-    def tdev(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    x = tdev(prob.x)
-    W = [tdev(a) for a in (prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up, prob.ws_down)]
-    del prob.w_gate_up, prob.w_down
-    sh = api.shape(d.T, d.H, d.E, d.k, d.S, d.I)
-    wts = api.weights(*W)
-    ws = api.workspace(sh, dev)
-    logits = tdev(logits_np)
-    drafts = torch.from_numpy(drafts_np).to(dev)
-    aws = api.spec_verify_workspace(w.B, w.K, w.V, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    T, k = d.T, d.k
-    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    counts = torch.empty(d.E, dtype=torch.int32, device=dev)
-    out = torch.empty((T, d.H), dtype=torch.bfloat16, device=dev)
-    alen = torch.empty(w.B, dtype=torch.int32, device=dev)
-    comm = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    # launches per step: route, permute+gather, grouped experts, combine | argmax partials, accept
-    launches_per_step = 6
-
-    def layer():
-        api.moe_verify_layer(x, wts, sh, ws, out=out, topk_idx=idx, counts=counts)
-
-    def accept():
-        api.spec_verify_accept(logits, drafts, aws, accept_len=alen, committed=comm)
-
+    api = step.api
+    stream = torch.cuda.current_stream(step.dev)
     for _ in range(max(args.warmup, 0)):
-        layer(); accept()
+        step.layer()
+        step.accept()
     torch.cuda.synchronize()
     assert api.get_device_error() == 0
 
-    # eager launches, for context
     eager_ms = []
     for i in range(min(args.steps, 10)):
         flush.fill_(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        layer(); accept()
+        step.layer()
+        step.accept()
         b.record(stream)
         b.synchronize()
         eager_ms.append(a.elapsed_time(b))
 
-    # the step as two CUDA graphs: the MoE layer (one PDL chain) and the acceptance
+    # the step as two CUDA graphs: the layer(s) (PDL-chained launches) and the acceptance
     graphs = [torch.cuda.CUDAGraph() for _ in range(2)]
-    for g, fn in zip(graphs, (layer, accept)):
+    for g, fn in zip(graphs, (step.layer, step.accept)):
         with torch.cuda.graph(g):
             fn()
     for _ in range(max(args.warmup, 0)):
@@ -292,13 +307,6 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     assert api.get_device_error() == 0
 
-    n_touched = int((counts > 0).sum().item())
-    H, I, S, E = d.H, d.I, d.S, d.E
-    # algorithmic bytes of the layer: router + touched routed + shared expert weights, x in, out
-    layer_bytes = E * H * 2 + (n_touched + S) * 3 * H * I * 2 + 2 * T * H * 2
-    accept_bytes = w.B * (w.K + 1) * w.V * 2
-
-    # timed region: per step, flush L2 (untimed), then events around the two graphs
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
@@ -325,98 +333,176 @@ def run_ours(args, rank, world, local):
             for g in graphs:
                 g.replay()
         torch.cuda.synchronize()
-    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
-    layer_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    accept_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        dist.barrier()
     assert api.get_device_error() == 0
+    total_ms = sum(e[0].elapsed_time(e[2]) for e in evs)
+    layer_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    accept_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
 
-    # end to end through the public API: pinned host inputs in, results back to the host
-    hx = x.cpu().pin_memory()
-    hl = logits.cpu().pin_memory()
-    hd = drafts.cpu().pin_memory()
-    h_out = torch.empty_like(out, device="cpu").pin_memory()
-    h_len = torch.empty_like(alen, device="cpu").pin_memory()
-    h_comm = torch.empty_like(comm, device="cpu").pin_memory()
-    dx, dl, dd = torch.empty_like(x), torch.empty_like(logits), torch.empty_like(drafts)
-
-    def e2e_step():
-        dx.copy_(hx, non_blocking=True)
-        dl.copy_(hl, non_blocking=True)
-        dd.copy_(hd, non_blocking=True)
-        api.moe_verify_layer(dx, wts, sh, ws, out=out)
-        api.spec_verify_accept(dl, dd, aws, accept_len=alen, committed=comm)
-        h_out.copy_(out, non_blocking=True)
-        h_len.copy_(alen, non_blocking=True)
-        h_comm.copy_(comm, non_blocking=True)
-
+    h2d, d2h = step.setup_e2e()
     for _ in range(max(args.warmup, 1)):
-        e2e_step()
+        step.e2e()
     torch.cuda.synchronize()
-    e2e_ms = []
+    e2e_total = 0.0
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        e2e_step()
+        step.e2e()
         b.record(stream)
         b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
+        e2e_total += a.elapsed_time(b)
     assert api.get_device_error() == 0
-    h2d = hx.numel() * 2 + hl.numel() * 2 + hd.numel() * 4
-    d2h = h_out.numel() * 2 + h_len.numel() * 4 + h_comm.numel() * 4
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_total], device=step.dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_total = float(t[0].item()), float(t[1].item())
+    return dict(total_ms=total_ms, layer_ms=layer_ms, accept_ms=accept_ms, eager_ms=statistics.mean(eager_ms),
+                e2e_total=e2e_total, h2d=h2d, d2h=d2h, clocks=clk.summary())
 
-    if rank != 0:
-        if world > 1:
-            dist.barrier()
-            dist.destroy_process_group()
-        return
-    ms_per_step = total_ms / args.steps
-    tokens = T * world * args.steps
-    value = tokens / (total_ms / 1e3)
-    peak, peak_kind = peaks()
-    layer_avg = sum(layer_ms) / len(layer_ms)
-    accept_avg = sum(accept_ms) / len(accept_ms)
-    achieved = layer_bytes / (layer_avg / 1e3) / 1e9
+
+def result_line(args, step, m, world, cpu):
+    hbm, tflops, peak_src = peaks()
+    w = step.w
+    byts, flops, acc_bytes = step.bytes_and_flops()
     khash = layer_source_hash()
-    traffic = ncu_traffic(khash)
+    if step.name == "prefill":
+        achieved = flops / (m["layer_ms"] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s", "frac": achieved / tflops,
+                "algorithmic_flops": flops}
+    else:
+        achieved = byts / (m["layer_ms"] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "algorithmic_bytes": byts}
+    roof.update({"kernel": "moe_verify_layer x%d: router, permute+gather, grouped SwiGLU experts (tcgen05), "
+                           "combine; one PDL-chained launch sequence per layer" % len(step.layers),
+                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "layer_ms": m["layer_ms"],
+                 "kernel_source_hash": khash})
+    if acc_bytes:
+        roof["accept"] = {"ms": m["accept_ms"], "algorithmic_bytes": acc_bytes,
+                          "achieved_gbs": acc_bytes / (m["accept_ms"] / 1e3) / 1e9}
+    tokens = step.T * world * args.steps
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "decode verify step: MoE layer T=128 (B=32,K=3), H=1280, E=64 top-6, S=2, I=896, "
-                               "then greedy acceptance over [32,4,129280] bf16 logits",
+        "metric": METRIC, "value": tokens / (m["total_ms"] / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["total_ms"] / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s: %s" % (step.name, describe(w, len(step.layers))),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "flushed between timed steps (256 MB write, outside the events)",
-                   "timing": "step replayed as 2 CUDA graphs (layer, acceptance), CUDA events per step",
+                   "l2": "flushed before every timed step (256 MB write, outside the events)",
+                   "timing": "step replayed as 2 CUDA graphs (layers, acceptance), CUDA events per step",
                    "clocks_window": "nvidia-smi every 100 ms over back-to-back steps around the timed ones",
-                   "eager_ms_per_step": sum(eager_ms) / len(eager_ms)},
-        "roofline": {"bound": "hbm",
-                     "kernel": "moe_verify_layer: router, permute+gather, grouped SwiGLU experts (tcgen05), "
-                               "combine; one PDL-chained launch sequence (the experts kernel carries the HBM stream)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_kind, "traffic": traffic, "algorithmic_bytes": layer_bytes,
-                     "touched_experts": n_touched, "layer_ms": layer_avg, "kernel_source_hash": khash,
-                     "accept": {"ms": accept_avg, "algorithmic_bytes": accept_bytes,
-                                "achieved_gbs": accept_bytes / (accept_avg / 1e3) / 1e9}},
-        "e2e": {"value": T * world * args.steps / (e2e_total / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+                   "eager_ms_per_step": m["eager_ms"]},
+        "roofline": roof,
+        "e2e": {"value": tokens / (m["e2e_total"] / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": m["d2h"]},
+        "gpu_launches": step.launches * args.steps,
+        "clocks": m["clocks"],
     }
-    if world == 1:
-        line["cpu_baseline"] = cpu_baseline_sample()
-    print(json.dumps(line), flush=True)
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+def workloads(name):
+    from lossless_speculative_verification_gb300 import synth
+    if name == "sweep":
+        return [("sweep", synth.sweep_workload(B, K), synth.sweep_seed(B, K))
+                for B in synth.SWEEP_B for K in synth.SWEEP_K]
+    return [(name, synth.WORKLOADS[name], 0)]
+
+
+# ----------------------------------------------------------------------------- CPU oracle (baseline and reference arm)
+def oracle_sampler(w, seed):
+    """The oracle as it stands, single-threaded, on a bounded sample of the workload: whole tokens
+    through every layer (and the acceptance of their sequences), cycling over the batch.  Returns
+    sample(seconds) -> cpu_baseline dict; the inputs are generated once, outside any timing."""
+    import oracle
+    from lossless_speculative_verification_gb300 import synth
+    oracle.build()
+    d = w.dims
+    if w.layers > 1:
+        st = synth.stack_problem(w, seed=seed)
+        layers, xs, hs = st["layers"], st["x0"], st["h0"]
+    else:
+        prob = synth.moe_problem(w, seed=seed)
+        layers = [dict(w_router=prob.w_router, w_gate_up=prob.w_gate_up, w_down=prob.w_down,
+                       ws_gate_up=prob.ws_gate_up, ws_down=prob.ws_down)]
+        xs = hs = prob.x
+    logits = drafts = None
+    if w.V:
+        logits, planted, drafts = synth.verify_problem(w, seed=seed)
+    state = {"n": 0}
+
+    def sample(seconds):
+        n0 = state["n"]
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            t = state["n"] % d.T
+            x, h = xs[t:t + 1], hs[t:t + 1]
+            for L in layers:
+                out, _, _ = oracle.moe_layer(h, L["w_router"], L["w_gate_up"], L["w_down"], L["ws_gate_up"],
+                                             L["ws_down"], d.k, d.S)
+                if len(layers) > 1:
+                    xn, hn = oracle.rmsnorm_residual(x, synth.bf16_bits(out.astype(np.float32)))
+                    x, h = synth.bf16_bits(xn.astype(np.float32)), synth.bf16_bits(hn.astype(np.float32))
+            if logits is not None and t % (w.K + 1) == 0:
+                b = t // (w.K + 1)
+                oracle.accept(logits[b:b + 1], drafts[b:b + 1])
+            state["n"] += 1
+        dt = time.perf_counter() - t0
+        n = state["n"] - n0
+        return {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "sample": "%d token passes (cycling over the %d tokens) through %d oracle layer(s)%s, %.1f s"
+                          % (n, d.T, len(layers), " plus the acceptance of their sequences" if w.V else "", dt)}
+
+    return sample
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    for name, w, seed in workloads(args.workload):
+        per_step = 2.0 if name != "sweep" else 0.5       # seconds of oracle work per timed step
+        sample = oracle_sampler(w, seed + args.seed)
+        sample(0.2 * max(args.warmup, 1))                # warm-up
+        t0 = time.perf_counter()
+        res = sample(per_step * args.steps)
+        dt = time.perf_counter() - t0
+        line = {
+            "impl": "reference", "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "%s: %s" % (name, describe(w, w.layers)), "l2": "n/a (CPU)"},
+            "cpu_baseline": res,
+            "e2e": {"value": res["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import torch
+    from lossless_speculative_verification_gb300 import _build
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for name, w, seed in workloads(args.workload):
+        step = DeviceStep(name, w, seed + args.seed + 1000 * rank, dev)
+        m = measure(step, args, local, world, flush, dist)
+        cpu = None
+        if rank == 0 and world == 1:
+            cpu = oracle_sampler(w, seed + args.seed)(12.0 if args.workload != "sweep" else 2.0)
+        if rank == 0:
+            print(json.dumps(result_line(args, step, m, world, cpu)), flush=True)
+        del step
+        torch.cuda.empty_cache()
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

@@ -25,7 +25,8 @@ namespace lsv {
 namespace {
 
 constexpr int kAccThreads = 256;
-constexpr int kUnroll = 8;
+constexpr int kUnroll = 4;
+constexpr int kAccMinBlocks = 8;  // resident CTAs per SM the chunking plans for (one wave)
 constexpr int kChunkQuantum = kAccThreads * 8;  // elements covered by one 16-B load per thread
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -55,7 +56,7 @@ __device__ __forceinline__ void scan8(const uint4& q, int base, float& bv, int& 
   }
 }
 
-__global__ void __launch_bounds__(kAccThreads) argmax_partial_kernel(const bf16* __restrict__ logits, int V,
+__global__ void __launch_bounds__(kAccThreads, kAccMinBlocks) argmax_partial_kernel(const bf16* __restrict__ logits, int V,
                                                                      int chunk, int nchunk, int vec_ok,
                                                                      float* __restrict__ pv,
                                                                      int* __restrict__ pi) {
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finalize_kernel(
 int chunk_elems(int R, int V, int num_sms) {
   // one wave of about 8 resident CTAs per SM: pick the chunks per row first, then
   // the chunk length (a multiple of 8 elements, so 16-byte loads stay aligned)
-  const long long target = (long long)num_sms * 8;
+  const long long target = (long long)num_sms * kAccMinBlocks;
   long long nchunk = target / (R > 0 ? R : 1);
   const long long max_chunks = ((long long)V + kChunkQuantum - 1) / kChunkQuantum;  // at least one quantum each
   if (nchunk > max_chunks) nchunk = max_chunks;

@@ -322,7 +322,7 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   if (e == cudaSuccess)
     e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,
                      nullptr, s);
-  const bool fused = L.nblk == 1;  // up to kPermChunk pairs: permutation, gather and plan in one launch
+  const bool fused = (long long)T * k <= kPermFusedMax;  // permutation, gather and plan in one launch
   if (e == cudaSuccess) {
     if (fused)
       e = launch_permute_gather(idx, T, k, E, H, S, I, ffn_token_tile(T, k, E), static_cast<const bf16*>(x), counts,

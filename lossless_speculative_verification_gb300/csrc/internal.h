@@ -53,7 +53,8 @@ struct WsLayout {
 };
 WsLayout ws_layout(int T, int H, int E, int k, int S, int I);
 
-constexpr int kPermChunk = 8192;  // (token, slot) entries per permutation block
+constexpr int kPermChunk = 1024;      // (token, slot) entries per block of the two-level permutation
+constexpr int kPermFusedMax = 8192;   // up to this many entries: one fused permutation + gather launch
 
 // Launch with programmatic stream serialization: the kernel may start while its
 // predecessor in the stream finishes; it must call pdl_wait() before touching
@@ -82,7 +83,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* cou
                            int32_t* perm, int32_t* inv, int32_t* blk_counts, int nblk, int* err,
                            cudaStream_t s);
 
-// Permutation + row gather + item table in one launch (T*k <= kPermChunk).
+// Permutation + row gather + item table in one launch (T*k <= kPermFusedMax).
 cudaError_t launch_permute_gather(const int32_t* idx, int T, int k, int E, int H, int S, int I, int BN,
                                   const bf16* x, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                                   bf16* xperm, int32_t* table, int* err, cudaStream_t s);

@@ -8,11 +8,12 @@
 // ranks, never from the order in which atomics land, so the result is unique
 // and run-to-run identical.
 //
-// Blocks own contiguous ranges of kPermChunk entries.  With more than one
-// block a count kernel first writes per-block histograms; the scatter kernel
-// derives every block's base per expert from them.  Inside a block, entries
-// are ranked a round of 1024 at a time: __match_any_sync groups equal experts
-// within a warp, and a per-expert scan over the 32 warps orders the warps.
+// Two-level form: blocks own contiguous ranges of kPermChunk entries.  With
+// more than one block a count kernel first writes per-block histograms; the
+// scatter kernel derives every block's base per expert from them.  Inside a
+// block, entries are ranked a round of 1024 at a time: __match_any_sync groups
+// equal experts within a warp, and a per-expert scan over the 32 warps orders
+// the warps.
 #include "ffn_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -153,8 +154,8 @@ __global__ void __launch_bounds__(kThreads) permute_scatter_kernel(
   }
 }
 
-// Permutation, row gather and item table in one launch, for up to kPermChunk
-// pairs.  CTA c owns the 32 pairs [32c, 32c+32): it histograms all pairs
+// Permutation, row gather and item table in one launch, for up to
+// kPermFusedMax pairs.  CTA c owns the 32 pairs [32c, 32c+32): it histograms all pairs
 // (cheap at these sizes) and, separately, the pairs before its slice, which
 // gives every expert's offset and the slice's base inside each expert segment;
 // warp 0 ranks the slice with __match_any_sync, and all warps copy the slice's

@@ -39,6 +39,22 @@ def test_route_parity(name):
     np.testing.assert_allclose(w.cpu().numpy(), ref["p"], rtol=1e-5, atol=1e-9)
 
 
+@pytest.mark.parametrize("T,H,E,k", [(300, 256, 8, 2), (257, 1280, 64, 6), (513, 512, 128, 8),
+                                     (1000, 256, 256, 6), (640, 1280, 64, 1)])
+def test_route_parity_tensor_core_path(T, H, E, k):
+    """Above 256 tokens the router runs on tcgen05 (one lane per token); every padded width."""
+    d = synth.MoeDims(T, H, E, k, 0, 64)
+    prob = synth.moe_problem(d, seed=T + E, hidden="sphere", row_ok=oracle.gap_ok(k))
+    x, wr = to_dev(prob.x), to_dev(prob.w_router)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    idx, w = api.moe_route(x, wr, k, logits=logits)
+    torch.cuda.synchronize()
+    ridx, rp, rlog = oracle.route(prob.x, prob.w_router, k, return_logits=True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(logits.cpu().numpy(), rlog, rtol=0, atol=2e-5 * np.sqrt(H / 256))
+    np.testing.assert_allclose(w.cpu().numpy(), rp, rtol=1e-5, atol=1e-9)
+
+
 # ----------------------------------------------------------------------------- permutation
 def random_routing(T, k, E, seed):
     rs = np.random.default_rng(seed)
