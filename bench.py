@@ -296,18 +296,45 @@ def measure(step, args, local, world, flush, dist):
         b.synchronize()
         eager_ms.append(a.elapsed_time(b))
 
-    # the step as two CUDA graphs: the layer(s) (PDL-chained launches) and the acceptance
-    graphs = [torch.cuda.CUDAGraph() for _ in range(2)]
-    for g, fn in zip(graphs, (step.layer, step.accept)):
+    # the step as one CUDA graph with its timing events recorded as graph nodes (start, after the
+    # layers, end); where torch cannot record events inside a graph, two graphs with events between
+    try:
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+        one_graph = True
+    except TypeError:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        one_graph = False
+    if one_graph:
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            fn()
+            evs[0].record()
+            step.layer()
+            evs[1].record()
+            step.accept()
+            evs[2].record()
+        graphs = [g]
+    else:
+        graphs = [torch.cuda.CUDAGraph() for _ in range(2)]
+        for g, fn in zip(graphs, (step.layer, step.accept)):
+            with torch.cuda.graph(g):
+                fn()
+
+    def replay():
+        if one_graph:
+            graphs[0].replay()
+        else:
+            evs[0].record(stream)
+            graphs[0].replay()
+            evs[1].record(stream)
+            graphs[1].replay()
+            evs[2].record(stream)
+
     for _ in range(max(args.warmup, 0)):
-        for g in graphs:
-            g.replay()
+        replay()
     torch.cuda.synchronize()
     assert api.get_device_error() == 0
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    step_ms, layer_list, accept_list = [], [], []
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -318,25 +345,24 @@ def measure(step, args, local, world, flush, dist):
         t_end = time.perf_counter() + 0.3
         while time.perf_counter() < t_end:
             flush.fill_(0)
-            for g in graphs:
-                g.replay()
+            replay()
+        torch.cuda.synchronize()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
-            evs[i][0].record(stream)
-            graphs[0].replay()
-            evs[i][1].record(stream)
-            graphs[1].replay()
-            evs[i][2].record(stream)
+            replay()
+            evs[2].synchronize()
+            step_ms.append(evs[0].elapsed_time(evs[2]))
+            layer_list.append(evs[0].elapsed_time(evs[1]))
+            accept_list.append(evs[1].elapsed_time(evs[2]))
         t_end = time.perf_counter() + 0.3
         while time.perf_counter() < t_end:
             flush.fill_(0)
-            for g in graphs:
-                g.replay()
+            replay()
         torch.cuda.synchronize()
     assert api.get_device_error() == 0
-    total_ms = sum(e[0].elapsed_time(e[2]) for e in evs)
-    layer_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    accept_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    total_ms = sum(step_ms)
+    layer_ms = statistics.mean(layer_list)
+    accept_ms = statistics.mean(accept_list)
 
     h2d, d2h = step.setup_e2e()
     for _ in range(max(args.warmup, 1)):
@@ -357,7 +383,7 @@ def measure(step, args, local, world, flush, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms, e2e_total = float(t[0].item()), float(t[1].item())
     return dict(total_ms=total_ms, layer_ms=layer_ms, accept_ms=accept_ms, eager_ms=statistics.mean(eager_ms),
-                e2e_total=e2e_total, h2d=h2d, d2h=d2h, clocks=clk.summary())
+                e2e_total=e2e_total, h2d=h2d, d2h=d2h, clocks=clk.summary(), one_graph=one_graph)
 
 
 def result_line(args, step, m, world, cpu):
@@ -388,7 +414,9 @@ def result_line(args, step, m, world, cpu):
         "config": {"workload": "%s: %s" % (step.name, describe(w, len(step.layers))),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MB write, outside the events)",
-                   "timing": "step replayed as 2 CUDA graphs (layers, acceptance), CUDA events per step",
+                   "timing": ("step replayed as one CUDA graph; CUDA events recorded as graph nodes at its start, "
+                              "after the layers and at its end" if m["one_graph"] else
+                              "step replayed as 2 CUDA graphs (layers, acceptance); CUDA events per step"),
                    "clocks_window": "nvidia-smi every 100 ms over back-to-back steps around the timed ones",
                    "eager_ms_per_step": m["eager_ms"]},
         "roofline": roof,

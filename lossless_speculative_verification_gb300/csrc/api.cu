@@ -264,8 +264,8 @@ lsv_status moe_grouped_ffn(const void* x, const int32_t* perm_src, const int32_t
   return from_cuda(launch_ffn(static_cast<const bf16*>(x), perm_src, offsets, static_cast<const bf16*>(wgu),
                               static_cast<const bf16*>(wd), static_cast<const bf16*>(wt->ws_gate_up),
                               static_cast<const bf16*>(wt->ws_down), shape->T, shape->H, shape->E, shape->k,
-                              shape->S, shape->I, y_perm, y_shared, static_cast<uint8_t*>(ws), L, *dc,
-                              reinterpret_cast<cudaStream_t>(stream)));
+                              shape->S, shape->I, y_perm, y_shared, /*y_bf16=*/false, static_cast<uint8_t*>(ws), L,
+                              *dc, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 lsv_status moe_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_shared,
@@ -279,8 +279,9 @@ lsv_status moe_combine(const float* y_perm, const int32_t* inv, const float* top
     return LSV_ERR_MISALIGNED;
   DeviceCtx* dc = nullptr;
   if (device_ctx(&dc) != cudaSuccess) return LSV_ERR_CUDA;
-  return from_cuda(launch_combine(y_perm, inv, topk_w, shape->S > 0 ? y_shared : nullptr, shape->T, shape->H,
-                                  shape->k, static_cast<bf16*>(out), dc->err, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_combine(y_perm, inv, topk_w, shape->S > 0 ? y_shared : nullptr, /*y_bf16=*/false,
+                                  shape->T, shape->H, shape->k, static_cast<bf16*>(out), dc->err,
+                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_moe_shape* shape, void* out,
@@ -310,8 +311,9 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   int32_t* offsets = reinterpret_cast<int32_t*>(w + L.offsets);
   int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
   int32_t* inv = reinterpret_cast<int32_t*>(w + L.inv);
-  float* y_perm = reinterpret_cast<float*>(w + L.y_perm);
-  float* y_sh = reinterpret_cast<float*>(w + L.y_sh);
+  // inside the layer the expert outputs stay in bf16 (half the bytes between the experts and the combine)
+  bf16* y_perm = reinterpret_cast<bf16*>(w + L.y_perm);
+  bf16* y_sh = reinterpret_cast<bf16*>(w + L.y_sh);
   const bf16* wgu = static_cast<const bf16*>(wt->w_gate_up);
   const bf16* wdn = static_cast<const bf16*>(wt->w_down);
   const bf16* wsgu = static_cast<const bf16*>(wt->ws_gate_up);
@@ -333,10 +335,11 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
                          L.nblk, dc->err, s);
   }
   if (e == cudaSuccess)
-    e = launch_ffn(static_cast<const bf16*>(x), perm, offsets, wgu, wdn, wsgu, wsdn, T, H, E, k, S, I, y_perm, y_sh, w,
-                   L, *dc, s, /*with_prep=*/!fused);
+    e = launch_ffn(static_cast<const bf16*>(x), perm, offsets, wgu, wdn, wsgu, wsdn, T, H, E, k, S, I, y_perm, y_sh,
+                   /*y_bf16=*/true, w, L, *dc, s, /*with_prep=*/!fused);
   if (e == cudaSuccess)
-    e = launch_combine(y_perm, inv, tw, S > 0 ? y_sh : nullptr, T, H, k, static_cast<bf16*>(out), dc->err, s);
+    e = launch_combine(y_perm, inv, tw, S > 0 ? y_sh : nullptr, /*y_bf16=*/true, T, H, k, static_cast<bf16*>(out),
+                       dc->err, s);
   return from_cuda(e);
 }
 

@@ -66,8 +66,9 @@ struct FfnParams {
   int* done;               // [G]
   bf16* act;               // [T*k, I]
   bf16* act_sh;            // [T, S*I]
-  float* y_perm;           // [T*k, H]
-  float* y_sh;             // [T, H]
+  void* y_perm;            // [T*k, H] fp32, or bf16 when y_bf16
+  void* y_sh;              // [T, H]   fp32, or bf16 when y_bf16
+  int y_bf16;
   int* err;
   uint64_t wait_ns;
 };
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           ++nx;
         }
       } else {
-        float* out = routed ? p.y_perm : p.y_sh;
+        void* out = routed ? p.y_perm : p.y_sh;
         const int h = m.ft * 128 + q * 32 + lane;
         for (int c0 = 16 * half; c0 < n_mma; c0 += 32) {
           uint32_t r[16];
@@ -439,8 +440,13 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int col = c0 + j;
-              if (col < m.cnt && m.row0 + col < nrows_out)
-                out[(size_t)(m.row0 + col) * p.H + h] = __uint_as_float(r[j]);
+              if (col < m.cnt && m.row0 + col < nrows_out) {
+                const size_t o = (size_t)(m.row0 + col) * p.H + h;
+                if (p.y_bf16)
+                  static_cast<bf16*>(out)[o] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                else
+                  static_cast<float*>(out)[o] = __uint_as_float(r[j]);
+              }
             }
           }
         }
@@ -488,7 +494,16 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
     } else {
       const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)(src / k) * H);
       uint4* d = reinterpret_cast<uint4*>(xperm + (size_t)row * H);
-      for (int c = lane; c < H / 8; c += 32) d[c] = __ldg(s + c);
+      // all loads of a stretch first, then the stores: every lane keeps 8 pieces in flight
+      for (int c0 = lane; c0 < H / 8; c0 += 8 * 32) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (c0 + 32 * u < H / 8) v[u] = __ldg(s + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (c0 + 32 * u < H / 8) d[c0 + 32 * u] = v[u];
+      }
     }
   }
   if (blockIdx.x == 0 && threadIdx.x < 32) build_item_table(offsets, T, H, E, k, S, I, BN, table, err);
@@ -498,7 +513,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
 template <int BN, int STAGES, int KCH>
 cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                     const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E, int k,
-                    int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
+                    int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws, const WsLayout& L,
                     const DeviceCtx& dc, cudaStream_t s, bool with_prep) {
   using SM = Smem<BN, STAGES, KCH>;
   static_assert(SM::kTotal <= 232448, "shared memory budget");
@@ -544,6 +559,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.act_sh = act_sh;
   p.y_perm = y_perm;
   p.y_sh = y_sh;
+  p.y_bf16 = y_bf16 ? 1 : 0;
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();
   return launch_pdl(ffn_kernel<BN, STAGES, KCH>, dim3(dc.num_sms), dim3(kFfnThreads), SM::kTotal, s, maps, p);
@@ -563,21 +579,21 @@ int ffn_token_tile(int T, int k, int E) {
 
 cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                        const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
-                       int k, int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
-                       const DeviceCtx& dc, cudaStream_t s, bool with_prep) {
+                       int k, int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws,
+                       const WsLayout& L, const DeviceCtx& dc, cudaStream_t s, bool with_prep) {
   switch (ffn_token_tile(T, k, E)) {
     case 32:
       return run_ffn<32, LSV_FFN_STAGES32, LSV_FFN_KCH32>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down,
-                                                          T, H, E, k, S, I, y_perm, y_sh, ws, L, dc, s, with_prep);
+                                                          T, H, E, k, S, I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep);
     case 64:
       return run_ffn<64, 4, 2>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                               y_sh, ws, L, dc, s, with_prep);
+                               y_sh, y_bf16, ws, L, dc, s, with_prep);
     case 128:
       return run_ffn<128, 6, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                                y_sh, ws, L, dc, s, with_prep);
+                                y_sh, y_bf16, ws, L, dc, s, with_prep);
     default:
       return run_ffn<256, 4, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                                y_sh, ws, L, dc, s, with_prep);
+                                y_sh, y_bf16, ws, L, dc, s, with_prep);
   }
 }
 

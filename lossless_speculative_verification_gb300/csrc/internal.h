@@ -98,13 +98,14 @@ cudaError_t launch_weight_prefetch(const bf16* w_gate_up, const bf16* w_down, co
 int ffn_token_tile(int T, int k, int E);
 // Grouped experts.  with_prep: first gather the routed rows and build the item
 // table (otherwise launch_permute_gather already did).
+// y_perm/y_sh are fp32, or bf16 when y_bf16 (the fused layer keeps them in bf16).
 cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                        const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
-                       int k, int S, int I, float* y_perm, float* y_sh, uint8_t* ws, const WsLayout& L,
-                       const DeviceCtx& dc, cudaStream_t s, bool with_prep = true);
+                       int k, int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws,
+                       const WsLayout& L, const DeviceCtx& dc, cudaStream_t s, bool with_prep = true);
 
-cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_sh,
-                           int T, int H, int k, bf16* out, int* err, cudaStream_t s);
+cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_sh,
+                           bool y_bf16, int T, int H, int k, bf16* out, int* err, cudaStream_t s);
 
 cudaError_t launch_rmsnorm_residual(bf16* x, const bf16* y, bf16* h, int T, int H, float eps, cudaStream_t s);
 
