@@ -318,9 +318,12 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   const bf16* wdn = static_cast<const bf16*>(wt->w_down);
   const bf16* wsgu = static_cast<const bf16*>(wt->ws_gate_up);
   const bf16* wsdn = static_cast<const bf16*>(wt->ws_down);
-  cudaError_t e = cudaSuccess;
+  // zero the grouped-expert kernel's counters before anything else of this layer runs,
+  // so that it can begin the routing-independent shared-expert items early
+  const int G = E + (S > 0 ? 1 : 0);
+  cudaError_t e = cudaMemsetAsync(w + L.table + (size_t)table_counters(G) * 4, 0, (size_t)(G + 1) * 4, s);
   const uint64_t pf = default_prefetch_bytes(*dc, T, E, k, S, I, H);
-  if (pf) e = launch_weight_prefetch(wgu, wdn, wsgu, wsdn, H, E, S, I, pf, *dc, s);
+  if (e == cudaSuccess && pf) e = launch_weight_prefetch(wgu, wdn, wsgu, wsdn, H, E, S, I, pf, *dc, s);
   if (e == cudaSuccess)
     e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,
                      nullptr, s);
@@ -336,7 +339,7 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   }
   if (e == cudaSuccess)
     e = launch_ffn(static_cast<const bf16*>(x), perm, offsets, wgu, wdn, wsgu, wsdn, T, H, E, k, S, I, y_perm, y_sh,
-                   /*y_bf16=*/true, w, L, *dc, s, /*with_prep=*/!fused);
+                   /*y_bf16=*/true, w, L, *dc, s, /*with_prep=*/!fused, /*early=*/true);
   if (e == cudaSuccess)
     e = launch_combine(y_perm, inv, tw, S > 0 ? y_sh : nullptr, /*y_bf16=*/true, T, H, k, static_cast<bf16*>(out),
                        dc->err, s);

@@ -18,8 +18,6 @@ namespace {
 // One CTA per token; thread c owns 8 consecutive columns and issues one 16-byte
 // (bf16) or two 16-byte (fp32) loads per source row, all independent, so every
 // thread has its k+1 rows in flight at once.
-constexpr int kCombMaxThreads = kMaxHidden / 8;
-
 // Raw 16-byte pieces per source row: one for 8 bf16 columns, two for 8 fp32 columns.
 template <typename YT>
 struct Piece;

@@ -71,6 +71,8 @@ struct FfnParams {
   int y_bf16;
   int* err;
   uint64_t wait_ns;
+  int* counter;            // next item to deal
+  int n_static;            // leading gate/up items of the shared group, decodable without the table
 };
 
 struct FfnMaps {
@@ -97,6 +99,21 @@ struct Item {
 
 template <int BN>
 __device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
+  if (it < p.n_static) {
+    // the shared group's gate/up items come first and their layout is fixed by T alone
+    Item m;
+    const int nft = p.S * p.I / 64;
+    const int tt = it / nft;
+    m.gu = 1;
+    m.slot = 0;
+    m.g = p.E;
+    m.ft = it - tt * nft;
+    m.row0 = tt * BN;
+    m.cnt = min(BN, p.T - tt * BN);
+    m.nk = p.H / 64;
+    m.need = p.n_static;
+    return m;
+  }
   const int* tb = p.table;
   const int G = p.G;
   const int n_gu = tb[0];
@@ -201,15 +218,25 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  // the prologue above overlaps the previous kernel; everything below reads its results
-  pdl_wait();
+  // The prologue above overlaps the previous kernels.  Items below n_static need
+  // nothing they produce; every thread waits for them (griddepcontrol.wait)
+  // before its first other item.
   pdl_trigger();
+  bool waited = false;
+  auto wait_inputs = [&](int it) {
+    if (!waited && it >= p.n_static) {
+      pdl_wait();
+      waited = true;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer + item dealer
     if (lane == 0) {
-      const int n_items = p.table[0] + p.table[1];
-      int* counter = const_cast<int*>(p.table) + 3;
+      int n_items = -1;
+      int* counter = p.counter;
+      // without early items the counters are zeroed by the preceding kernel: wait for it first
+      if (p.n_static == 0) wait_inputs(0);
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
@@ -224,7 +251,11 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           break;
         }
         int it = atomicAdd(counter, 1);
-        if (it >= n_items) it = -1;
+        if (it >= p.n_static) {
+          wait_inputs(it);
+          if (n_items < 0) n_items = p.table[0] + p.table[1];
+          if (it >= n_items) it = -1;
+        }
         item_slot[slot] = it;
         mbar_arrive(&item_full[slot]);  // release: the slot write is visible to the waiters
         if (++slot == NS) {
@@ -311,6 +342,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           slot_phase ^= 1u;
         }
         if (it < 0 || *abort_flag) break;
+        wait_inputs(it);
         const Item m = decode_item<BN>(it, p);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_ns)) {
           set_error(p.err, kErrTimeout);
@@ -390,6 +422,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       }
       // the same decision in all epilogue warps keeps their named barriers matched
       if (named_bar_red_or(kEpiBarAll, kEpiThreads, it < 0)) break;
+      wait_inputs(it);
       const Item m = decode_item<BN>(it, p);
       const bool got = mbar_wait(&tfull[acc], acc_phase, p.wait_ns);
       if (!got) set_error(p.err, kErrTimeout);
@@ -481,7 +514,7 @@ template <int BN>
 __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ perm,
                                                        const int32_t* __restrict__ offsets, int T, int H, int E,
                                                        int k, int S, int I, bf16* __restrict__ xperm,
-                                                       int32_t* __restrict__ table, int* err) {
+                                                       int32_t* __restrict__ table, int* err, bool zero_counters) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -506,7 +539,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
       }
     }
   }
-  if (blockIdx.x == 0 && threadIdx.x < 32) build_item_table(offsets, T, H, E, k, S, I, BN, table, err);
+  if (blockIdx.x == 0 && threadIdx.x < 32) build_item_table(offsets, T, H, E, k, S, I, BN, table, err, zero_counters);
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -514,7 +547,7 @@ template <int BN, int STAGES, int KCH>
 cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                     const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E, int k,
                     int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws, const WsLayout& L,
-                    const DeviceCtx& dc, cudaStream_t s, bool with_prep) {
+                    const DeviceCtx& dc, cudaStream_t s, bool with_prep, bool early) {
   using SM = Smem<BN, STAGES, KCH>;
   static_assert(SM::kTotal <= 232448, "shared memory budget");
   static int attr_done[64] = {0};
@@ -534,7 +567,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   if (with_prep) {
     const int prep_blocks = max(1, (nrows + 7) / 8);
     const cudaError_t e = launch_pdl(ffn_prep_kernel<BN>, dim3(prep_blocks), dim3(256), 0, s, x, perm, offsets, T,
-                                     H, E, k, S, I, xperm, table, dc.err);
+                                     H, E, k, S, I, xperm, table, dc.err, /*zero_counters=*/!early);
     if (e != cudaSuccess) return e;
   }
 
@@ -554,7 +587,9 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.T = T; p.H = H; p.E = E; p.k = k; p.S = S; p.I = I; p.G = G;
   p.offsets = offsets;
   p.table = table;
-  p.done = table + 8 + 2 * G + 2;
+  p.done = table + table_counters(G);
+  p.counter = table + table_counters(G) + G;
+  p.n_static = (early && S > 0) ? ((T + BN - 1) / BN) * (S * I / 64) : 0;
   p.act = act;
   p.act_sh = act_sh;
   p.y_perm = y_perm;
@@ -580,20 +615,20 @@ int ffn_token_tile(int T, int k, int E) {
 cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                        const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
                        int k, int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws,
-                       const WsLayout& L, const DeviceCtx& dc, cudaStream_t s, bool with_prep) {
+                       const WsLayout& L, const DeviceCtx& dc, cudaStream_t s, bool with_prep, bool early) {
   switch (ffn_token_tile(T, k, E)) {
     case 32:
       return run_ffn<32, LSV_FFN_STAGES32, LSV_FFN_KCH32>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down,
-                                                          T, H, E, k, S, I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep);
+                                                          T, H, E, k, S, I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
     case 64:
       return run_ffn<64, 4, 2>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                               y_sh, y_bf16, ws, L, dc, s, with_prep);
+                               y_sh, y_bf16, ws, L, dc, s, with_prep, early);
     case 128:
       return run_ffn<128, 6, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                                y_sh, y_bf16, ws, L, dc, s, with_prep);
+                                y_sh, y_bf16, ws, L, dc, s, with_prep, early);
     default:
       return run_ffn<256, 4, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                                y_sh, y_bf16, ws, L, dc, s, with_prep);
+                                y_sh, y_bf16, ws, L, dc, s, with_prep, early);
   }
 }
 

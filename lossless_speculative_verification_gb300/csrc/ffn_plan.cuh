@@ -15,10 +15,12 @@ __host__ __device__ __forceinline__ int slot_group(int slot, int E, int S) {
 }
 
 // Item table (layout in internal.h) from the expert offsets, for token tiles of
-// BN rows.  Executed by all 32 lanes of one warp.  Offsets that do not describe
+// BN rows.  Executed by all 32 lanes of one warp.  zero_counters: also reset
+// the completion and dealing counters (otherwise the caller did, before the
+// routing began).  Offsets that do not describe
 // a partition of [0, T*k) schedule no item and raise LSV_ERR_DEVICE_INDEX.
 __device__ __forceinline__ void build_item_table(const int32_t* offsets, int T, int H, int E, int k, int S, int I,
-                                                 int BN, int32_t* table, int* err) {
+                                                 int BN, int32_t* table, int* err, bool zero_counters) {
   const int lane = threadIdx.x & 31;
   const int nrows = T * k;
   const int G = E + (S > 0 ? 1 : 0);
@@ -76,7 +78,7 @@ __device__ __forceinline__ void build_item_table(const int32_t* offsets, int T, 
       table[8 + slot] = gu_run;
       table[8 + G + 1 + slot] = dn_run;
     }
-    if (slot < G) table[8 + 2 * G + 2 + slot] = 0;
+    if (zero_counters && slot < G) table[8 + 2 * G + 2 + slot] = 0;
     gu_run += gu_loc[j];
     dn_run += dn_loc[j];
   }
@@ -84,7 +86,7 @@ __device__ __forceinline__ void build_item_table(const int32_t* offsets, int T, 
     table[0] = gu_incl;
     table[1] = dn_incl;
     table[2] = G;
-    table[3] = 0;  // next item to deal
+    if (zero_counters) table[8 + 3 * G + 2] = 0;  // next item to deal
   }
 }
 

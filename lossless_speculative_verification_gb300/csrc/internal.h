@@ -33,13 +33,16 @@ uint64_t wait_limit_ns();
 
 // ---------------------------------------------------------------- FFN tile table
 // int32 table in the workspace, written by the prep kernel, read by the FFN kernel.
-//   [0] gate/up items  [1] down items  [2] groups G  [3] next item to deal (zeroed by the prep kernel)
+//   [0] gate/up items  [1] down items  [2] groups G
 //   [8 .. 8+G]             gate/up item start per group slot (exclusive scan, G+1 entries)
 //   [8+G+1 .. 8+2G+1]      down item start per group slot (G+1 entries)
-//   [8+2G+2 .. 8+3G+1]     completed gate/up items per group slot (zeroed by the prep kernel)
-// Group slots are the dealing order: the shared group first (when S > 0), then
+//   [8+2G+2 .. 8+3G+1]     counters: completed gate/up items per group slot ...
+//   [8+3G+2]               ... and the next item to deal
+// The G+1 counters are contiguous so that one memset can zero them.  Group
+// slots are the dealing order: the shared group first (when S > 0), then
 // routed experts 0..E-1.
-inline int table_ints(int G) { return 8 + 3 * G + 2; }
+inline int table_ints(int G) { return 8 + 3 * G + 3; }
+inline int table_counters(int G) { return 8 + 2 * G + 2; }
 
 struct FfnGeom {
   int T, H, E, k, S, I, G, BN;
@@ -97,12 +100,16 @@ cudaError_t launch_weight_prefetch(const bf16* w_gate_up, const bf16* w_down, co
 
 int ffn_token_tile(int T, int k, int E);
 // Grouped experts.  with_prep: first gather the routed rows and build the item
-// table (otherwise launch_permute_gather already did).
+// table (otherwise launch_permute_gather already did).  early: the table's
+// counters were zeroed before the routing began, and the shared group's
+// gate/up items (which do not depend on the routing) may start before the
+// preceding kernels finish.
 // y_perm/y_sh are fp32, or bf16 when y_bf16 (the fused layer keeps them in bf16).
 cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                        const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
                        int k, int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws,
-                       const WsLayout& L, const DeviceCtx& dc, cudaStream_t s, bool with_prep = true);
+                       const WsLayout& L, const DeviceCtx& dc, cudaStream_t s, bool with_prep = true,
+                       bool early = false);
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_sh,
                            bool y_bf16, int T, int H, int k, bf16* out, int* err, cudaStream_t s);

@@ -172,8 +172,10 @@ __global__ void __launch_bounds__(kPgThreads) permute_gather_kernel(
   __shared__ int pre[kMaxExperts];
   __shared__ int off[kMaxExperts + 1];
   __shared__ int pos_s[kPgSlice];
-  pdl_wait();
+  // the grouped-expert kernel that follows may start its routing-independent
+  // items at once; anything that reads this kernel's results waits for it
   pdl_trigger();
+  pdl_wait();
   const int n = T * k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s0 = blockIdx.x * kPgSlice;
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(kPgThreads) permute_gather_kernel(
     }
     pos_s[lane] = pos;
   } else if (warp == 1 && blockIdx.x == 0) {
-    build_item_table(off, T, H, E, k, S, I, BN, table, err);
+    build_item_table(off, T, H, E, k, S, I, BN, table, err, /*zero_counters=*/false);
   }
   __syncthreads();
   for (int j = warp; j < s1 - s0; j += kPgThreads / 32) {
