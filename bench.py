@@ -296,41 +296,50 @@ def measure(step, args, local, world, flush, dist):
         b.synchronize()
         eager_ms.append(a.elapsed_time(b))
 
-    # the step as one CUDA graph with its timing events recorded as graph nodes (start, after the
-    # layers, end); where torch cannot record events inside a graph, two graphs with events between
+    # The step as one CUDA graph with its timing events recorded as graph nodes.  The step time
+    # comes from a graph with events at its start and end only; the layer/acceptance split (for
+    # the roofline) from replays of a second graph with one more event between the two, which
+    # costs the acceptance its programmatic early launch.  Where torch cannot record events
+    # inside a graph: two graphs with events between them.
     try:
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
         one_graph = True
     except TypeError:
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         one_graph = False
     if one_graph:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+        g_step, g_split = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
             evs[0].record()
             step.layer()
-            evs[1].record()
             step.accept()
+            evs[1].record()
+        with torch.cuda.graph(g_split):
             evs[2].record()
-        graphs = [g]
+            step.layer()
+            evs[3].record()
+            step.accept()
+            evs[4].record()
+        graphs = [g_step, g_split]
     else:
         graphs = [torch.cuda.CUDAGraph() for _ in range(2)]
         for g, fn in zip(graphs, (step.layer, step.accept)):
             with torch.cuda.graph(g):
                 fn()
 
-    def replay():
+    def replay(split):
         if one_graph:
-            graphs[0].replay()
+            graphs[1 if split else 0].replay()
         else:
-            evs[0].record(stream)
-            graphs[0].replay()
-            evs[1].record(stream)
-            graphs[1].replay()
             evs[2].record(stream)
+            graphs[0].replay()
+            evs[3].record(stream)
+            graphs[1].replay()
+            evs[4].record(stream)
 
     for _ in range(max(args.warmup, 0)):
-        replay()
+        replay(False)
+        replay(True)
     torch.cuda.synchronize()
     assert api.get_device_error() == 0
 
@@ -345,19 +354,27 @@ def measure(step, args, local, world, flush, dist):
         t_end = time.perf_counter() + 0.3
         while time.perf_counter() < t_end:
             flush.fill_(0)
-            replay()
+            replay(False)
         torch.cuda.synchronize()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
-            replay()
-            evs[2].synchronize()
-            step_ms.append(evs[0].elapsed_time(evs[2]))
-            layer_list.append(evs[0].elapsed_time(evs[1]))
-            accept_list.append(evs[1].elapsed_time(evs[2]))
+            replay(not one_graph)
+            if one_graph:
+                evs[1].synchronize()
+                step_ms.append(evs[0].elapsed_time(evs[1]))
+            else:
+                evs[4].synchronize()
+                step_ms.append(evs[2].elapsed_time(evs[4]))
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            replay(True)
+            evs[4].synchronize()
+            layer_list.append(evs[2].elapsed_time(evs[3]))
+            accept_list.append(evs[3].elapsed_time(evs[4]))
         t_end = time.perf_counter() + 0.3
         while time.perf_counter() < t_end:
             flush.fill_(0)
-            replay()
+            replay(False)
         torch.cuda.synchronize()
     assert api.get_device_error() == 0
     total_ms = sum(step_ms)
@@ -414,8 +431,9 @@ def result_line(args, step, m, world, cpu):
         "config": {"workload": "%s: %s" % (step.name, describe(w, len(step.layers))),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MB write, outside the events)",
-                   "timing": ("step replayed as one CUDA graph; CUDA events recorded as graph nodes at its start, "
-                              "after the layers and at its end" if m["one_graph"] else
+                   "timing": ("step replayed as one CUDA graph with CUDA events recorded as graph nodes at its "
+                              "start and end; the layer/acceptance split from K more replays of the same step "
+                              "with an event between them" if m["one_graph"] else
                               "step replayed as 2 CUDA graphs (layers, acceptance); CUDA events per step"),
                    "clocks_window": "nvidia-smi every 100 ms over back-to-back steps around the timed ones",
                    "eager_ms_per_step": m["eager_ms"]},

@@ -167,8 +167,8 @@ lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t
  *   (max, index) pairs), held by every device that loads the library until
  *   the process exits.  A problem needing more partials returns
  *   LSV_ERR_UNSUPPORTED before any launch; the count is B*(K+1) rows times
- *   the chunks per row (on a 152-SM GB300 9 chunks per row at 128 rows
- *   of 129,280 logits, 1 chunk per row beyond 1,216 rows, so up to 16,384 rows).
+ *   the chunks per row (on a 152-SM GB300 3 chunks per row at 128 rows of
+ *   129,280 logits, 1 chunk per row beyond 456 rows, so up to 16,384 rows).
  *   The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  *   routine.  The first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress) and caches it; make that first call before

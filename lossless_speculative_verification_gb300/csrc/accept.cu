@@ -8,10 +8,11 @@
 // identical to greedy decoding (kg.zhiyong.dev, "Why FastMTP fits OCR
 // particularly well"; evolve.pub review, Section 3.1 / Eq. 2).
 //
-// Phase 1 streams the logits once: each CTA owns a chunk of one row, loads it
-// with 16-byte non-allocating loads (8 bf16 each, several in flight per
-// thread) and writes the chunk's (max, first index).  Phase 2 (one CTA per
-// sequence, one warp per row) reduces the chunk partials and applies the rule.
+// Phase 1 streams the logits once: each CTA owns a chunk of one row, streams it
+// through a ring of shared-memory buffers filled by 1-D bulk copies (64 KB in
+// flight per CTA from a single issuing thread), scans it and writes the
+// chunk's (max, first index).  Phase 2 (one CTA per sequence, one warp per
+// row) reduces the chunk partials and applies the rule.
 // No atomics decide anything, so the result is deterministic.
 #include <limits.h>
 
@@ -25,17 +26,20 @@ namespace lsv {
 namespace {
 
 constexpr int kAccThreads = 256;
-constexpr int kUnroll = 4;
-constexpr int kAccMinBlocks = 8;  // resident CTAs per SM the chunking plans for (one wave)
-constexpr int kChunkQuantum = kAccThreads * 8;  // elements covered by one 16-B load per thread
-
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+#ifndef LSV_ACC_CTAS_PER_SM
+#define LSV_ACC_CTAS_PER_SM 3
+#endif
+#ifndef LSV_ACC_PIECE
+#define LSV_ACC_PIECE 16384
+#endif
+#ifndef LSV_ACC_RING
+#define LSV_ACC_RING 4
+#endif
+constexpr int kAccCtasPerSm = LSV_ACC_CTAS_PER_SM;  // resident CTAs per SM the chunking plans for (one wave)
+constexpr int kPiece = LSV_ACC_PIECE;                // bytes per bulk copy
+constexpr int kRingSlots = LSV_ACC_RING;             // bulk copies in flight per CTA
+constexpr int kMinChunk = 2048;       // elements
+constexpr int kScanVec = 4;           // 16-byte vectors a thread holds per scan step
 
 // (value desc, index asc) maximum
 __device__ __forceinline__ void better(float v, int i, float& bv, int& bi) {
@@ -56,43 +60,8 @@ __device__ __forceinline__ void scan8(const uint4& q, int base, float& bv, int& 
   }
 }
 
-__global__ void __launch_bounds__(kAccThreads, kAccMinBlocks) argmax_partial_kernel(const bf16* __restrict__ logits, int V,
-                                                                     int chunk, int nchunk, int vec_ok,
-                                                                     float* __restrict__ pv,
-                                                                     int* __restrict__ pi) {
-  pdl_wait();
-  pdl_trigger();
-  const int r = blockIdx.x, c = blockIdx.y;
-  const bf16* row = logits + (size_t)r * V;
-  const int begin = c * chunk;
-  const int end = min(V, begin + chunk);
-  float bv = -INFINITY;
-  int bi = INT_MAX;
-  if (vec_ok) {
-    // every thread walks its vectors in increasing index order
-    const int n8 = (end - begin) >> 3;
-    const uint4* p = reinterpret_cast<const uint4*>(row + begin);
-    for (int j0 = threadIdx.x; j0 < n8; j0 += kUnroll * kAccThreads) {
-      uint4 q[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int j = j0 + u * kAccThreads;
-        q[u] = j < n8 ? ld_stream_v4(p + j) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int j = j0 + u * kAccThreads;
-        if (j < n8) scan8(q[u], begin + 8 * j, bv, bi);
-      }
-    }
-    for (int e = begin + 8 * n8 + threadIdx.x; e < end; e += kAccThreads)
-      better(__bfloat162float(row[e]), e, bv, bi);
-  } else {
-    for (int e = begin + threadIdx.x; e < end; e += kAccThreads) {
-      const float f = __bfloat162float(row[e]);
-      if (f > bv) { bv = f; bi = e; }
-    }
-  }
+// Block-wide (max, first index) of the per-thread candidates, written by thread 0.
+__device__ __forceinline__ void block_reduce_store(float bv, int bi, float* pv, int* pi, size_t at) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -108,9 +77,107 @@ __global__ void __launch_bounds__(kAccThreads, kAccMinBlocks) argmax_partial_ker
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int w = 1; w < kAccThreads / 32; ++w) better(sv[w], si[w], bv, bi);
-    pv[(size_t)r * nchunk + c] = bv;
-    pi[(size_t)r * nchunk + c] = bi;
+    pv[at] = bv;
+    pi[at] = bi;
   }
+}
+
+// Rows whose start is not 16-byte aligned (V not a multiple of 8): 2-byte loads.
+__global__ void __launch_bounds__(kAccThreads) argmax_partial_scalar_kernel(const bf16* __restrict__ logits, int V,
+                                                                            int chunk, int nchunk,
+                                                                            float* __restrict__ pv,
+                                                                            int* __restrict__ pi) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x, c = blockIdx.y;
+  const bf16* row = logits + (size_t)r * V;
+  const int begin = c * chunk;
+  const int end = min(V, begin + chunk);
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  for (int e = begin + threadIdx.x; e < end; e += kAccThreads) {
+    const float f = __bfloat162float(row[e]);
+    if (f > bv) { bv = f; bi = e; }
+  }
+  block_reduce_store(bv, bi, pv, pi, (size_t)r * nchunk + c);
+}
+
+// 16-byte aligned rows: the chunk streams through a ring of kRingSlots shared
+// buffers filled by 1-D bulk copies (one thread issues them; kRingSlots x 16 KB
+// in flight), and the 256 threads scan each buffer as it lands.
+__global__ void __launch_bounds__(kAccThreads) argmax_partial_bulk_kernel(const bf16* __restrict__ logits, int V,
+                                                                          int chunk, int nchunk,
+                                                                          float* __restrict__ pv,
+                                                                          int* __restrict__ pi, int* err,
+                                                                          uint64_t wait_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t bar[kRingSlots];
+  const int r = blockIdx.x, c = blockIdx.y;
+  const int begin = c * chunk;                 // a multiple of 8 elements
+  const int end = min(V, begin + chunk);
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(logits + (size_t)r * V + begin);
+  const int bytes = (end - begin) * 2;         // a multiple of 16
+  const int npieces = (bytes + kPiece - 1) / kPiece;
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < kRingSlots; ++q) mbar_init(&bar[q], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < kRingSlots && q < npieces; ++q) {
+      const int n = min(kPiece, bytes - q * kPiece);
+      mbar_arrive_expect_tx(&bar[q], n);
+      bulk_load(ring + q * kPiece, src + (size_t)q * kPiece, n, &bar[q]);
+    }
+  }
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  bool ok = true;
+  for (int q = 0; q < npieces; ++q) {
+    const int slot = q % kRingSlots;
+    if (!mbar_wait(&bar[slot], (q / kRingSlots) & 1, wait_ns)) {
+      set_error(err, kErrTimeout);
+      ok = false;
+    }
+    if (__syncthreads_or(!ok)) break;
+    const int n = min(kPiece, bytes - q * kPiece);
+    const uint4* v = reinterpret_cast<const uint4*>(ring + slot * kPiece);
+    const int e0 = begin + q * (kPiece / 2);
+    for (int j0 = threadIdx.x; j0 < n / 16; j0 += kScanVec * kAccThreads) {
+      // this thread's vectors of the piece, in increasing index order
+      uint4 w[kScanVec];
+      __nv_bfloat162 m2 = __float2bfloat162_rn(-INFINITY);
+#pragma unroll
+      for (int u = 0; u < kScanVec; ++u) {
+        const int j = j0 + u * kAccThreads;
+        w[u] = j < n / 16 ? v[j] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);  // -inf pairs
+        m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&w[u].x));
+        m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&w[u].y));
+        m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&w[u].z));
+        m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&w[u].w));
+      }
+      const float m = fmaxf(__low2float(m2), __high2float(m2));
+      if (m > bv) {
+        // a new maximum (rare after the first pieces): locate its first occurrence among the
+        // values still in registers; equal values seen earlier keep their lower index
+        for (int u = 0; u < kScanVec; ++u) {
+          const int j = j0 + u * kAccThreads;
+          if (j < n / 16) scan8(w[u], e0 + 8 * j, bv, bi);
+        }
+      }
+    }
+    __syncthreads();  // the slot is free again
+    if (threadIdx.x == 0 && q + kRingSlots < npieces) {
+      const int qn = q + kRingSlots;
+      const int nn = min(kPiece, bytes - qn * kPiece);
+      mbar_arrive_expect_tx(&bar[slot], nn);
+      bulk_load(ring + slot * kPiece, src + (size_t)qn * kPiece, nn, &bar[slot]);
+    }
+  }
+  block_reduce_store(bv, bi, pv, pi, (size_t)r * nchunk + c);
 }
 
 // One CTA per sequence, one warp per verified row: each warp reduces its row's
@@ -154,17 +221,19 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finalize_kernel(
   }
 }
 
-int chunk_elems(int R, int V, int num_sms) {
-  // one wave of about 8 resident CTAs per SM: pick the chunks per row first, then
-  // the chunk length (a multiple of 8 elements, so 16-byte loads stay aligned)
-  const long long target = (long long)num_sms * kAccMinBlocks;
-  long long nchunk = target / (R > 0 ? R : 1);
-  const long long max_chunks = ((long long)V + kChunkQuantum - 1) / kChunkQuantum;  // at least one quantum each
-  if (nchunk > max_chunks) nchunk = max_chunks;
-  if (nchunk < 1) nchunk = 1;
-  long long per = ((long long)V + nchunk - 1) / nchunk;
+// Chunks per row and chunk length: one wave of about kAccCtasPerSm CTAs per SM
+// in total, at least kMinChunk elements per chunk, chunk lengths a multiple of
+// 8 elements (so that every chunk of an aligned row starts on 16 bytes).
+void chunk_plan(int R, int V, int num_sms, int* chunk, int* nchunk) {
+  const long long target = (long long)num_sms * kAccCtasPerSm;
+  long long n = target / (R > 0 ? R : 1);
+  const long long max_chunks = ((long long)V + kMinChunk - 1) / kMinChunk;
+  if (n > max_chunks) n = max_chunks;
+  if (n < 1) n = 1;
+  long long per = ((long long)V + n - 1) / n;
   per = (per + 7) / 8 * 8;
-  return (int)per;
+  *chunk = (int)per;
+  *nchunk = (int)(((long long)V + per - 1) / per);
 }
 
 }  // namespace
@@ -172,8 +241,8 @@ int chunk_elems(int R, int V, int num_sms) {
 size_t accept_ws_bytes(int B, int K, int V, int num_sms) {
   const int R = B * (K + 1);
   if (R == 0) return 256;
-  const int chunk = chunk_elems(R, V, num_sms);
-  const size_t nchunk = (V + chunk - 1) / chunk;
+  int chunk, nchunk;
+  chunk_plan(R, V, num_sms, &chunk, &nchunk);
   const size_t one = ((size_t)R * nchunk * 4 + 255) / 256 * 256;
   return 2 * one;
 }
@@ -183,17 +252,30 @@ cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int 
                           cudaStream_t s) {
   const int R = B * (K + 1);
   if (R == 0) return cudaSuccess;
-  const int chunk = chunk_elems(R, V, dc.num_sms);
-  const int nchunk = (V + chunk - 1) / chunk;
+  int chunk, nchunk;
+  chunk_plan(R, V, dc.num_sms, &chunk, &nchunk);
   const size_t one = ((size_t)R * nchunk * 4 + 255) / 256 * 256;
   float* pv = reinterpret_cast<float*>(ws);
   int* pi = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + one);
-  const int vec_ok = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
-  cudaError_t e = launch_pdl(argmax_partial_kernel, dim3(R, nchunk), dim3(kAccThreads), 0, s, logits, V, chunk,
-                             nchunk, vec_ok, pv, pi);
+  const bool aligned = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+  cudaError_t e;
+  if (aligned) {
+    constexpr int kSmem = kRingSlots * kPiece + 128;
+    static int attr_done[64] = {0};
+    if (dc.device >= 0 && dc.device < 64 && !attr_done[dc.device]) {
+      e = cudaFuncSetAttribute(argmax_partial_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      attr_done[dc.device] = 1;
+    }
+    e = launch_pdl(argmax_partial_bulk_kernel, dim3(R, nchunk), dim3(kAccThreads), kSmem, s, logits, V, chunk, nchunk,
+                   pv, pi, dc.err, wait_limit_ns());
+  } else {
+    e = launch_pdl(argmax_partial_scalar_kernel, dim3(R, nchunk), dim3(kAccThreads), 0, s, logits, V, chunk, nchunk,
+                   pv, pi);
+  }
   if (e != cudaSuccess) return e;
-  return launch_pdl(accept_finalize_kernel, dim3(B), dim3(32 * min(K + 1, kFinWarps)), 0, s, (const float*)pv, (const int*)pi,
-                    nchunk, drafts, B, K, argmax, accept_len, committed);
+  return launch_pdl(accept_finalize_kernel, dim3(B), dim3(32 * min(K + 1, kFinWarps)), 0, s, (const float*)pv,
+                    (const int*)pi, nchunk, drafts, B, K, argmax, accept_len, committed);
 }
 
 }  // namespace lsv
