@@ -12,7 +12,8 @@ Prints one JSON line per measured configuration (rank 0; the default run
 prints exactly one).  `value` is tokens/s with all inputs resident in HBM;
 `e2e` is the same through the public API with host buffers (pinned host ->
 device copies and the read-back inside the timed region).  Before every
-timed step L2 is flushed by writing a 256 MB buffer (outside the events).
+timed step L2 is flushed by writing a 256 MB buffer and reading it back (outside the
+events), so that no dirty line of the flush is written back inside the step.
 The `--impl reference` arm times the CPU oracle on a bounded sample of the
 same workload.
 
@@ -274,6 +275,14 @@ class DeviceStep:
         self.h_out.copy_(self.out, non_blocking=True)
 
 
+def flush_l2(flush, i):
+    """Evict the step's data from L2: write a buffer larger than L2, then read it back, so that the
+    L2 holds only clean lines of the flush buffer and the step pays no write-back of them."""
+    import torch
+    flush.fill_(i & 0xFF)
+    torch.amax(flush.view(torch.int32))
+
+
 def measure(step, args, local, world, flush, dist):
     """Warm up, time `steps` graph replays (L2 flushed before each), then the e2e path."""
     import torch
@@ -287,7 +296,7 @@ def measure(step, args, local, world, flush, dist):
 
     eager_ms = []
     for i in range(min(args.steps, 10)):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, i)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         step.layer()
@@ -353,11 +362,11 @@ def measure(step, args, local, world, flush, dist):
         clk.wait_first_sample()
         t_end = time.perf_counter() + 0.3
         while time.perf_counter() < t_end:
-            flush.fill_(0)
+            flush_l2(flush, 0)
             replay(False)
         torch.cuda.synchronize()
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i)
             replay(not one_graph)
             if one_graph:
                 evs[1].synchronize()
@@ -366,14 +375,14 @@ def measure(step, args, local, world, flush, dist):
                 evs[4].synchronize()
                 step_ms.append(evs[2].elapsed_time(evs[4]))
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i)
             replay(True)
             evs[4].synchronize()
             layer_list.append(evs[2].elapsed_time(evs[3]))
             accept_list.append(evs[3].elapsed_time(evs[4]))
         t_end = time.perf_counter() + 0.3
         while time.perf_counter() < t_end:
-            flush.fill_(0)
+            flush_l2(flush, 0)
             replay(False)
         torch.cuda.synchronize()
     assert api.get_device_error() == 0
@@ -387,7 +396,7 @@ def measure(step, args, local, world, flush, dist):
     torch.cuda.synchronize()
     e2e_total = 0.0
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, i)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         step.e2e()
@@ -430,7 +439,7 @@ def result_line(args, step, m, world, cpu):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "%s: %s" % (step.name, describe(w, len(step.layers))),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "flushed before every timed step (256 MB write, outside the events)",
+                   "l2": "flushed before every timed step (256 MB written, then read back, outside the events)",
                    "timing": ("step replayed as one CUDA graph with CUDA events recorded as graph nodes at its "
                               "start and end; the layer/acceptance split from K more replays of the same step "
                               "with an event between them" if m["one_graph"] else
