@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the timed oracle sample (for profiler runs; the line then has no cpu_baseline)")
     return ap.parse_args()
 
 
@@ -552,7 +554,7 @@ def run_ours(args, rank, world, local):
         step = DeviceStep(name, w, seed + args.seed + 1000 * rank, dev)
         m = measure(step, args, local, world, flush, dist)
         cpu = None
-        if rank == 0 and world == 1:
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
             cpu = oracle_sampler(w, seed + args.seed)(12.0 if args.workload != "sweep" else 2.0)
         if rank == 0:
             print(json.dumps(result_line(args, step, m, world, cpu)), flush=True)

@@ -17,8 +17,8 @@
 // with the 128-byte swizzle, loaded by TMA.
 //
 //   gate/up item (g, token tile, 64 features f0..f0+63):
-//     A = [gate rows f0..f0+63 ; up rows f0..f0+63]  (two 64-row TMA boxes)
-//     D[128 x n] in TMEM: lanes 0-63 gate, lanes 64-127 up
+//     A = gate row f0, up row f0, gate row f0+1, up row f0+1, ...  (one 3-D TMA box)
+//     D[128 x n] in TMEM: lane 2j gate of feature f0+j, lane 2j+1 its up
 //     epilogue: act[row, f] = bf16( silu(gate) * up )
 //   down item (g, token tile, 128 outputs h0..h0+127):
 //     A = W_down rows h0..h0+127, B = act rows;  y[row, h] = D (fp32)
@@ -47,9 +47,20 @@ constexpr int kFfnThreads = 320;         // 10 warps
 constexpr int kEpiWarps = 8;             // warps 2..9: two per TMEM lane quadrant
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
-constexpr int kXchStride = 9;            // padded 8-value row of the gate/up exchange buffer
-constexpr int kXchPair = 2 * 32 * kXchStride;  // floats per (pair, buffer): gate->up and up->gate halves
-constexpr int kEpiBarAll = 5;            // named barrier over all epilogue warps (ids 1..4: warp pairs)
+constexpr int kEpiBarAll = 1;            // named barrier over all epilogue warps
+
+// Token tiles from which on the producer takes each next item index one item early.
+#ifndef LSV_FFN_DEAL_AHEAD_BN
+#define LSV_FFN_DEAL_AHEAD_BN 128
+#endif
+
+// Pipeline of the CTA-pair kernel (token tiles of 256 rows): stages and K chunks per stage.
+#ifndef LSV_FFN_STAGES256P
+#define LSV_FFN_STAGES256P 6
+#endif
+#ifndef LSV_FFN_KCH256P
+#define LSV_FFN_KCH256P 1
+#endif
 
 // Decode-size pipeline: K chunks (64 wide) per stage and stage count.
 #ifndef LSV_FFN_KCH32
@@ -73,11 +84,12 @@ struct FfnParams {
   uint64_t wait_ns;
   int* counter;            // next item to deal
   int n_static;            // leading gate/up items of the shared group, decodable without the table
+  int deal_ahead;          // take each next item index one item early
 };
 
 struct FfnMaps {
-  CUtensorMap wgu;     // [E*2I, H]   box 64 x 64
-  CUtensorMap wsgu;    // [2SI, H]    box 64 x 64
+  CUtensorMap wgu;     // [E*2I, H]   as {H, 2, E*2I}, box 64 x 2 x 64 (gate/up interleaved)
+  CUtensorMap wsgu;    // [2SI, H]    as {H, 2, SI},   box 64 x 2 x 64
   CUtensorMap wd;      // [E*H, I]    box 64 x 128
   CUtensorMap wsd;     // [H, SI]     box 64 x 128
   CUtensorMap xperm;   // [T*k, H]    box 64 x BN
@@ -90,36 +102,48 @@ struct Item {
   int gu;    // 1: gate/up, 0: down
   int slot;  // position of the group in the dealing order
   int g;     // group
-  int ft;    // feature tile (64 features for gate/up, 128 outputs for down)
+  int ft;    // first feature tile (64 features for gate/up, 128 outputs for down); FPI tiles per item
+  int nft;   // feature tiles of this kind in the group
   int row0;  // first token row of the tile in the group's row space
   int cnt;   // valid token rows in the tile (1..BN)
   int nk;    // 64-wide K chunks
-  int need;  // gate/up items of group g (for a down item's dependency)
+  int need;  // completions a down item of group g waits for (one per gate/up feature tile)
 };
 
-template <int BN>
-__device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
+// Shared-memory copy of the item table's starts and the expert offsets, so that
+// decoding an item costs no global-memory round trips:
+//   [0] gate/up items, [1] all items, [2, 2+G] gate/up starts per slot,
+//   [3+G, 3+2G] down starts per slot, [4+2G, 4+2G+E] expert offsets.
+constexpr int kTabInts = 2 + 2 * (kMaxExperts + 2) + kMaxExperts + 1;
+constexpr int kDealFailed = -2;  // the mailbox wait ran out
+
+// Item `it` of the dealing order.  FPI feature tiles per item (2 for CTA pairs:
+// tile ft + rank goes to the CTA of that rank).
+template <int BN, int FPI>
+__device__ __forceinline__ Item decode_item(int it, const FfnParams& p, const int* tab) {
   if (it < p.n_static) {
     // the shared group's gate/up items come first and their layout is fixed by T alone
     Item m;
     const int nft = p.S * p.I / 64;
-    const int tt = it / nft;
+    const int nit = (nft + FPI - 1) / FPI;
+    const int tt = it / nit;
     m.gu = 1;
     m.slot = 0;
     m.g = p.E;
-    m.ft = it - tt * nft;
+    m.ft = (it - tt * nit) * FPI;
+    m.nft = nft;
     m.row0 = tt * BN;
     m.cnt = min(BN, p.T - tt * BN);
     m.nk = p.H / 64;
-    m.need = p.n_static;
+    m.need = p.n_static * FPI;
     return m;
   }
-  const int* tb = p.table;
   const int G = p.G;
-  const int n_gu = tb[0];
+  const int n_gu = tab[0];
+  const int* offsets = tab + 4 + 2 * G;
   Item m;
   m.gu = it < n_gu;
-  const int* starts = m.gu ? tb + 8 : tb + 8 + G + 1;
+  const int* starts = m.gu ? tab + 2 : tab + 3 + G;
   const int local_it = m.gu ? it : it - n_gu;
   int lo = 0, hi = G - 1;  // largest g with starts[g] <= local_it
   while (lo < hi) {
@@ -130,14 +154,15 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
   m.g = slot_group(lo, p.E, p.S);
   const bool routed = m.g < p.E;
   const int inter = routed ? p.I : p.S * p.I;
-  const int nft = m.gu ? inter / 64 : (p.H + 127) / 128;
+  m.nft = m.gu ? inter / 64 : (p.H + 127) / 128;
+  const int nit = (m.nft + FPI - 1) / FPI;
   const int local = local_it - starts[m.slot];
-  const int tt = local / nft;
-  m.ft = local - tt * nft;
+  const int tt = local / nit;
+  m.ft = (local - tt * nit) * FPI;
   int seg0, segn;
   if (routed) {
-    seg0 = p.offsets[m.g];
-    segn = p.offsets[m.g + 1] - seg0;
+    seg0 = offsets[m.g];
+    segn = offsets[m.g + 1] - seg0;
   } else {
     seg0 = 0;
     segn = p.T;
@@ -145,35 +170,44 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p) {
   m.row0 = seg0 + tt * BN;
   m.cnt = min(BN, segn - tt * BN);
   m.nk = m.gu ? p.H / 64 : inter / 64;
-  m.need = tb[8 + m.slot + 1] - tb[8 + m.slot];
+  m.need = (tab[2 + m.slot + 1] - tab[2 + m.slot]) * FPI;
   return m;
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the hardware exponential and the fast divide (the
+// result is rounded to bf16; for z below about -88, e^-z overflows and it gives -0).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-template <int BN, int STAGES, int KCH>
+template <int BN, int STAGES, int KCH, bool PAIR>
 struct Smem {
-  static constexpr int kChunkA = kATileBytes;               // one 64-wide K chunk of A
-  static constexpr int kChunkB = BN * 128;                  // one 64-wide K chunk of B
+  static constexpr int kChunkA = kATileBytes;                   // one 64-wide K chunk of A
+  static constexpr int kChunkB = (PAIR ? BN / 2 : BN) * 128;    // one 64-wide K chunk of this CTA's B rows
   static constexpr int kStageBytes = KCH * (kChunkA + kChunkB);
   static constexpr int kRing = STAGES * kStageBytes;
-  static constexpr int kXch = 4 /*pairs*/ * 2 /*buffers*/ * kXchPair * 4;
   static constexpr int kItemSlots = 4;
-  static constexpr int kBars = (2 * STAGES + 5 + 2 * kItemSlots) * 8;
-  static constexpr int kTotal = 1024 /*alignment slack*/ + kRing + kXch + kBars + 16 + kItemSlots * 4;
+  static constexpr int kBars = (2 * STAGES + 5 + 4 * kItemSlots) * 8;
+  static constexpr int kTotal = 1024 /*alignment slack*/ + kRing + kBars + 16 + 2 * kItemSlots * 4 +
+                                kItemSlots * (int)sizeof(Item) + kTabInts * 4;
   static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
 };
 
-template <int BN, int STAGES, int KCH>
+// PAIR: the kernel runs as clusters of two CTAs.  The even CTA (the leader)
+// deals items and passes each index to its peer through a shared-memory
+// mailbox; both CTAs stage their own A tile (feature tile ft + rank) and their
+// half of the token rows, and count the bytes on the leader's stage barrier.
+// The leader issues one M = 256 MMA stream for both (cta_group::2) and its
+// commits release the stage and accumulator barriers of both CTAs; each
+// CTA's epilogue drains its own TMEM and reports back to the leader.
+template <int BN, int STAGES, int KCH, bool PAIR>
 __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_constant__ FfnMaps maps,
                                                               const FfnParams p) {
-  using SM = Smem<BN, STAGES, KCH>;
+  using SM = Smem<BN, STAGES, KCH, PAIR>;
   constexpr int NS = SM::kItemSlots;
+  constexpr int FPI = PAIR ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* xch = reinterpret_cast<float*>(smem + SM::kRing);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kRing + SM::kXch);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kRing);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -181,11 +215,18 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
   uint64_t* final_bar = tempty + 2;
   uint64_t* item_full = final_bar + 1;
   uint64_t* item_empty = item_full + NS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(item_empty + NS);
+  uint64_t* deal_full = item_empty + NS;   // PAIR, peer: an index is in the mailbox
+  uint64_t* deal_empty = deal_full + NS;   // PAIR, leader: the peer has taken the index
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(deal_empty + NS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* deal_slot = item_slot + NS;
+  Item* item_ring = reinterpret_cast<Item*>(const_cast<int*>(deal_slot + NS));  // decoded items
+  int* tab = reinterpret_cast<int*>(item_ring + NS);                             // kTabInts
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -194,19 +235,26 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiThreads);
+      mbar_init(&tempty[a], PAIR ? 2 : kEpiThreads);
     }
     for (int q = 0; q < NS; ++q) {
       mbar_init(&item_full[q], 1);
-      mbar_init(&item_empty[q], 1 + kEpiThreads);
+      mbar_init(&item_empty[q], (!PAIR || leader ? 1 : 0) + kEpiThreads);
+      mbar_init(&deal_full[q], 1);
+      mbar_init(&deal_empty[q], 1);
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, SM::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, SM::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, SM::kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (threadIdx.x == 32) {
     tma_prefetch_desc(&maps.wgu);
@@ -214,8 +262,12 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     tma_prefetch_desc(&maps.wsgu);
     tma_prefetch_desc(&maps.wsd);
   }
+  __syncwarp();
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // both CTAs' barriers exist before either signals the other
+  else
+    __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // The prologue above overlaps the previous kernels.  Items below n_static need
@@ -233,12 +285,52 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer + item dealer
     if (lane == 0) {
-      int n_items = -1;
       int* counter = p.counter;
       // without early items the counters are zeroed by the preceding kernel: wait for it first
       if (p.n_static == 0) wait_inputs(0);
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
+      bool have_tab = false;
+      int dq = 0;  // mailbox position (PAIR)
+      uint32_t dq_phase = 0;
+      // An index past the early items needs the routing: wait for the preceding kernels and
+      // copy the item table to shared memory (once); -1 past the last item.
+      auto resolve = [&](int it) {
+        if (it >= p.n_static) {
+          wait_inputs(it);
+          if (!have_tab) {
+            const int G = p.G;
+            tab[0] = p.table[0];
+            tab[1] = p.table[0] + p.table[1];
+            for (int i = 0; i <= G; ++i) {
+              tab[2 + i] = p.table[8 + i];
+              tab[3 + G + i] = p.table[8 + G + 1 + i];
+            }
+            for (int i = 0; i <= p.E; ++i) tab[4 + 2 * G + i] = p.offsets[i];
+            have_tab = true;
+          }
+          if (it >= tab[1]) it = -1;
+        }
+        return it;
+      };
+      // Next index from the counter; a pair's leader also posts it to the peer's mailbox at once.
+      auto deal = [&]() -> int {
+        const int raw = atomicAdd(counter, 1);
+        if constexpr (PAIR) {
+          if (!mbar_wait(&deal_empty[dq], dq_phase ^ 1u, p.wait_ns)) {
+            set_error(p.err, kErrTimeout);
+            return kDealFailed;
+          }
+          st_shared_cluster_s32(mapa_shared(smem_u32((const void*)&deal_slot[dq]), 1), raw);
+          mbar_arrive_cluster(mapa_shared(smem_u32(&deal_full[dq]), 1));
+          if (++dq == NS) {
+            dq = 0;
+            dq_phase ^= 1u;
+          }
+        }
+        return raw;
+      };
+      int ahead = -1;  // index taken from the counter one item early (p.deal_ahead)
       int stage = 0;
       uint32_t phase = 0;
       int slot = 0;
@@ -250,20 +342,53 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           ok = false;
           break;
         }
-        int it = atomicAdd(counter, 1);
-        if (it >= p.n_static) {
-          wait_inputs(it);
-          if (n_items < 0) n_items = p.table[0] + p.table[1];
-          if (it >= n_items) it = -1;
+        int it = -1;
+        if (!PAIR || leader) {
+          const int raw = ahead >= 0 ? ahead : deal();
+          ahead = -1;
+          if (raw == kDealFailed) {
+            ok = false;
+            break;
+          }
+          it = resolve(raw);
+        } else if constexpr (PAIR) {
+          // the peer takes the leader's indices, in order, from its mailbox
+          if (!mbar_wait_cluster(&deal_full[dq], dq_phase, p.wait_ns)) {
+            set_error(p.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+          const int raw = deal_slot[dq];
+          mbar_arrive_cluster(mapa_shared(smem_u32(&deal_empty[dq]), 0));
+          if (++dq == NS) {
+            dq = 0;
+            dq_phase ^= 1u;
+          }
+          it = resolve(raw);
+        }
+        Item m;
+        if (it >= 0) {
+          m = decode_item<BN, FPI>(it, p, tab);
+          item_ring[slot] = m;
         }
         item_slot[slot] = it;
-        mbar_arrive(&item_full[slot]);  // release: the slot write is visible to the waiters
+        mbar_arrive(&item_full[slot]);  // release: the slot writes are visible to the waiters
         if (++slot == NS) {
           slot = 0;
           slot_phase ^= 1u;
         }
         if (it < 0) break;
-        const Item m = decode_item<BN>(it, p);
+        // Take the next index now, so that the counter's round trip overlaps this item's loads.
+        // A held index never waits on anything (only a gate/up item is held while the current one
+        // is a gate/up item, and all gate/up items precede all down items), so every down item's
+        // wait still ends.
+        if (p.deal_ahead && (!PAIR || leader)) {
+          ahead = deal();
+          if (ahead == kDealFailed) {
+            ok = false;
+            break;
+          }
+        }
         const bool routed = m.g < p.E;
         if (!m.gu) {
           if (!wait_counter_geq(&p.done[m.slot], m.need, p.wait_ns)) {
@@ -275,15 +400,15 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         }
         const CUtensorMap* amap = m.gu ? (routed ? &maps.wgu : &maps.wsgu) : (routed ? &maps.wd : &maps.wsd);
         const CUtensorMap* bmap = m.gu ? (routed ? &maps.xperm : &maps.x) : (routed ? &maps.act : &maps.act_sh);
-        int arow0, arow1 = 0;
-        if (m.gu) {
-          const int inter = routed ? p.I : p.S * p.I;
-          const int gbase = routed ? m.g * 2 * p.I : 0;
-          arow0 = gbase + m.ft * 64;
-          arow1 = gbase + inter + m.ft * 64;
-        } else {
-          arow0 = (routed ? m.g * p.H : 0) + m.ft * 128;
-        }
+        // this CTA's feature tile; past the group's last tile (odd count, PAIR) it stages the last
+        // one again and its epilogue discards the result
+        const int ft = min(m.ft + (int)rank, m.nft - 1);
+        // gate/up: the gate rows of 64 features, each staged next to its up row (3-D box);
+        // down: 128 output rows
+        const int arow0 = m.gu ? (routed ? m.g * 2 * p.I : 0) + ft * 64 : (routed ? m.g * p.H : 0) + ft * 128;
+        // PAIR: the MMA takes n/2 token rows from each CTA
+        const int n_mma = max(16, (m.cnt + 15) & ~15);
+        const int brow0 = m.row0 + (PAIR ? (int)rank * (n_mma / 2) : 0);
         for (int kc0 = 0; kc0 < m.nk; kc0 += KCH) {
           const int nch = min(KCH, m.nk - kc0);
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
@@ -293,17 +418,31 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           }
           uint8_t* a_s = smem + stage * SM::kStageBytes;
           uint8_t* b_s = a_s + KCH * SM::kChunkA;
-          mbar_arrive_expect_tx(&full[stage], nch * (SM::kChunkA + SM::kChunkB));
-          // all K chunks of one weight row block back to back: neighbouring 128-byte pieces of
-          // every row reach the memory system together
-          for (int c = 0; c < nch; ++c)
-            tma_load_2d(a_s + c * SM::kChunkA, amap, &full[stage], (kc0 + c) * 64, arow0, pol_w);
-          if (m.gu)
+          if constexpr (PAIR) {
+            // both CTAs' bytes complete the leader's stage barrier
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * nch * (SM::kChunkA + SM::kChunkB));
+            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+            for (int c = 0; c < nch; ++c) {
+              if (m.gu)
+                tma_load_3d_pair(a_s + c * SM::kChunkA, amap, fb, (kc0 + c) * 64, 0, arow0, pol_w);
+              else
+                tma_load_2d_pair(a_s + c * SM::kChunkA, amap, fb, (kc0 + c) * 64, arow0, pol_w);
+            }
             for (int c = 0; c < nch; ++c)
-              tma_load_2d(a_s + c * SM::kChunkA + kATileBytes / 2, amap, &full[stage], (kc0 + c) * 64, arow1,
-                          pol_w);
-          for (int c = 0; c < nch; ++c)
-            tma_load_2d(b_s + c * SM::kChunkB, bmap, &full[stage], (kc0 + c) * 64, m.row0, pol_x);
+              tma_load_2d_pair(b_s + c * SM::kChunkB, bmap, fb, (kc0 + c) * 64, brow0, pol_x);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], nch * (SM::kChunkA + SM::kChunkB));
+            // all K chunks of one weight row block back to back: neighbouring 128-byte pieces of
+            // every row reach the memory system together
+            for (int c = 0; c < nch; ++c) {
+              if (m.gu)
+                tma_load_3d(a_s + c * SM::kChunkA, amap, &full[stage], (kc0 + c) * 64, 0, arow0, pol_w);
+              else
+                tma_load_2d(a_s + c * SM::kChunkA, amap, &full[stage], (kc0 + c) * 64, arow0, pol_w);
+            }
+            for (int c = 0; c < nch; ++c)
+              tma_load_2d(b_s + c * SM::kChunkB, bmap, &full[stage], (kc0 + c) * 64, brow0, pol_x);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -320,8 +459,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (the leader's, for a pair)
+    if (lane == 0 && (!PAIR || leader)) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -336,22 +475,23 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           break;
         }
         const int it = item_slot[slot];
+        const Item m = item_ring[slot];
         mbar_arrive(&item_empty[slot]);
         if (++slot == NS) {
           slot = 0;
           slot_phase ^= 1u;
         }
         if (it < 0 || *abort_flag) break;
-        wait_inputs(it);
-        const Item m = decode_item<BN>(it, p);
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_ns)) {
+        const bool freed = PAIR ? mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, p.wait_ns)
+                                : mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_ns);
+        if (!freed) {
           set_error(p.err, kErrTimeout);
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const int n_mma = max(16, (m.cnt + 15) & ~15);
-        const uint32_t idesc = idesc_bf16_f32(128, n_mma);
+        const uint32_t idesc = idesc_bf16_f32(PAIR ? 256 : 128, n_mma);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kc0 = 0; kc0 < m.nk; kc0 += KCH) {
           const int nch = min(KCH, m.nk - kc0);
@@ -369,19 +509,30 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           const uint32_t b_s = a_s + KCH * SM::kChunkA;
           for (int c = 0; c < nch; ++c) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(d_tmem, sdesc_kmajor_sw128(a_s + c * SM::kChunkA + kk * 32),
-                        sdesc_kmajor_sw128(b_s + c * SM::kChunkB + kk * 32), idesc,
-                        ((kc0 + c) | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_kmajor_sw128(a_s + c * SM::kChunkA + kk * 32);
+              const uint64_t bd = sdesc_kmajor_sw128(b_s + c * SM::kChunkB + kk * 32);
+              const uint32_t accum = ((kc0 + c) | kk) ? 1u : 0u;
+              if constexpr (PAIR)
+                umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+              else
+                umma_bf16(d_tmem, ad, bd, idesc, accum);
+            }
           }
-          umma_commit(&empty[stage]);
+          if constexpr (PAIR)
+            umma_commit_pair_mc(&empty[stage], 0x3);
+          else
+            umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (PAIR)
+          umma_commit_pair_mc(&tfull[acc], 0x3);
+        else
+          umma_commit(&tfull[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -390,31 +541,34 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       __threadfence_block();
       if (!ok) mbar_arrive(&tfull[acc]);
       // every MMA issued by this thread has completed before TMEM is released
-      umma_commit(final_bar);
+      if constexpr (PAIR)
+        umma_commit_pair_mc(final_bar, 0x1);
+      else
+        umma_commit(final_bar);
       if (!mbar_wait(final_bar, 0, p.wait_ns)) set_error(p.err, kErrTimeout);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..9)
     // Warp w may read TMEM lanes 32*(w%4)..+31.  Two warps per quadrant split the
-    // 16-column chunks of an accumulator (half h takes chunks h, h+2, ...).  For
-    // gate/up items the warp holding gate rows (quadrant 0/1) and the one holding
-    // the matching up rows (quadrant 2/3) swap half of each chunk through shared
-    // memory, so that both compute SwiGLU on eight columns.
+    // accumulator's columns in blocks of EC = 16 (half h takes blocks h, h+2, ...).
+    // A gate/up accumulator holds feature j's gate products in lane 2j and its up
+    // products in lane 2j+1: the two lanes swap half of each block with one
+    // shuffle per column, and each computes SwiGLU on the other half.
+    constexpr int EC = 16;
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int pair = (q & 1) + 2 * half;     // gate/up warp pair, named barrier 1 + pair
-    const bool is_gate = q < 2;
-    float* xpair = xch + pair * 2 * kXchPair;
+    const bool is_up = lane & 1;
     int acc = 0;
     uint32_t acc_phase = 0;
     int slot = 0;
     uint32_t slot_phase = 0;
-    int nx = 0;  // chunks exchanged so far (selects the buffer)
     while (true) {
       const bool got_item = mbar_wait(&item_full[slot], slot_phase, p.wait_ns);
       if (!got_item) set_error(p.err, kErrTimeout);
       const int it = got_item ? item_slot[slot] : -1;
+      Item m;
+      if (it >= 0) m = item_ring[slot];
       mbar_arrive(&item_empty[slot]);
       if (++slot == NS) {
         slot = 0;
@@ -423,7 +577,6 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       // the same decision in all epilogue warps keeps their named barriers matched
       if (named_bar_red_or(kEpiBarAll, kEpiThreads, it < 0)) break;
       wait_inputs(it);
-      const Item m = decode_item<BN>(it, p);
       const bool got = mbar_wait(&tfull[acc], acc_phase, p.wait_ns);
       if (!got) set_error(p.err, kErrTimeout);
       if (named_bar_red_or(kEpiBarAll, kEpiThreads, !got || *abort_flag)) break;
@@ -431,47 +584,39 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       const bool routed = m.g < p.E;
       const int nrows_out = routed ? p.T * p.k : p.T;
       const int n_mma = max(16, (m.cnt + 15) & ~15);
+      const int ft = m.ft + (int)rank;
+      const bool own = ft < m.nft;  // false: the duplicate tile of an odd count (PAIR)
       const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
       if (m.gu) {
         bf16* out = routed ? p.act : p.act_sh;
         const int ld = routed ? p.I : p.S * p.I;
-        const int f = m.ft * 64 + (q & 1) * 32 + lane;
-        for (int c0 = 16 * half; c0 < n_mma; c0 += 32) {
-          uint32_t r[16];
+        const int f = ft * 64 + 16 * q + (lane >> 1);
+        for (int c0 = EC * half; c0 < n_mma; c0 += 2 * EC) {
+          uint32_t r[EC];
           tmem_ld_32x32b_x16(t_row + c0, r);
           tmem_ld_wait();
-          float* buf = xpair + (nx & 1) * kXchPair;
-          float* g2u = buf + lane * kXchStride;                 // gate values of columns 8..15
-          float* u2g = buf + (32 + lane) * kXchStride;          // up values of columns 0..7
-          if (is_gate) {
+          // the gate lane takes the block's first EC/2 columns, the up lane the rest
+          const int cb = c0 + (is_up ? EC / 2 : 0);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) g2u[j] = __uint_as_float(r[8 + j]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) u2g[j] = __uint_as_float(r[j]);
-          }
-          named_bar_sync(1 + pair, 64);
-          const int jb = is_gate ? 0 : 8;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int col = c0 + jb + j;
-            const float gv = is_gate ? __uint_as_float(r[j]) : g2u[j];
-            const float uv = is_gate ? u2g[j] : __uint_as_float(r[8 + j]);
-            if (col < m.cnt && m.row0 + col < nrows_out)
+          for (int j = 0; j < EC / 2; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, __uint_as_float(is_up ? r[j] : r[EC / 2 + j]), 1);
+            const float gv = is_up ? other : __uint_as_float(r[j]);
+            const float uv = is_up ? __uint_as_float(r[EC / 2 + j]) : other;
+            const int col = cb + j;
+            if (own && col < m.cnt && m.row0 + col < nrows_out)
               out[(size_t)(m.row0 + col) * ld + f] = __float2bfloat16_rn(silu(gv) * uv);
           }
-          ++nx;
         }
       } else {
         void* out = routed ? p.y_perm : p.y_sh;
-        const int h = m.ft * 128 + q * 32 + lane;
-        for (int c0 = 16 * half; c0 < n_mma; c0 += 32) {
-          uint32_t r[16];
+        const int h = ft * 128 + q * 32 + lane;
+        for (int c0 = EC * half; c0 < n_mma; c0 += 2 * EC) {
+          uint32_t r[EC];
           tmem_ld_32x32b_x16(t_row + c0, r);
           tmem_ld_wait();
-          if (h < p.H) {
+          if (own && h < p.H) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < EC; ++j) {
               const int col = c0 + j;
               if (col < m.cnt && m.row0 + col < nrows_out) {
                 const size_t o = (size_t)(m.row0 + col) * p.H + h;
@@ -485,14 +630,28 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         }
       }
       tc_fence_before_sync();
-      mbar_arrive(&tempty[acc]);
-      if (m.gu) {
-        // publish this gate/up item to the down items of its group
+      if constexpr (PAIR) {
+        // one arrival per CTA on the leader's accumulator barrier, after all of this CTA's TMEM reads
         named_bar_sync(kEpiBarAll, kEpiThreads);
         if (threadIdx.x == 64) {
-          fence_proxy_async_global();
-          __threadfence();
-          atomicAdd(&p.done[m.slot], 1);
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+          if (m.gu) {
+            // publish this gate/up tile to the down items of its group
+            fence_proxy_async_global();
+            __threadfence();
+            atomicAdd(&p.done[m.slot], 1);
+          }
+        }
+      } else {
+        mbar_arrive(&tempty[acc]);
+        if (m.gu) {
+          // publish this gate/up item to the down items of its group
+          named_bar_sync(kEpiBarAll, kEpiThreads);
+          if (threadIdx.x == 64) {
+            fence_proxy_async_global();
+            __threadfence();
+            atomicAdd(&p.done[m.slot], 1);
+          }
         }
       }
       acc ^= 1;
@@ -500,11 +659,18 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     }
   }
 
+  __syncwarp();
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // the leader's MMAs into the peer's TMEM and shared memory are complete
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, SM::kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, SM::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, SM::kTmemCols);
   }
 }
 
@@ -543,18 +709,40 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
 }
 
 // ----------------------------------------------------------------------------- host side
-template <int BN, int STAGES, int KCH>
+template <int BN, int STAGES, int KCH, bool PAIR>
 cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
                     const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E, int k,
                     int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws, const WsLayout& L,
                     const DeviceCtx& dc, cudaStream_t s, bool with_prep, bool early) {
-  using SM = Smem<BN, STAGES, KCH>;
+  using SM = Smem<BN, STAGES, KCH, PAIR>;
   static_assert(SM::kTotal <= 232448, "shared memory budget");
+  static_assert(!PAIR || ffn_fpi(BN) == 2, "CTA pairs take two feature tiles per item");
+  auto kernel = ffn_kernel<BN, STAGES, KCH, PAIR>;
   static int attr_done[64] = {0};
-  if (dc.device >= 0 && dc.device < 64 && !attr_done[dc.device]) {
-    cudaError_t e = cudaFuncSetAttribute(ffn_kernel<BN, STAGES, KCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SM::kTotal);
+  static int grid_for[64] = {0};  // PAIR: CTAs of the largest set of co-resident pairs
+  if (dc.device < 0 || dc.device >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dc.device]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
     if (e != cudaSuccess) return e;
+    grid_for[dc.device] = dc.num_sms;
+    if (PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * ((dc.num_sms + 1) / 2));
+      cfg.blockDim = dim3(kFfnThreads);
+      cfg.dynamicSmemBytes = SM::kTotal;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (clusters < 1) return cudaErrorInvalidConfiguration;
+      grid_for[dc.device] = 2 * min(clusters, (dc.num_sms + 1) / 2);
+    }
     attr_done[dc.device] = 1;
   }
   int32_t* table = reinterpret_cast<int32_t*>(ws + L.table);
@@ -573,14 +761,16 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
 
   FfnMaps maps;
   const int SI = S > 0 ? S * I : 64;
-  const bool ok = make_map(&maps.wgu, w_gate_up, (uint64_t)E * 2 * I, H, 64) &&
-                  make_map(&maps.wsgu, S > 0 ? ws_gate_up : w_gate_up, S > 0 ? (uint64_t)2 * S * I : 1, H, 64) &&
+  constexpr int BROWS = PAIR ? BN / 2 : BN;  // token rows one CTA stages per K chunk
+  const bool ok = make_map_gu(&maps.wgu, w_gate_up, (uint64_t)E * 2 * I, I, H) &&
+                  make_map_gu(&maps.wsgu, S > 0 ? ws_gate_up : w_gate_up, S > 0 ? (uint64_t)S * I : 1,
+                              S > 0 ? (uint64_t)S * I : 1, H) &&
                   make_map(&maps.wd, w_down, (uint64_t)E * H, I, 128) &&
                   make_map(&maps.wsd, S > 0 ? ws_down : w_down, S > 0 ? (uint64_t)H : 1, S > 0 ? SI : I, 128) &&
-                  make_map(&maps.xperm, xperm, nrows, H, BN) && make_map(&maps.x, x, T, H, BN) &&
-                  make_map(&maps.act, act, nrows, I, BN) &&
+                  make_map(&maps.xperm, xperm, nrows, H, BROWS) && make_map(&maps.x, x, T, H, BROWS) &&
+                  make_map(&maps.act, act, nrows, I, BROWS) &&
                   make_map(&maps.act_sh, S > 0 ? (const void*)act_sh : (const void*)act, S > 0 ? T : 1,
-                           S > 0 ? SI : I, BN);
+                           S > 0 ? SI : I, BROWS);
   if (!ok) return cudaErrorInvalidValue;
 
   FfnParams p;
@@ -589,7 +779,8 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.table = table;
   p.done = table + table_counters(G);
   p.counter = table + table_counters(G) + G;
-  p.n_static = (early && S > 0) ? ((T + BN - 1) / BN) * (S * I / 64) : 0;
+  constexpr int FPI = PAIR ? 2 : 1;
+  p.n_static = (early && S > 0) ? ((T + BN - 1) / BN) * ((S * I / 64 + FPI - 1) / FPI) : 0;
   p.act = act;
   p.act_sh = act_sh;
   p.y_perm = y_perm;
@@ -597,18 +788,39 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.y_bf16 = y_bf16 ? 1 : 0;
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();
-  return launch_pdl(ffn_kernel<BN, STAGES, KCH>, dim3(dc.num_sms), dim3(kFfnThreads), SM::kTotal, s, maps, p);
+  // With many short items (large token tiles) the counter's round trip at each item boundary
+  // would drain the ring; with few long ones, holding an index would lengthen the tail.
+  p.deal_ahead = BN >= LSV_FFN_DEAL_AHEAD_BN ? 1 : 0;
+  if (!PAIR) return launch_pdl(kernel, dim3(dc.num_sms), dim3(kFfnThreads), SM::kTotal, s, maps, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_for[dc.device]);
+  cfg.blockDim = dim3(kFfnThreads);
+  cfg.dynamicSmemBytes = SM::kTotal;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, maps, p);
 }
 
 }  // namespace
 
 // Token tile: the smallest of 32/64/128/256 that holds the mean rows per expert
 // with room for the spread of a multinomial draw.
+#ifndef LSV_FFN_MAX_BN
+#define LSV_FFN_MAX_BN 256
+#endif
 int ffn_token_tile(int T, int k, int E) {
   const double mean = E > 0 ? (double)T * k / E : 0.0;
   if (mean <= 20.0) return 32;
-  if (mean <= 44.0) return 64;
-  if (mean <= 96.0) return 128;
+  if (mean <= 44.0 || LSV_FFN_MAX_BN <= 64) return 64;
+  if (mean <= 96.0 || LSV_FFN_MAX_BN <= 128) return 128;
   return 256;
 }
 
@@ -618,17 +830,22 @@ cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offset
                        const WsLayout& L, const DeviceCtx& dc, cudaStream_t s, bool with_prep, bool early) {
   switch (ffn_token_tile(T, k, E)) {
     case 32:
-      return run_ffn<32, LSV_FFN_STAGES32, LSV_FFN_KCH32>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down,
-                                                          T, H, E, k, S, I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+      return run_ffn<32, LSV_FFN_STAGES32, LSV_FFN_KCH32, false>(x, perm, offsets, w_gate_up, w_down, ws_gate_up,
+                                                                 ws_down, T, H, E, k, S, I, y_perm, y_sh, y_bf16,
+                                                                 ws, L, dc, s, with_prep, early);
     case 64:
-      return run_ffn<64, 4, 2>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                               y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+      return run_ffn<64, 4, 2, false>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I,
+                                      y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
     case 128:
-      return run_ffn<128, 6, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                                y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+      return run_ffn<128, 6, 1, false>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I,
+                                       y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
     default:
-      return run_ffn<256, 4, 1>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I, y_perm,
-                                y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+      if constexpr (ffn_fpi(256) == 2)
+        return run_ffn<256, LSV_FFN_STAGES256P, LSV_FFN_KCH256P, true>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I,
+                                        y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+      else
+        return run_ffn<256, 4, 1, false>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S,
+                                         I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
   }
 }
 

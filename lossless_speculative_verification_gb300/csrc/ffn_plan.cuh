@@ -8,6 +8,14 @@
 
 namespace lsv {
 
+// Feature tiles per item.  With token tiles of 256 rows the expert kernel runs
+// as CTA pairs (one MMA stream over two SMs, M = 256): an item is then two
+// neighbouring feature tiles of one token tile, one per CTA of the pair.
+#ifndef LSV_FFN_PAIR
+#define LSV_FFN_PAIR 1
+#endif
+__host__ __device__ constexpr int ffn_fpi(int BN) { return (LSV_FFN_PAIR && BN >= 256) ? 2 : 1; }
+
 // Dealing order of the groups: the shared group (the largest items) first, then
 // the routed experts in index order.
 __host__ __device__ __forceinline__ int slot_group(int slot, int E, int S) {
@@ -15,16 +23,18 @@ __host__ __device__ __forceinline__ int slot_group(int slot, int E, int S) {
 }
 
 // Item table (layout in internal.h) from the expert offsets, for token tiles of
-// BN rows.  Executed by all 32 lanes of one warp.  zero_counters: also reset
-// the completion and dealing counters (otherwise the caller did, before the
-// routing began).  Offsets that do not describe
-// a partition of [0, T*k) schedule no item and raise LSV_ERR_DEVICE_INDEX.
+// BN rows and ffn_fpi(BN) feature tiles per item.  Executed by all 32 lanes of
+// one warp.  zero_counters: also reset the completion and dealing counters
+// (otherwise the caller did, before the routing began).  Offsets that do not
+// describe a partition of [0, T*k) schedule no item and raise
+// LSV_ERR_DEVICE_INDEX.
 __device__ __forceinline__ void build_item_table(const int32_t* offsets, int T, int H, int E, int k, int S, int I,
                                                  int BN, int32_t* table, int* err, bool zero_counters) {
   const int lane = threadIdx.x & 31;
   const int nrows = T * k;
   const int G = E + (S > 0 ? 1 : 0);
-  const int nft_dn = (H + 127) / 128;
+  const int fpi = ffn_fpi(BN);
+  const int nft_dn = ((H + 127) / 128 + fpi - 1) / fpi;
   constexpr int PER = (kMaxExperts + 1 + 31) / 32;  // 9 slots per lane covers G <= 257
   int gu_loc[PER], dn_loc[PER];
   int gu_sum = 0, dn_sum = 0;
@@ -36,10 +46,10 @@ __device__ __forceinline__ void build_item_table(const int32_t* offsets, int T, 
     if (g < E) {
       const int c = offsets[g + 1] - offsets[g];
       ntt = (c + BN - 1) / BN;
-      nft_gu = I / 64;
+      nft_gu = (I / 64 + fpi - 1) / fpi;
     } else if (g < G) {
       ntt = (T + BN - 1) / BN;
-      nft_gu = S * I / 64;
+      nft_gu = (S * I / 64 + fpi - 1) / fpi;
     }
     gu_loc[j] = ntt * nft_gu;
     dn_loc[j] = ntt * nft_dn;

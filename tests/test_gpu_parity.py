@@ -3,6 +3,8 @@ seeded inputs.  Integer results (routing, permutation, counts, greedy tokens,
 acceptance) must match bit for bit; floating-point layer outputs within
 rel-L2 <= 1e-2 and max-abs <= 2e-2 (bf16 tensor-core products against the
 fp64 oracle)."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -10,8 +12,8 @@ import torch
 import oracle
 from lossless_speculative_verification_gb300 import api, synth
 
-from gpu_util import (assert_layer_close, bf16_f64, dev_problem, from_dev_bf16, need_gpu, sample_rows,
-                      to_dev)
+from gpu_util import (DevProblem, assert_layer_close, bf16_f64, dev_problem, from_dev_bf16, need_gpu,
+                      sample_rows, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -107,6 +109,52 @@ def test_grouped_ffn_parity(name, nsample):
     toks = sample_rows(d.T, min(nsample, d.T), 2)
     ref_sh = oracle.shared_rows(prob.x, prob.ws_gate_up, prob.ws_down, d.S, toks)
     assert_layer_close(y_sh.cpu().numpy()[toks], ref_sh, "shared")
+
+
+# Token tiles of 256 rows run as CTA pairs, each item two feature tiles (one per CTA).  These shapes
+# give odd feature-tile counts (the second CTA of the last item has no tile of its own), a partial
+# last down tile (H % 128 == 64) and ragged token tiles, through the standalone and the fused paths.
+PAIR_SHAPES = [(1100, 1344, 16, 2, 1, 960), (1500, 1280, 8, 1, 2, 896), (2100, 1280, 64, 6, 2, 896)]
+
+
+@functools.lru_cache(maxsize=None)
+def pair_problem(T, H, E, k, S, I):
+    d = synth.MoeDims(T, H, E, k, S, I)
+    return DevProblem(synth.moe_problem(d, seed=5, row_ok=oracle.gap_ok(k)))
+
+
+@pytest.mark.parametrize("T,H,E,k,S,I", PAIR_SHAPES)
+def test_grouped_ffn_pairs(T, H, E, k, S, I):
+    P = pair_problem(T, H, E, k, S, I)
+    d, prob = P.d, P.prob
+    r = P.oracle_route()
+    dev = lambda a: torch.from_numpy(a).cuda()
+    y_perm, y_sh = api.moe_grouped_ffn(P.x, dev(r["perm"]), dev(r["offsets"]), dev(r["counts"]), P.wts, P.sh, P.ws)
+    torch.cuda.synchronize()
+    rows = sample_rows(d.T * d.k, 128, 11)
+    for e in (int(np.argmin(r["counts"])), int(np.argmax(r["counts"]))):
+        rows = np.union1d(rows, np.arange(r["offsets"][e], r["offsets"][e + 1])[-40:])
+    expert = np.searchsorted(r["offsets"], rows, side="right") - 1
+    token = r["perm"][rows] // d.k
+    ref = oracle.expert_rows(prob.x, prob.w_gate_up, prob.w_down, token, expert)
+    assert_layer_close(y_perm.cpu().numpy()[rows], ref, "routed")
+    toks = sample_rows(d.T, 96, 12)
+    ref_sh = oracle.shared_rows(prob.x, prob.ws_gate_up, prob.ws_down, d.S, toks)
+    assert_layer_close(y_sh.cpu().numpy()[toks], ref_sh, "shared")
+
+
+@pytest.mark.parametrize("T,H,E,k,S,I", PAIR_SHAPES)
+def test_layer_pairs(T, H, E, k, S, I):
+    P = pair_problem(T, H, E, k, S, I)
+    d, prob = P.d, P.prob
+    idx = torch.empty((d.T, d.k), dtype=torch.int32, device="cuda")
+    out = api.moe_verify_layer(P.x, P.wts, P.sh, P.ws, topk_idx=idx)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), P.oracle_route()["idx"])
+    toks = sample_rows(d.T, 96, 13)
+    ref, _, _ = oracle.moe_layer(prob.x, prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up,
+                                 prob.ws_down, d.k, d.S, tokens=toks)
+    assert_layer_close(bf16_f64(from_dev_bf16(out))[toks], ref, "pairs")
 
 
 # ----------------------------------------------------------------------------- combine
