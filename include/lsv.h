@@ -133,6 +133,10 @@ lsv_status moe_combine(const float *y_perm, const int32_t *inv, const float *top
 /* The whole MoE layer: route, permute, grouped experts, combine.
  *   x   [T, H] bf16 in;  out [T, H] bf16 out
  *   topk_idx_opt [T, k] int32 and counts_opt [E] int32: optional copies of the routing.
+ * The expert outputs are kept in bf16 between the experts and the combine.
+ * Up to 256 tokens the router itself places each routed row (one launch less);
+ * the order of rows inside an expert is then decided by atomics, which no
+ * output depends on: out is bit-identical from run to run.
  * ws: lsv_workspace_size(shape). */
 lsv_status moe_verify_layer(const void *x, const lsv_moe_weights *weights, const lsv_moe_shape *shape, void *out,
                             int32_t *topk_idx_opt, int32_t *counts_opt, void *ws, size_t ws_bytes,

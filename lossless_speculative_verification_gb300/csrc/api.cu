@@ -85,11 +85,12 @@ WsLayout ws_layout(int T, int H, int E, int k, int S, int I) {
   L.perm = take(n * 4);
   L.inv = take(n * 4);
   L.blk_counts = take((size_t)L.nblk * E * 4);
-  L.table = take((size_t)table_ints(G) * 4);
-  L.xperm = take(n * H * 2);
-  L.act = take(n * I * 2);
+  L.table = take((size_t)table_ints(G, E) * 4);
+  const size_t rows = routed_rows(T, k, E);
+  L.xperm = take(rows * H * 2);
+  L.act = take(rows * I * 2);
   L.act_sh = take((size_t)T * S * I * 2);
-  L.y_perm = take(n * H * 4);
+  L.y_perm = take(rows * H * 4);
   L.y_sh = take((size_t)T * H * 4);
   L.total = align256(o);
   return L;
@@ -261,8 +262,9 @@ lsv_status moe_grouped_ffn(const void* x, const int32_t* perm_src, const int32_t
   // with no routed pairs the routed weights are never read; any valid pointer serves their tensor maps
   const void* wgu = wt->w_gate_up ? wt->w_gate_up : wt->ws_gate_up;
   const void* wd = wt->w_down ? wt->w_down : wt->ws_down;
-  return from_cuda(launch_ffn(static_cast<const bf16*>(x), perm_src, offsets, static_cast<const bf16*>(wgu),
-                              static_cast<const bf16*>(wd), static_cast<const bf16*>(wt->ws_gate_up),
+  return from_cuda(launch_ffn(static_cast<const bf16*>(x), perm_src, offsets, nullptr, 0,
+                              static_cast<const bf16*>(wgu), static_cast<const bf16*>(wd),
+                              static_cast<const bf16*>(wt->ws_gate_up),
                               static_cast<const bf16*>(wt->ws_down), shape->T, shape->H, shape->E, shape->k,
                               shape->S, shape->I, y_perm, y_shared, /*y_bf16=*/false, static_cast<uint8_t*>(ws), L,
                               *dc, reinterpret_cast<cudaStream_t>(stream)));
@@ -280,7 +282,7 @@ lsv_status moe_combine(const float* y_perm, const int32_t* inv, const float* top
   DeviceCtx* dc = nullptr;
   if (device_ctx(&dc) != cudaSuccess) return LSV_ERR_CUDA;
   return from_cuda(launch_combine(y_perm, inv, topk_w, shape->S > 0 ? y_shared : nullptr, /*y_bf16=*/false,
-                                  shape->T, shape->H, shape->k, static_cast<bf16*>(out), dc->err,
+                                  shape->T, shape->H, shape->k, shape->T * shape->k, static_cast<bf16*>(out), dc->err,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -318,31 +320,52 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   const bf16* wdn = static_cast<const bf16*>(wt->w_down);
   const bf16* wsgu = static_cast<const bf16*>(wt->ws_gate_up);
   const bf16* wsdn = static_cast<const bf16*>(wt->ws_down);
-  // zero the grouped-expert kernel's counters before anything else of this layer runs,
-  // so that it can begin the routing-independent shared-expert items early
+  // zero the grouped-expert kernel's counters (and the router's slot counters) before anything
+  // else of this layer runs, so that it can begin the routing-independent shared-expert items early
   const int G = E + (S > 0 ? 1 : 0);
-  cudaError_t e = cudaMemsetAsync(w + L.table + (size_t)table_counters(G) * 4, 0, (size_t)(G + 1) * 4, s);
+  int32_t* table = reinterpret_cast<int32_t*>(w + L.table);
+  cudaError_t e = cudaMemsetAsync(table + table_counters(G), 0, (size_t)table_zeroed_ints(G, E) * 4, s);
   const uint64_t pf = default_prefetch_bytes(*dc, T, E, k, S, I, H);
   if (e == cudaSuccess && pf) e = launch_weight_prefetch(wgu, wdn, wsgu, wsdn, H, E, S, I, pf, *dc, s);
-  if (e == cudaSuccess)
-    e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,
-                     nullptr, s);
-  const bool fused = (long long)T * k <= kPermFusedMax;  // permutation, gather and plan in one launch
-  if (e == cudaSuccess) {
-    if (fused)
-      e = launch_permute_gather(idx, T, k, E, H, S, I, ffn_token_tile(T, k, E), static_cast<const bf16*>(x), counts,
-                                offsets, perm, inv, reinterpret_cast<bf16*>(w + L.xperm),
-                                reinterpret_cast<int32_t*>(w + L.table), dc->err, s);
-    else
-      e = launch_permute(idx, T, k, E, counts, offsets, perm, inv, reinterpret_cast<int32_t*>(w + L.blk_counts),
-                         L.nblk, dc->err, s);
+  const int BN = ffn_token_tile(T, k, E);
+  if (use_slots(T)) {
+    // the router places the rows and builds the item table: no permutation launch
+    RouteSlots sl;
+    sl.xperm = reinterpret_cast<bf16*>(w + L.xperm);
+    sl.inv = inv;
+    sl.table = table;
+    sl.counts = counts_opt;
+    sl.S = S;
+    sl.I = I;
+    sl.BN = BN;
+    sl.err = dc->err;
+    if (e == cudaSuccess)
+      e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,
+                       nullptr, s, &sl);
+    if (e == cudaSuccess)
+      e = launch_ffn(static_cast<const bf16*>(x), nullptr, nullptr, table + table_slots(G), T, wgu, wdn, wsgu, wsdn,
+                     T, H, E, k, S, I, y_perm, y_sh, /*y_bf16=*/true, w, L, *dc, s, /*with_prep=*/false,
+                     /*early=*/true);
+  } else {
+    if (e == cudaSuccess)
+      e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,
+                       nullptr, s);
+    const bool fused = (long long)T * k <= kPermFusedMax;  // permutation, gather and plan in one launch
+    if (e == cudaSuccess) {
+      if (fused)
+        e = launch_permute_gather(idx, T, k, E, H, S, I, BN, static_cast<const bf16*>(x), counts, offsets, perm,
+                                  inv, reinterpret_cast<bf16*>(w + L.xperm), table, dc->err, s);
+      else
+        e = launch_permute(idx, T, k, E, counts, offsets, perm, inv, reinterpret_cast<int32_t*>(w + L.blk_counts),
+                           L.nblk, dc->err, s);
+    }
+    if (e == cudaSuccess)
+      e = launch_ffn(static_cast<const bf16*>(x), perm, offsets, nullptr, 0, wgu, wdn, wsgu, wsdn, T, H, E, k, S, I,
+                     y_perm, y_sh, /*y_bf16=*/true, w, L, *dc, s, /*with_prep=*/!fused, /*early=*/true);
   }
   if (e == cudaSuccess)
-    e = launch_ffn(static_cast<const bf16*>(x), perm, offsets, wgu, wdn, wsgu, wsdn, T, H, E, k, S, I, y_perm, y_sh,
-                   /*y_bf16=*/true, w, L, *dc, s, /*with_prep=*/!fused, /*early=*/true);
-  if (e == cudaSuccess)
-    e = launch_combine(y_perm, inv, tw, S > 0 ? y_sh : nullptr, /*y_bf16=*/true, T, H, k, static_cast<bf16*>(out),
-                       dc->err, s);
+    e = launch_combine(y_perm, inv, tw, S > 0 ? y_sh : nullptr, /*y_bf16=*/true, T, H, k,
+                       use_slots(T) ? E * T : T * k, static_cast<bf16*>(out), dc->err, s);
   return from_cuda(e);
 }
 

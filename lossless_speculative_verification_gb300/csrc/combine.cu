@@ -51,7 +51,8 @@ struct Piece<float> {
 template <typename YT>
 __global__ void __launch_bounds__(256) combine_kernel(const YT* __restrict__ y_perm, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ topk_w, const YT* __restrict__ y_sh,
-                                                      int T, int H, int k, bf16* __restrict__ out, int* err) {
+                                                      int T, int H, int k, int rows_y, bf16* __restrict__ out,
+                                                      int* err) {
   const int t = blockIdx.x;
   __shared__ int rows[kMaxTopK];
   __shared__ float wts[kMaxTopK];
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const YT* __restrict__ y_p
   pdl_trigger();
   if (threadIdx.x < k) {
     int r = inv[(size_t)t * k + threadIdx.x];
-    if (r < 0 || r >= T * k) {  // never read outside y_perm
+    if (r < 0 || r >= rows_y) {  // never read outside y_perm
       set_error(err, kErrDeviceIndex);
       r = -1;
     }
@@ -126,15 +127,15 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_residual_kernel(bf16* __
 }  // namespace
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_sh,
-                           bool y_bf16, int T, int H, int k, bf16* out, int* err, cudaStream_t s) {
+                           bool y_bf16, int T, int H, int k, int rows_y, bf16* out, int* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   int threads = ((H / 8 + 31) / 32) * 32;
   if (threads > 256) threads = 256;
   if (y_bf16)
     return launch_pdl(combine_kernel<bf16>, dim3(T), dim3(threads), 0, s, static_cast<const bf16*>(y_perm), inv,
-                      topk_w, static_cast<const bf16*>(y_sh), T, H, k, out, err);
+                      topk_w, static_cast<const bf16*>(y_sh), T, H, k, rows_y, out, err);
   return launch_pdl(combine_kernel<float>, dim3(T), dim3(threads), 0, s, static_cast<const float*>(y_perm), inv,
-                    topk_w, static_cast<const float*>(y_sh), T, H, k, out, err);
+                    topk_w, static_cast<const float*>(y_sh), T, H, k, rows_y, out, err);
 }
 
 cudaError_t launch_rmsnorm_residual(bf16* x, const bf16* y, bf16* h, int T, int H, float eps, cudaStream_t s) {

@@ -72,7 +72,10 @@ constexpr int kEpiBarAll = 1;            // named barrier over all epilogue warp
 
 struct FfnParams {
   int T, H, E, k, S, I, G;
-  const int32_t* offsets;  // [E+1]
+  const int32_t* offsets;  // [E+1] (compact row space)
+  const int32_t* seg_counts;  // [E] rows per expert (slot placement), with
+  int seg_cap;                // rows reserved per expert (0: compact row space, offsets)
+  int rows_routed;            // rows of the routed row space
   const int32_t* table;    // tile table (see internal.h)
   int* done;               // [G]
   bf16* act;               // [T*k, I]
@@ -110,11 +113,12 @@ struct Item {
   int need;  // completions a down item of group g waits for (one per gate/up feature tile)
 };
 
-// Shared-memory copy of the item table's starts and the expert offsets, so that
-// decoding an item costs no global-memory round trips:
+// Shared-memory copy of the item table's starts and each expert's rows, so
+// that decoding an item costs no global-memory round trips:
 //   [0] gate/up items, [1] all items, [2, 2+G] gate/up starts per slot,
-//   [3+G, 3+2G] down starts per slot, [4+2G, 4+2G+E] expert offsets.
-constexpr int kTabInts = 2 + 2 * (kMaxExperts + 2) + kMaxExperts + 1;
+//   [3+G, 3+2G] down starts per slot, [4+2G, 4+2G+E) first row per expert,
+//   [4+2G+E, 4+2G+2E) rows per expert.
+constexpr int kTabInts = 2 + 2 * (kMaxExperts + 2) + 2 * kMaxExperts;
 constexpr int kDealFailed = -2;  // the mailbox wait ran out
 
 // Item `it` of the dealing order.  FPI feature tiles per item (2 for CTA pairs:
@@ -140,7 +144,8 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p, const in
   }
   const int G = p.G;
   const int n_gu = tab[0];
-  const int* offsets = tab + 4 + 2 * G;
+  const int* seg_first = tab + 4 + 2 * G;
+  const int* seg_rows = seg_first + p.E;
   Item m;
   m.gu = it < n_gu;
   const int* starts = m.gu ? tab + 2 : tab + 3 + G;
@@ -161,8 +166,8 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p, const in
   m.ft = (local - tt * nit) * FPI;
   int seg0, segn;
   if (routed) {
-    seg0 = offsets[m.g];
-    segn = offsets[m.g + 1] - seg0;
+    seg0 = seg_first[m.g];
+    segn = seg_rows[m.g];
   } else {
     seg0 = 0;
     segn = p.T;
@@ -306,7 +311,11 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
               tab[2 + i] = p.table[8 + i];
               tab[3 + G + i] = p.table[8 + G + 1 + i];
             }
-            for (int i = 0; i <= p.E; ++i) tab[4 + 2 * G + i] = p.offsets[i];
+            for (int e = 0; e < p.E; ++e) {
+              const bool slots = p.seg_cap > 0;
+              tab[4 + 2 * G + e] = slots ? e * p.seg_cap : p.offsets[e];
+              tab[4 + 2 * G + p.E + e] = slots ? p.seg_counts[e] : p.offsets[e + 1] - p.offsets[e];
+            }
             have_tab = true;
           }
           if (it >= tab[1]) it = -1;
@@ -582,7 +591,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       if (named_bar_red_or(kEpiBarAll, kEpiThreads, !got || *abort_flag)) break;
       tc_fence_after_sync();
       const bool routed = m.g < p.E;
-      const int nrows_out = routed ? p.T * p.k : p.T;
+      const int nrows_out = routed ? p.rows_routed : p.T;
       const int n_mma = max(16, (m.cnt + 15) & ~15);
       const int ft = m.ft + (int)rank;
       const bool own = ft < m.nft;  // false: the duplicate tile of an odd count (PAIR)
@@ -705,12 +714,13 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
       }
     }
   }
-  if (blockIdx.x == 0 && threadIdx.x < 32) build_item_table(offsets, T, H, E, k, S, I, BN, table, err, zero_counters);
+  if (blockIdx.x == 0 && threadIdx.x < 32) build_item_table(offsets, nullptr, T, H, E, k, S, I, BN, table, err, zero_counters);
 }
 
 // ----------------------------------------------------------------------------- host side
 template <int BN, int STAGES, int KCH, bool PAIR>
-cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
+cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const int32_t* seg_counts,
+                    int seg_cap, const bf16* w_gate_up,
                     const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E, int k,
                     int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws, const WsLayout& L,
                     const DeviceCtx& dc, cudaStream_t s, bool with_prep, bool early) {
@@ -751,6 +761,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   bf16* act_sh = reinterpret_cast<bf16*>(ws + L.act_sh);
   const int G = E + (S > 0 ? 1 : 0);
   const int nrows = T * k;
+  const int rows_routed = seg_cap > 0 ? E * seg_cap : nrows;
 
   if (with_prep) {
     const int prep_blocks = max(1, (nrows + 7) / 8);
@@ -767,8 +778,8 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
                               S > 0 ? (uint64_t)S * I : 1, H) &&
                   make_map(&maps.wd, w_down, (uint64_t)E * H, I, 128) &&
                   make_map(&maps.wsd, S > 0 ? ws_down : w_down, S > 0 ? (uint64_t)H : 1, S > 0 ? SI : I, 128) &&
-                  make_map(&maps.xperm, xperm, nrows, H, BROWS) && make_map(&maps.x, x, T, H, BROWS) &&
-                  make_map(&maps.act, act, nrows, I, BROWS) &&
+                  make_map(&maps.xperm, xperm, rows_routed, H, BROWS) && make_map(&maps.x, x, T, H, BROWS) &&
+                  make_map(&maps.act, act, rows_routed, I, BROWS) &&
                   make_map(&maps.act_sh, S > 0 ? (const void*)act_sh : (const void*)act, S > 0 ? T : 1,
                            S > 0 ? SI : I, BROWS);
   if (!ok) return cudaErrorInvalidValue;
@@ -776,6 +787,9 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   FfnParams p;
   p.T = T; p.H = H; p.E = E; p.k = k; p.S = S; p.I = I; p.G = G;
   p.offsets = offsets;
+  p.seg_counts = seg_counts;
+  p.seg_cap = seg_cap;
+  p.rows_routed = rows_routed;
   p.table = table;
   p.done = table + table_counters(G);
   p.counter = table + table_counters(G) + G;
@@ -824,29 +838,28 @@ int ffn_token_tile(int T, int k, int E) {
   return 256;
 }
 
-cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const bf16* w_gate_up,
-                       const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E,
-                       int k, int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws,
-                       const WsLayout& L, const DeviceCtx& dc, cudaStream_t s, bool with_prep, bool early) {
+cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const int32_t* seg_counts,
+                       int seg_cap, const bf16* w_gate_up, const bf16* w_down, const bf16* ws_gate_up,
+                       const bf16* ws_down, int T, int H, int E, int k, int S, int I, void* y_perm, void* y_sh,
+                       bool y_bf16, uint8_t* ws, const WsLayout& L, const DeviceCtx& dc, cudaStream_t s,
+                       bool with_prep, bool early) {
+#define LSV_RUN_FFN(BN_, ST_, KCH_, PAIR_)                                                                     \
+  run_ffn<BN_, ST_, KCH_, PAIR_>(x, perm, offsets, seg_counts, seg_cap, w_gate_up, w_down, ws_gate_up, ws_down, \
+                                 T, H, E, k, S, I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early)
   switch (ffn_token_tile(T, k, E)) {
     case 32:
-      return run_ffn<32, LSV_FFN_STAGES32, LSV_FFN_KCH32, false>(x, perm, offsets, w_gate_up, w_down, ws_gate_up,
-                                                                 ws_down, T, H, E, k, S, I, y_perm, y_sh, y_bf16,
-                                                                 ws, L, dc, s, with_prep, early);
+      return LSV_RUN_FFN(32, LSV_FFN_STAGES32, LSV_FFN_KCH32, false);
     case 64:
-      return run_ffn<64, 4, 2, false>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I,
-                                      y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+      return LSV_RUN_FFN(64, 4, 2, false);
     case 128:
-      return run_ffn<128, 6, 1, false>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I,
-                                       y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+      return LSV_RUN_FFN(128, 6, 1, false);
     default:
       if constexpr (ffn_fpi(256) == 2)
-        return run_ffn<256, LSV_FFN_STAGES256P, LSV_FFN_KCH256P, true>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S, I,
-                                        y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+        return LSV_RUN_FFN(256, LSV_FFN_STAGES256P, LSV_FFN_KCH256P, true);
       else
-        return run_ffn<256, 4, 1, false>(x, perm, offsets, w_gate_up, w_down, ws_gate_up, ws_down, T, H, E, k, S,
-                                         I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early);
+        return LSV_RUN_FFN(256, 4, 1, false);
   }
+#undef LSV_RUN_FFN
 }
 
 }  // namespace lsv

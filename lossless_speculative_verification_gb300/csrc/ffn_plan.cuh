@@ -22,14 +22,17 @@ __host__ __device__ __forceinline__ int slot_group(int slot, int E, int S) {
   return S > 0 ? (slot == 0 ? E : slot - 1) : slot;
 }
 
-// Item table (layout in internal.h) from the expert offsets, for token tiles of
-// BN rows and ffn_fpi(BN) feature tiles per item.  Executed by all 32 lanes of
-// one warp.  zero_counters: also reset the completion and dealing counters
-// (otherwise the caller did, before the routing began).  Offsets that do not
-// describe a partition of [0, T*k) schedule no item and raise
+// Item table (layout in internal.h), for token tiles of BN rows and
+// ffn_fpi(BN) feature tiles per item.  Rows per expert come from the expert
+// offsets (compact row space: offsets must partition [0, T*k)) or, when
+// `counts` is given, from per-expert row counts of at most T (slot placement).
+// Executed by all 32 lanes of one warp.  zero_counters: also reset the
+// completion and dealing counters (otherwise the caller did, before the
+// routing began).  Inconsistent offsets or counts schedule no item and raise
 // LSV_ERR_DEVICE_INDEX.
-__device__ __forceinline__ void build_item_table(const int32_t* offsets, int T, int H, int E, int k, int S, int I,
-                                                 int BN, int32_t* table, int* err, bool zero_counters) {
+__device__ __forceinline__ void build_item_table(const int32_t* offsets, const int32_t* counts, int T, int H, int E,
+                                                 int k, int S, int I, int BN, int32_t* table, int* err,
+                                                 bool zero_counters) {
   const int lane = threadIdx.x & 31;
   const int nrows = T * k;
   const int G = E + (S > 0 ? 1 : 0);
@@ -44,8 +47,8 @@ __device__ __forceinline__ void build_item_table(const int32_t* offsets, int T, 
     const int g = slot < G ? slot_group(slot, E, S) : G;
     int ntt = 0, nft_gu = 0;
     if (g < E) {
-      const int c = offsets[g + 1] - offsets[g];
-      ntt = (c + BN - 1) / BN;
+      const int c = counts ? counts[g] : offsets[g + 1] - offsets[g];
+      ntt = c > 0 ? (c + BN - 1) / BN : 0;
       nft_gu = (I / 64 + fpi - 1) / fpi;
     } else if (g < G) {
       ntt = (T + BN - 1) / BN;
@@ -60,9 +63,9 @@ __device__ __forceinline__ void build_item_table(const int32_t* offsets, int T, 
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int g = lane * PER + j;
-    if (g < E && (offsets[g] > offsets[g + 1])) bad = 1;
+    if (g < E && (counts ? (counts[g] < 0 || counts[g] > T) : offsets[g] > offsets[g + 1])) bad = 1;
   }
-  if (lane == 0 && (offsets[0] != 0 || offsets[E] != nrows)) bad = 1;
+  if (!counts && lane == 0 && (offsets[0] != 0 || offsets[E] != nrows)) bad = 1;
   bad = __any_sync(0xffffffffu, bad);
   if (bad) {
     gu_sum = dn_sum = 0;

@@ -15,6 +15,7 @@
 // fp32 rounding (far below the router gaps the selection depends on).  The
 // E logits of each token then go through shared memory to one warp per token
 // for the softmax and the k selection rounds.
+#include "ffn_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -40,14 +41,18 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
                                                                  const bf16* __restrict__ wr, int T, int H,
                                                                  int E, int k, int32_t* __restrict__ idx,
                                                                  float* __restrict__ w,
-                                                                 float* __restrict__ logits) {
+                                                                 float* __restrict__ logits, const RouteSlots sl) {
   __shared__ float lg[TT][kMaxExperts];
+  __shared__ int sel_row[kMaxTopK];
+  __shared__ int s_cnt[kMaxExperts + 1];
+  __shared__ int is_last;
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * TT;
   const int nt = min(TT, T - t0);
   const int n8 = H / 8;  // 16-byte groups per row
+  const bool slots = TT == 1 && sl.xperm != nullptr;
 
   // warp w owns experts [4w, 4w+4), [4w+64, 4w+68), ...: four independent rows in flight per step
   for (int e0 = warp * kExpPerWarp; e0 < E; e0 += kRouteWarps * kExpPerWarp) {
@@ -90,7 +95,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
   }
   __syncthreads();
 
-  // softmax + top-k: one warp per token
+  // softmax + top-k: one warp per token.  The selection is by rank: an expert's
+  // rank is the number of experts with a larger logit, or an equal logit and a
+  // lower index, so ranks are distinct and ties go to the lower index.
   for (int i = warp; i < nt; i += kRouteWarps) {
     const int t = t0 + i;
     float m = -INFINITY;
@@ -103,33 +110,51 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
     if (logits)
       for (int e = lane; e < E; e += 32) logits[(size_t)t * E + e] = lg[i][e];
-    uint32_t taken = 0;  // bit j: expert lane + 32 j already selected
-    for (int s = 0; s < k; ++s) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-      for (int j = 0, e = lane; e < E; ++j, e += 32) {
-        const float v = lg[i][e];
-        if (!(taken & (1u << j)) && (v > bv || (v == bv && e < be))) {
-          bv = v;
-          be = e;
-        }
+    for (int e = lane; e < E; e += 32) {
+      const float v = lg[i][e];
+      int r = 0;
+      for (int e2 = 0; e2 < E; ++e2) {
+        const float v2 = lg[i][e2];
+        r += (v2 > v || (v2 == v && e2 < e)) ? 1 : 0;
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
+      if (r < k) {
+        idx[(size_t)t * k + r] = e;
+        w[(size_t)t * k + r] = expf(v - m) / z;
+        if (slots) {
+          // the next free row of expert e's region
+          const int row = e * T + atomicAdd(&sl.table[table_slots(E + (sl.S > 0 ? 1 : 0)) + e], 1);
+          sl.inv[(size_t)t * k + r] = row;
+          sel_row[r] = row;
         }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == 0) {
-        idx[(size_t)t * k + s] = be;
-        w[(size_t)t * k + s] = expf(bv - m) / z;
       }
     }
   }
+  if (!slots) return;
+
+  // The last CTA to take its rows sees every expert's final row count and builds the item
+  // table, while the other CTAs place their token's row at its k rows of the routed row space.
+  __syncthreads();
+  const int G = E + (sl.S > 0 ? 1 : 0);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    is_last = atomicAdd(&sl.table[table_arrive(G)], 1) == (int)gridDim.x - 1;
+  }
+  if (warp < k) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t0 * H);
+    uint4* dst = reinterpret_cast<uint4*>(sl.xperm + (size_t)sel_row[warp] * H);
+    for (int c = lane; c < n8; c += 32) dst[c] = __ldg(src + c);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = __ldcg(&sl.table[table_slots(G) + e]);
+    s_cnt[e] = c;
+    if (sl.counts) sl.counts[e] = c;
+  }
+  __syncthreads();
+  if (warp == 0)
+    build_item_table(nullptr, s_cnt, T, H, E, k, sl.S, sl.I, sl.BN, sl.table, sl.err, /*zero_counters=*/false);
 }
 
 // ----------------------------------------------------------------------------- tensor-core router
@@ -322,9 +347,13 @@ cudaError_t run_route_tc(const bf16* x, const bf16* wr, int T, int H, int E, int
 }  // namespace
 
 cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int k, int32_t* idx, float* w,
-                         float* logits, cudaStream_t s) {
+                         float* logits, cudaStream_t s, const RouteSlots* slots) {
+  RouteSlots sl = {};
+  if (slots) sl = *slots;
   if (T == 0) return cudaSuccess;
+  static_assert(kSlotMaxTokens == kRouteTcMinTokens, "slot placement needs the one-token-per-CTA router");
   if (T > kRouteTcMinTokens) {
+    if (slots) return cudaErrorInvalidValue;
     DeviceCtx* dc = nullptr;
     const cudaError_t e = device_ctx(&dc);
     if (e != cudaSuccess) return e;
@@ -334,10 +363,11 @@ cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int
   }
   const dim3 block(kRouteWarps * 32);
   // about one CTA per SM at decode sizes; more tokens per CTA once T is large
-  if (T <= 256) return launch_pdl(route_kernel<1>, dim3(T), block, 0, s, x, wr, T, H, E, k, idx, w, logits);
+  if (T <= 256) return launch_pdl(route_kernel<1>, dim3(T), block, 0, s, x, wr, T, H, E, k, idx, w, logits, sl);
+  if (slots) return cudaErrorInvalidValue;  // slot placement is for the one-token-per-CTA router only
   if (T <= 1024)
-    return launch_pdl(route_kernel<4>, dim3((T + 3) / 4), block, 0, s, x, wr, T, H, E, k, idx, w, logits);
-  return launch_pdl(route_kernel<8>, dim3((T + 7) / 8), block, 0, s, x, wr, T, H, E, k, idx, w, logits);
+    return launch_pdl(route_kernel<4>, dim3((T + 3) / 4), block, 0, s, x, wr, T, H, E, k, idx, w, logits, sl);
+  return launch_pdl(route_kernel<8>, dim3((T + 7) / 8), block, 0, s, x, wr, T, H, E, k, idx, w, logits, sl);
 }
 
 }  // namespace lsv
