@@ -54,6 +54,11 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed oracle sample (for profiler runs; the line then has no cpu_baseline)")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="no benchmark: read an ncu CSV of this workload's run (metrics dram__bytes_read.sum, "
+                         "dram__bytes_write.sum, gpu__time_duration.sum) and write profiles/layer_<workload>"
+                         "_traffic.json, the DRAM bytes of one layer that the roofline's `traffic` reports")
+    ap.add_argument("--ncu-command", default="", help="with --record-traffic: the command that made the CSV")
     return ap.parse_args()
 
 
@@ -155,6 +160,56 @@ def ncu_traffic(workload, kernel_hash):
     if d.get("kernel_source_hash") != kernel_hash:
         return None
     return d.get("dram_bytes_per_layer")
+
+
+def record_traffic(args):
+    """Sum DRAM bytes over each layer's launches (a layer: from a router launch to the next combine)
+    in an ncu CSV, and store the mean per layer beside the source hash it was taken on."""
+    import csv
+    launches = {}
+    with open(args.record_traffic, newline="") as f:
+        hdr = None
+        for row in csv.reader(f):
+            if row and row[0] == "ID":
+                hdr = row
+                continue
+            if not hdr or len(row) != len(hdr):
+                continue
+            r = dict(zip(hdr, row))
+            e = launches.setdefault(int(r["ID"]), {"name": r["Kernel Name"].split("(")[0].split("::")[-1].strip()})
+            scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1, "usecond": 1e3,
+                     "msecond": 1e6, "ns": 1, "us": 1e3, "ms": 1e6}.get(r["Metric Unit"], 1)
+            try:
+                e[r["Metric Name"]] = float(r["Metric Value"].replace(",", "")) * scale
+            except ValueError:
+                pass
+    layers, cur = [], None
+    for i in sorted(launches):
+        e = launches[i]
+        base = e["name"].split("<")[0]
+        if base.startswith("route"):
+            cur = []
+        if cur is None:
+            continue
+        cur.append(e)
+        if base == "combine_kernel":
+            layers.append(cur)
+            cur = None
+    if not layers:
+        raise SystemExit("no complete layer (router ... combine) in %s" % args.record_traffic)
+    per_layer = [sum(e.get("dram__bytes_read.sum", 0) + e.get("dram__bytes_write.sum", 0) for e in L) for L in layers]
+    last = {e["name"]: {"read": int(e.get("dram__bytes_read.sum", 0)), "write": int(e.get("dram__bytes_write.sum", 0)),
+                        "ns": int(e.get("gpu__time_duration.sum", 0))} for e in layers[-1]}
+    out = {"workload": args.workload, "command": args.ncu_command,
+           "note": "sum of DRAM read+write bytes over one layer's launches, mean over the %d layers in the "
+                   "capture; the writes include write-backs of the benchmark's own L2-flush buffer" % len(layers),
+           "kernel_source_hash": layer_source_hash(), "dram_bytes_per_layer": int(sum(per_layer) / len(per_layer)),
+           "per_kernel_last_layer": last}
+    path = os.path.join(ROOT, "profiles", "layer_%s_traffic.json" % args.workload)
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+    print(json.dumps(out))
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -567,6 +622,9 @@ def run_ours(args, rank, world, local):
 
 def main():
     args = parse()
+    if args.record_traffic:
+        record_traffic(args)
+        return
     rank, world, local = dist_env()
     if args.warmup < 0 or args.steps <= 0:
         raise SystemExit("steps must be positive")

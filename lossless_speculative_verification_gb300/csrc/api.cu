@@ -329,23 +329,18 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   if (e == cudaSuccess && pf) e = launch_weight_prefetch(wgu, wdn, wsgu, wsdn, H, E, S, I, pf, *dc, s);
   const int BN = ffn_token_tile(T, k, E);
   if (use_slots(T)) {
-    // the router places the rows and builds the item table: no permutation launch
+    // the router places the rows, the expert kernel builds its item table: no permutation launch
     RouteSlots sl;
     sl.xperm = reinterpret_cast<bf16*>(w + L.xperm);
     sl.inv = inv;
-    sl.table = table;
-    sl.counts = counts_opt;
-    sl.S = S;
-    sl.I = I;
-    sl.BN = BN;
-    sl.err = dc->err;
+    sl.slots = table + table_slots(G);
     if (e == cudaSuccess)
       e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,
                        nullptr, s, &sl);
     if (e == cudaSuccess)
       e = launch_ffn(static_cast<const bf16*>(x), nullptr, nullptr, table + table_slots(G), T, wgu, wdn, wsgu, wsdn,
                      T, H, E, k, S, I, y_perm, y_sh, /*y_bf16=*/true, w, L, *dc, s, /*with_prep=*/false,
-                     /*early=*/true);
+                     /*early=*/true, counts_opt);
   } else {
     if (e == cudaSuccess)
       e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,

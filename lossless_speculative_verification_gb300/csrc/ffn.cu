@@ -24,7 +24,8 @@
 //     A = W_down rows h0..h0+127, B = act rows;  y[row, h] = D (fp32)
 //
 // One persistent CTA per SM, warp-specialised: warp 0 issues TMA, warp 1
-// allocates TMEM and issues tcgen05.mma (one thread), warps 2-9 drain TMEM.
+// allocates TMEM and issues tcgen05.mma (one thread), warps 2-9 drain TMEM,
+// warp 10 builds the shared-memory item table once the routing is known.
 // A STAGES-deep shared-memory ring (KCH K-chunks per stage, so that the
 // neighbouring 128-byte pieces of each weight row are requested together)
 // decouples loads from MMAs, and two TMEM accumulators decouple MMAs from the
@@ -43,8 +44,9 @@
 namespace lsv {
 namespace {
 
-constexpr int kFfnThreads = 320;         // 10 warps
+constexpr int kFfnThreads = 352;         // 11 warps
 constexpr int kEpiWarps = 8;             // warps 2..9: two per TMEM lane quadrant
+constexpr int kTabWarp = 10;             // builds the shared-memory item table
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kATileBytes = 128 * 128;   // 128 rows x 64 bf16
 constexpr int kEpiBarAll = 1;            // named barrier over all epilogue warps
@@ -76,6 +78,8 @@ struct FfnParams {
   const int32_t* seg_counts;  // [E] rows per expert (slot placement), with
   int seg_cap;                // rows reserved per expert (0: compact row space, offsets)
   int rows_routed;            // rows of the routed row space
+  int32_t* counts_out;        // slot placement: optional copy of seg_counts
+  int BN;                     // token tile (item table)
   const int32_t* table;    // tile table (see internal.h)
   int* done;               // [G]
   bf16* act;               // [T*k, I]
@@ -113,12 +117,12 @@ struct Item {
   int need;  // completions a down item of group g waits for (one per gate/up feature tile)
 };
 
-// Shared-memory copy of the item table's starts and each expert's rows, so
-// that decoding an item costs no global-memory round trips:
-//   [0] gate/up items, [1] all items, [2, 2+G] gate/up starts per slot,
-//   [3+G, 3+2G] down starts per slot, [4+2G, 4+2G+E) first row per expert,
-//   [4+2G+E, 4+2G+2E) rows per expert.
-constexpr int kTabInts = 2 + 2 * (kMaxExperts + 2) + 2 * kMaxExperts;
+// Shared-memory item table, so that decoding an item costs no global-memory
+// round trips: the item table's layout up to its down starts ([0] gate/up
+// items, [1] down items, [8, 8+G] gate/up starts per slot, [9+G, 9+2G] down
+// starts per slot), then [10+2G, 10+2G+E) first row per expert and
+// [10+2G+E, 10+2G+2E) rows per expert.
+constexpr int kTabInts = 8 + 2 * (kMaxExperts + 2) + 2 * kMaxExperts;
 constexpr int kDealFailed = -2;  // the mailbox wait ran out
 
 // Item `it` of the dealing order.  FPI feature tiles per item (2 for CTA pairs:
@@ -144,11 +148,11 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p, const in
   }
   const int G = p.G;
   const int n_gu = tab[0];
-  const int* seg_first = tab + 4 + 2 * G;
+  const int* seg_first = tab + 10 + 2 * G;
   const int* seg_rows = seg_first + p.E;
   Item m;
   m.gu = it < n_gu;
-  const int* starts = m.gu ? tab + 2 : tab + 3 + G;
+  const int* starts = m.gu ? tab + 8 : tab + 9 + G;
   const int local_it = m.gu ? it : it - n_gu;
   int lo = 0, hi = G - 1;  // largest g with starts[g] <= local_it
   while (lo < hi) {
@@ -175,7 +179,7 @@ __device__ __forceinline__ Item decode_item(int it, const FfnParams& p, const in
   m.row0 = seg0 + tt * BN;
   m.cnt = min(BN, segn - tt * BN);
   m.nk = m.gu ? p.H / 64 : inter / 64;
-  m.need = (tab[2 + m.slot + 1] - tab[2 + m.slot]) * FPI;
+  m.need = (tab[8 + m.slot + 1] - tab[8 + m.slot]) * FPI;
   return m;
 }
 
@@ -190,7 +194,7 @@ struct Smem {
   static constexpr int kStageBytes = KCH * (kChunkA + kChunkB);
   static constexpr int kRing = STAGES * kStageBytes;
   static constexpr int kItemSlots = 4;
-  static constexpr int kBars = (2 * STAGES + 5 + 4 * kItemSlots) * 8;
+  static constexpr int kBars = (2 * STAGES + 6 + 4 * kItemSlots) * 8;
   static constexpr int kTotal = 1024 /*alignment slack*/ + kRing + kBars + 16 + 2 * kItemSlots * 4 +
                                 kItemSlots * (int)sizeof(Item) + kTabInts * 4;
   static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
@@ -222,7 +226,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
   uint64_t* item_empty = item_full + NS;
   uint64_t* deal_full = item_empty + NS;   // PAIR, peer: an index is in the mailbox
   uint64_t* deal_empty = deal_full + NS;   // PAIR, leader: the peer has taken the index
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(deal_empty + NS);
+  uint64_t* tab_ready = deal_empty + NS;   // the table warp has filled `tab`
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tab_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);
   volatile int* deal_slot = item_slot + NS;
@@ -249,6 +254,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       mbar_init(&deal_empty[q], 1);
     }
     mbar_init(final_bar, 1);
+    mbar_init(tab_ready, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -298,27 +304,19 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       bool have_tab = false;
       int dq = 0;  // mailbox position (PAIR)
       uint32_t dq_phase = 0;
-      // An index past the early items needs the routing: wait for the preceding kernels and
-      // copy the item table to shared memory (once); -1 past the last item.
+      // An index past the early items needs the routing: wait for the preceding kernels and for
+      // the shared-memory item table; -1 past the last item.
       auto resolve = [&](int it) {
         if (it >= p.n_static) {
           wait_inputs(it);
           if (!have_tab) {
-            const int G = p.G;
-            tab[0] = p.table[0];
-            tab[1] = p.table[0] + p.table[1];
-            for (int i = 0; i <= G; ++i) {
-              tab[2 + i] = p.table[8 + i];
-              tab[3 + G + i] = p.table[8 + G + 1 + i];
-            }
-            for (int e = 0; e < p.E; ++e) {
-              const bool slots = p.seg_cap > 0;
-              tab[4 + 2 * G + e] = slots ? e * p.seg_cap : p.offsets[e];
-              tab[4 + 2 * G + p.E + e] = slots ? p.seg_counts[e] : p.offsets[e + 1] - p.offsets[e];
+            if (!mbar_wait(tab_ready, 0, p.wait_ns)) {
+              set_error(p.err, kErrTimeout);
+              return -1;
             }
             have_tab = true;
           }
-          if (it >= tab[1]) it = -1;
+          if (it >= tab[0] + tab[1]) it = -1;
         }
         return it;
       };
@@ -557,6 +555,33 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
       if (!mbar_wait(final_bar, 0, p.wait_ns)) set_error(p.err, kErrTimeout);
     }
     __syncwarp();
+  } else if (warp == kTabWarp) {
+    // ------------------------------------------------------------ item table
+    // As soon as the routing is complete: the shared-memory item table, from the per-expert
+    // row counts (slot placement) or from the table and offsets the preceding kernel wrote.
+    pdl_wait();
+    const int G = p.G;
+    int* seg_first = tab + 10 + 2 * G;
+    int* seg_rows = seg_first + p.E;
+    if (p.seg_cap > 0) {
+      build_item_table(nullptr, p.seg_counts, p.T, p.H, p.E, p.k, p.S, p.I, p.BN, tab, p.err,
+                       /*zero_counters=*/false);
+      for (int e = lane; e < p.E; e += 32) {
+        const int c = p.seg_counts[e];
+        seg_first[e] = e * p.seg_cap;
+        seg_rows[e] = c;
+        if (p.counts_out && blockIdx.x == 0) p.counts_out[e] = c;
+      }
+    } else {
+      if (lane < 2) tab[lane] = p.table[lane];
+      for (int i = lane; i <= 2 * G + 1; i += 32) tab[8 + i] = p.table[8 + i];
+      for (int e = lane; e < p.E; e += 32) {
+        seg_first[e] = p.offsets[e];
+        seg_rows[e] = p.offsets[e + 1] - p.offsets[e];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tab_ready);  // release: the table is visible to the waiter
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..9)
     // Warp w may read TMEM lanes 32*(w%4)..+31.  Two warps per quadrant split the
@@ -723,7 +748,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
                     int seg_cap, const bf16* w_gate_up,
                     const bf16* w_down, const bf16* ws_gate_up, const bf16* ws_down, int T, int H, int E, int k,
                     int S, int I, void* y_perm, void* y_sh, bool y_bf16, uint8_t* ws, const WsLayout& L,
-                    const DeviceCtx& dc, cudaStream_t s, bool with_prep, bool early) {
+                    const DeviceCtx& dc, cudaStream_t s, bool with_prep, bool early, int32_t* counts_out) {
   using SM = Smem<BN, STAGES, KCH, PAIR>;
   static_assert(SM::kTotal <= 232448, "shared memory budget");
   static_assert(!PAIR || ffn_fpi(BN) == 2, "CTA pairs take two feature tiles per item");
@@ -790,6 +815,8 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.seg_counts = seg_counts;
   p.seg_cap = seg_cap;
   p.rows_routed = rows_routed;
+  p.counts_out = counts_out;
+  p.BN = BN;
   p.table = table;
   p.done = table + table_counters(G);
   p.counter = table + table_counters(G) + G;
@@ -842,10 +869,11 @@ cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offset
                        int seg_cap, const bf16* w_gate_up, const bf16* w_down, const bf16* ws_gate_up,
                        const bf16* ws_down, int T, int H, int E, int k, int S, int I, void* y_perm, void* y_sh,
                        bool y_bf16, uint8_t* ws, const WsLayout& L, const DeviceCtx& dc, cudaStream_t s,
-                       bool with_prep, bool early) {
+                       bool with_prep, bool early, int32_t* counts_out) {
 #define LSV_RUN_FFN(BN_, ST_, KCH_, PAIR_)                                                                     \
   run_ffn<BN_, ST_, KCH_, PAIR_>(x, perm, offsets, seg_counts, seg_cap, w_gate_up, w_down, ws_gate_up, ws_down, \
-                                 T, H, E, k, S, I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early)
+                                 T, H, E, k, S, I, y_perm, y_sh, y_bf16, ws, L, dc, s, with_prep, early,   \
+                                 counts_out)
   switch (ffn_token_tile(T, k, E)) {
     case 32:
       return LSV_RUN_FFN(32, LSV_FFN_STAGES32, LSV_FFN_KCH32, false);

@@ -38,14 +38,12 @@ uint64_t wait_limit_ns();
 //   [8+G+1 .. 8+2G+1]      down item start per group slot (G+1 entries)
 //   [8+2G+2 .. 8+3G+1]     counters: completed gate/up items per group slot ...
 //   [8+3G+2]               ... and the next item to deal
-//   [8+3G+3]               router CTAs finished (slot placement, below)
-//   [8+3G+4 .. 8+3G+3+E]   rows placed per expert (slot placement)
+//   [8+3G+3 .. 8+3G+2+E]   rows placed per expert (slot placement, below)
 // The counters from [8+2G+2] on are contiguous so that one memset zeroes
 // them.  Group slots are the dealing order: the shared group first (when
 // S > 0), then routed experts 0..E-1.
 __host__ __device__ inline int table_counters(int G) { return 8 + 2 * G + 2; }
-__host__ __device__ inline int table_arrive(int G) { return 8 + 3 * G + 3; }
-__host__ __device__ inline int table_slots(int G) { return table_arrive(G) + 1; }
+__host__ __device__ inline int table_slots(int G) { return 8 + 3 * G + 3; }
 __host__ __device__ inline int table_ints(int G, int E) { return table_slots(G) + E; }
 __host__ __device__ inline int table_zeroed_ints(int G, int E) { return table_ints(G, E) - table_counters(G); }
 
@@ -53,7 +51,8 @@ __host__ __device__ inline int table_zeroed_ints(int G, int E) { return table_in
 // CUDA cores): inside moe_verify_layer the router itself places each routed
 // row at expert e's next free row of a fixed region [e*T, (e+1)*T) -- an
 // atomic per-expert counter, so rows of one expert appear in any order, which
-// no result depends on -- and the last router CTA builds the item table.
+// no result depends on -- and each expert kernel CTA builds the item table from
+// the per-expert counts.
 constexpr int kSlotMaxTokens = 256;
 inline bool use_slots(int T) { return T > 0 && T <= kSlotMaxTokens; }
 // Rows of the routed row space (x_perm, act, y_perm) the workspace provides.
@@ -101,12 +100,9 @@ inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, 
 // Slot placement by the CUDA-core router (see use_slots): where to place the
 // routed rows and what the last router CTA writes.
 struct RouteSlots {
-  bf16* xperm;      // [E*T, H] routed row space
-  int32_t* inv;     // [T*k] row of each (token, rank)
-  int32_t* table;   // item table; its counters were zeroed before the router
-  int32_t* counts;  // optional [E]: final rows per expert
-  int S, I, BN;     // expert-kernel geometry for the item table
-  int* err;
+  bf16* xperm;     // [E*T, H] routed row space
+  int32_t* inv;    // [T*k] row of each (token, rank)
+  int32_t* slots;  // [E] rows taken per expert, zeroed before the router
 };
 
 cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int k, int32_t* idx, float* w,
@@ -136,12 +132,13 @@ int ffn_token_tile(int T, int k, int E);
 // preceding kernels finish.
 // y_perm/y_sh are fp32, or bf16 when y_bf16 (the fused layer keeps them in bf16).
 // seg_cap > 0: slot placement (expert e's rows are [e*seg_cap, e*seg_cap +
-// seg_counts[e]), table built by the router; offsets and perm unused).
+// seg_counts[e]); every CTA builds the item table from seg_counts; offsets and
+// perm unused; counts_out, if given, receives seg_counts).
 cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, const int32_t* seg_counts,
                        int seg_cap, const bf16* w_gate_up, const bf16* w_down, const bf16* ws_gate_up,
                        const bf16* ws_down, int T, int H, int E, int k, int S, int I, void* y_perm, void* y_sh,
                        bool y_bf16, uint8_t* ws, const WsLayout& L, const DeviceCtx& dc, cudaStream_t s,
-                       bool with_prep = true, bool early = false);
+                       bool with_prep = true, bool early = false, int32_t* counts_out = nullptr);
 
 // rows_y: rows of y_perm (inv entries outside [0, rows_y) raise LSV_ERR_DEVICE_INDEX).
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_sh,

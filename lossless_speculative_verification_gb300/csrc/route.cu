@@ -15,7 +15,6 @@
 // fp32 rounding (far below the router gaps the selection depends on).  The
 // E logits of each token then go through shared memory to one warp per token
 // for the softmax and the k selection rounds.
-#include "ffn_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -26,6 +25,7 @@ namespace {
 constexpr int kRouteWarps = 16;
 constexpr int kRouteTcMinTokens = 256;  // above this many tokens the router runs on tensor cores
 constexpr int kExpPerWarp = 4;
+constexpr int kLoadAhead = 5;  // 16-byte pieces per row and lane in flight together (H = 1280: a whole row)
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -44,8 +44,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
                                                                  float* __restrict__ logits, const RouteSlots sl) {
   __shared__ float lg[TT][kMaxExperts];
   __shared__ int sel_row[kMaxTopK];
-  __shared__ int s_cnt[kMaxExperts + 1];
-  __shared__ int is_last;
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -54,34 +52,44 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
   const int n8 = H / 8;  // 16-byte groups per row
   const bool slots = TT == 1 && sl.xperm != nullptr;
 
-  // warp w owns experts [4w, 4w+4), [4w+64, 4w+68), ...: four independent rows in flight per step
+  // warp w owns experts [4w, 4w+4), [4w+64, 4w+68), ...; each lane loads kLoadAhead 16-byte pieces
+  // of each of the four rows (and of x) before it uses any, so that one memory round trip
+  // covers a whole row block
   for (int e0 = warp * kExpPerWarp; e0 < E; e0 += kRouteWarps * kExpPerWarp) {
     float acc[kExpPerWarp][TT];
 #pragma unroll
     for (int q = 0; q < kExpPerWarp; ++q)
 #pragma unroll
       for (int i = 0; i < TT; ++i) acc[q][i] = 0.0f;
-#pragma unroll 5
-    for (int c = lane; c < n8; c += 32) {
-      uint4 wv[kExpPerWarp];
+    for (int c0 = lane; c0 < n8; c0 += 32 * kLoadAhead) {
+      uint4 wv[kExpPerWarp][kLoadAhead];
+      uint4 xv[TT][kLoadAhead];
 #pragma unroll
-      for (int q = 0; q < kExpPerWarp; ++q)
-        wv[q] = (e0 + q < E) ? __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + q) * H) + c)
-                             : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < kLoadAhead; ++u) {
+        const int c = c0 + 32 * u;
 #pragma unroll
-      for (int i = 0; i < TT; ++i) {
-        if (i < nt) {
+        for (int q = 0; q < kExpPerWarp; ++q)
+          wv[q][u] = (c < n8 && e0 + q < E) ? __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + q) * H) + c)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int i = 0; i < TT; ++i)
+          xv[i][u] = (c < n8 && i < nt) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + c)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadAhead; ++u)
+#pragma unroll
+        for (int i = 0; i < TT; ++i) {
           float xf[8];
-          bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + c), xf);
+          bf16x8_to_f32(xv[i][u], xf);
 #pragma unroll
           for (int q = 0; q < kExpPerWarp; ++q) {
             float wf[8];
-            bf16x8_to_f32(wv[q], wf);
+            bf16x8_to_f32(wv[q][u], wf);
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[q][i] = fmaf(xf[j], wf[j], acc[q][i]);
           }
         }
-      }
     }
 #pragma unroll
     for (int q = 0; q < kExpPerWarp; ++q)
@@ -122,7 +130,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
         w[(size_t)t * k + r] = expf(v - m) / z;
         if (slots) {
           // the next free row of expert e's region
-          const int row = e * T + atomicAdd(&sl.table[table_slots(E + (sl.S > 0 ? 1 : 0)) + e], 1);
+          const int row = e * T + atomicAdd(&sl.slots[e], 1);
           sl.inv[(size_t)t * k + r] = row;
           sel_row[r] = row;
         }
@@ -131,30 +139,13 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
   }
   if (!slots) return;
 
-  // The last CTA to take its rows sees every expert's final row count and builds the item
-  // table, while the other CTAs place their token's row at its k rows of the routed row space.
+  // place the token's row at its k rows of the routed row space
   __syncthreads();
-  const int G = E + (sl.S > 0 ? 1 : 0);
-  if (threadIdx.x == 0) {
-    __threadfence();
-    is_last = atomicAdd(&sl.table[table_arrive(G)], 1) == (int)gridDim.x - 1;
-  }
   if (warp < k) {
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t0 * H);
     uint4* dst = reinterpret_cast<uint4*>(sl.xperm + (size_t)sel_row[warp] * H);
     for (int c = lane; c < n8; c += 32) dst[c] = __ldg(src + c);
   }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int c = __ldcg(&sl.table[table_slots(G) + e]);
-    s_cnt[e] = c;
-    if (sl.counts) sl.counts[e] = c;
-  }
-  __syncthreads();
-  if (warp == 0)
-    build_item_table(nullptr, s_cnt, T, H, E, k, sl.S, sl.I, sl.BN, sl.table, sl.err, /*zero_counters=*/false);
 }
 
 // ----------------------------------------------------------------------------- tensor-core router
@@ -363,11 +354,8 @@ cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int
   }
   const dim3 block(kRouteWarps * 32);
   // about one CTA per SM at decode sizes; more tokens per CTA once T is large
-  if (T <= 256) return launch_pdl(route_kernel<1>, dim3(T), block, 0, s, x, wr, T, H, E, k, idx, w, logits, sl);
-  if (slots) return cudaErrorInvalidValue;  // slot placement is for the one-token-per-CTA router only
-  if (T <= 1024)
-    return launch_pdl(route_kernel<4>, dim3((T + 3) / 4), block, 0, s, x, wr, T, H, E, k, idx, w, logits, sl);
-  return launch_pdl(route_kernel<8>, dim3((T + 7) / 8), block, 0, s, x, wr, T, H, E, k, idx, w, logits, sl);
+  // one CTA per token (at most 256 tokens here; more go to the tensor-core router above)
+  return launch_pdl(route_kernel<1>, dim3(T), block, 0, s, x, wr, T, H, E, k, idx, w, logits, sl);
 }
 
 }  // namespace lsv
