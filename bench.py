@@ -272,10 +272,13 @@ class DeviceStep:
             self.comm = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
         else:
             self.logits = None
-        # our launches per step.  Per layer: route, fused permute+gather (<= 8192 pairs; else count,
-        # scatter and prep), experts, combine, and rmsnorm in the stack.  Acceptance: partials + finalize.
-        per_layer = 4 if d.T * d.k <= 8192 else 6
-        self.launches = len(self.layers) * (per_layer + (1 if w.layers > 1 else 0)) + (2 if w.V else 0)
+        # our kernel launches per step (the counter memset is not one).  Per layer: up to 256 tokens the
+        # router (which places the rows), experts, combine; above, the tensor-core router, the fused
+        # permutation + gather (<= 8192 pairs; else count, scatter and prep), experts, combine; plus
+        # rmsnorm in the stack.  Acceptance: partials + finalize.
+        per_layer = 3 if d.T <= 256 else (4 if d.T * d.k <= 8192 else 6)
+        acc = 2 if w.V else 0
+        self.launches = len(self.layers) * (per_layer + (1 if w.layers > 1 else 0)) + acc
 
     def _layers(self, x_in):
         api = self.api

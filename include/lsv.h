@@ -76,7 +76,11 @@ typedef struct {
 } lsv_moe_weights;
 
 /* Bytes of workspace moe_verify_layer / moe_grouped_ffn / moe_permute need for
- * `shape` (a multiple of 256).  Returns 0 for an unsupported shape. */
+ * `shape` (a multiple of 256).  Returns 0 for an unsupported shape.
+ * The first 4 KiB of the workspace are a counter block, at the same place for
+ * every shape: they must be zero before the workspace's first use, and every
+ * call that raises no device error leaves them zero again, so one workspace
+ * serves any sequence of calls and shapes (zero them again after an error). */
 size_t lsv_workspace_size(const lsv_moe_shape *shape);
 
 /* Start streaming expert weights into L2, in the order moe_grouped_ffn reads

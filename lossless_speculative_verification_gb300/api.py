@@ -58,7 +58,8 @@ def workspace_size(sh: MoeShape) -> int:
 
 
 def workspace(sh: MoeShape, device=None) -> torch.Tensor:
-    return torch.empty(workspace_size(sh), dtype=torch.uint8, device=device or "cuda")
+    """Zero-filled: the layer wants the workspace's counter block zero before the first call."""
+    return torch.zeros(workspace_size(sh), dtype=torch.uint8, device=device or "cuda")
 
 
 def moe_prefetch_weights(w: MoeWeights, sh: MoeShape, max_bytes: int, stream=None) -> None:

@@ -78,6 +78,7 @@ WsLayout ws_layout(int T, int H, int E, int k, int S, int I) {
     o = align256(o + bytes);
     return at;
   };
+  L.counters = take(kCounterBytes);
   L.topk_idx = take(n * 4);
   L.topk_w = take(n * 4);
   L.counts = take((size_t)E * 4);
@@ -85,7 +86,7 @@ WsLayout ws_layout(int T, int H, int E, int k, int S, int I) {
   L.perm = take(n * 4);
   L.inv = take(n * 4);
   L.blk_counts = take((size_t)L.nblk * E * 4);
-  L.table = take((size_t)table_ints(G, E) * 4);
+  L.table = take((size_t)table_ints(G) * 4);
   const size_t rows = routed_rows(T, k, E);
   L.xperm = take(rows * H * 2);
   L.act = take(rows * I * 2);
@@ -320,11 +321,11 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   const bf16* wdn = static_cast<const bf16*>(wt->w_down);
   const bf16* wsgu = static_cast<const bf16*>(wt->ws_gate_up);
   const bf16* wsdn = static_cast<const bf16*>(wt->ws_down);
-  // zero the grouped-expert kernel's counters (and the router's slot counters) before anything
-  // else of this layer runs, so that it can begin the routing-independent shared-expert items early
-  const int G = E + (S > 0 ? 1 : 0);
+  // The counter block is zero on entry (the previous call's expert kernel cleared it), so the
+  // expert kernel can begin its routing-independent shared-expert items while the router runs.
   int32_t* table = reinterpret_cast<int32_t*>(w + L.table);
-  cudaError_t e = cudaMemsetAsync(table + table_counters(G), 0, (size_t)table_zeroed_ints(G, E) * 4, s);
+  int32_t* cnt = reinterpret_cast<int32_t*>(w + L.counters);
+  cudaError_t e = cudaSuccess;
   const uint64_t pf = default_prefetch_bytes(*dc, T, E, k, S, I, H);
   if (e == cudaSuccess && pf) e = launch_weight_prefetch(wgu, wdn, wsgu, wsdn, H, E, S, I, pf, *dc, s);
   const int BN = ffn_token_tile(T, k, E);
@@ -333,12 +334,12 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
     RouteSlots sl;
     sl.xperm = reinterpret_cast<bf16*>(w + L.xperm);
     sl.inv = inv;
-    sl.slots = table + table_slots(G);
+    sl.slots = cnt + kCntSlots;
     if (e == cudaSuccess)
       e = launch_route(static_cast<const bf16*>(x), static_cast<const bf16*>(wt->w_router), T, H, E, k, idx, tw,
                        nullptr, s, &sl);
     if (e == cudaSuccess)
-      e = launch_ffn(static_cast<const bf16*>(x), nullptr, nullptr, table + table_slots(G), T, wgu, wdn, wsgu, wsdn,
+      e = launch_ffn(static_cast<const bf16*>(x), nullptr, nullptr, cnt + kCntSlots, T, wgu, wdn, wsgu, wsdn,
                      T, H, E, k, S, I, y_perm, y_sh, /*y_bf16=*/true, w, L, *dc, s, /*with_prep=*/false,
                      /*early=*/true, counts_opt);
   } else {
@@ -360,7 +361,8 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   }
   if (e == cudaSuccess)
     e = launch_combine(y_perm, inv, tw, S > 0 ? y_sh : nullptr, /*y_bf16=*/true, T, H, k,
-                       use_slots(T) ? E * T : T * k, static_cast<bf16*>(out), dc->err, s);
+                       use_slots(T) ? E * T : T * k, static_cast<bf16*>(out), dc->err, s, cnt,
+                       (int)(kCounterBytes / 4));
   return from_cuda(e);
 }
 

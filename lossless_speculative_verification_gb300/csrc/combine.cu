@@ -52,12 +52,15 @@ template <typename YT>
 __global__ void __launch_bounds__(256) combine_kernel(const YT* __restrict__ y_perm, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ topk_w, const YT* __restrict__ y_sh,
                                                       int T, int H, int k, int rows_y, bf16* __restrict__ out,
-                                                      int* err) {
+                                                      int* err, int32_t* __restrict__ clear, int n_clear) {
   const int t = blockIdx.x;
   __shared__ int rows[kMaxTopK];
   __shared__ float wts[kMaxTopK];
   pdl_wait();
   pdl_trigger();
+  // the layer's counter block, for the next call (everything that used it has completed)
+  if (clear && t == 0)
+    for (int i = threadIdx.x; i < n_clear; i += blockDim.x) clear[i] = 0;
   if (threadIdx.x < k) {
     int r = inv[(size_t)t * k + threadIdx.x];
     if (r < 0 || r >= rows_y) {  // never read outside y_perm
@@ -127,15 +130,16 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_residual_kernel(bf16* __
 }  // namespace
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_sh,
-                           bool y_bf16, int T, int H, int k, int rows_y, bf16* out, int* err, cudaStream_t s) {
+                           bool y_bf16, int T, int H, int k, int rows_y, bf16* out, int* err, cudaStream_t s,
+                           int32_t* clear, int n_clear) {
   if (T == 0) return cudaSuccess;
   int threads = ((H / 8 + 31) / 32) * 32;
   if (threads > 256) threads = 256;
   if (y_bf16)
     return launch_pdl(combine_kernel<bf16>, dim3(T), dim3(threads), 0, s, static_cast<const bf16*>(y_perm), inv,
-                      topk_w, static_cast<const bf16*>(y_sh), T, H, k, rows_y, out, err);
+                      topk_w, static_cast<const bf16*>(y_sh), T, H, k, rows_y, out, err, clear, n_clear);
   return launch_pdl(combine_kernel<float>, dim3(T), dim3(threads), 0, s, static_cast<const float*>(y_perm), inv,
-                    topk_w, static_cast<const float*>(y_sh), T, H, k, rows_y, out, err);
+                    topk_w, static_cast<const float*>(y_sh), T, H, k, rows_y, out, err, clear, n_clear);
 }
 
 cudaError_t launch_rmsnorm_residual(bf16* x, const bf16* y, bf16* h, int T, int H, float eps, cudaStream_t s) {

@@ -90,6 +90,9 @@ struct FfnParams {
   int* err;
   uint64_t wait_ns;
   int* counter;            // next item to deal
+  int* exit_count;         // CTAs finished (with clear_at_end, the last one clears the counters)
+  int clear_at_end;
+  int32_t* slots_clear;    // slot placement: the per-expert row counters, cleared at the end
   int n_static;            // leading gate/up items of the shared group, decodable without the table
   int deal_ahead;          // take each next item index one item early
 };
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     // ------------------------------------------------------------ TMA producer + item dealer
     if (lane == 0) {
       int* counter = p.counter;
-      // without early items the counters are zeroed by the preceding kernel: wait for it first
+      // without early items the preceding kernel (the standalone prep) clears the counters: wait for it
       if (p.n_static == 0) wait_inputs(0);
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
@@ -564,8 +567,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     int* seg_first = tab + 10 + 2 * G;
     int* seg_rows = seg_first + p.E;
     if (p.seg_cap > 0) {
-      build_item_table(nullptr, p.seg_counts, p.T, p.H, p.E, p.k, p.S, p.I, p.BN, tab, p.err,
-                       /*zero_counters=*/false);
+      build_item_table(nullptr, p.seg_counts, p.T, p.H, p.E, p.k, p.S, p.I, p.BN, tab, p.err);
       for (int e = lane; e < p.E; e += 32) {
         const int c = p.seg_counts[e];
         seg_first[e] = e * p.seg_cap;
@@ -706,6 +708,26 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     else
       tmem_dealloc(tmem_base, SM::kTmemCols);
   }
+  // Standalone calls: the last CTA to finish sets the counters back to zero for the next call
+  // (every other CTA has finished everything that reads or adds to them).  Inside the layer the
+  // combine kernel that follows clears them instead, off this kernel's critical path.
+  if (p.clear_at_end) {
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = atomicAdd(p.exit_count, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+      for (int g = threadIdx.x; g < p.G; g += blockDim.x) p.done[g] = 0;
+      if (p.seg_cap > 0)
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.slots_clear[e] = 0;
+      if (threadIdx.x == 0) {
+        *p.counter = 0;
+        *p.exit_count = 0;
+      }
+    }
+  }
 }
 
 // Gathers the routed token rows into expert order (x_perm[r] = x[perm[r] / k])
@@ -714,7 +736,8 @@ template <int BN>
 __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ perm,
                                                        const int32_t* __restrict__ offsets, int T, int H, int E,
                                                        int k, int S, int I, bf16* __restrict__ xperm,
-                                                       int32_t* __restrict__ table, int* err, bool zero_counters) {
+                                                       int32_t* __restrict__ table, int* err,
+                                                       int32_t* __restrict__ counters) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -739,7 +762,14 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const bf16* __restrict__ 
       }
     }
   }
-  if (blockIdx.x == 0 && threadIdx.x < 32) build_item_table(offsets, nullptr, T, H, E, k, S, I, BN, table, err, zero_counters);
+  if (blockIdx.x == 0 && threadIdx.x < 32) {
+    build_item_table(offsets, nullptr, T, H, E, k, S, I, BN, table, err);
+    if (counters) {  // standalone call: clear the expert kernel's counters as well
+      const int G = E + (S > 0 ? 1 : 0);
+      for (int g = lane; g < G; g += 32) counters[kCntDone + g] = 0;
+      if (lane == 0) counters[kCntDeal] = 0;
+    }
+  }
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -781,6 +811,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
     attr_done[dc.device] = 1;
   }
   int32_t* table = reinterpret_cast<int32_t*>(ws + L.table);
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + L.counters);
   bf16* xperm = reinterpret_cast<bf16*>(ws + L.xperm);
   bf16* act = reinterpret_cast<bf16*>(ws + L.act);
   bf16* act_sh = reinterpret_cast<bf16*>(ws + L.act_sh);
@@ -791,7 +822,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   if (with_prep) {
     const int prep_blocks = max(1, (nrows + 7) / 8);
     const cudaError_t e = launch_pdl(ffn_prep_kernel<BN>, dim3(prep_blocks), dim3(256), 0, s, x, perm, offsets, T,
-                                     H, E, k, S, I, xperm, table, dc.err, /*zero_counters=*/!early);
+                                     H, E, k, S, I, xperm, table, dc.err, early ? nullptr : counters);
     if (e != cudaSuccess) return e;
   }
 
@@ -818,8 +849,11 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.counts_out = counts_out;
   p.BN = BN;
   p.table = table;
-  p.done = table + table_counters(G);
-  p.counter = table + table_counters(G) + G;
+  p.done = counters + kCntDone;
+  p.counter = counters + kCntDeal;
+  p.exit_count = counters + kCntExit;
+  p.clear_at_end = early ? 0 : 1;  // the layer (early items) clears them in its combine
+  p.slots_clear = seg_cap > 0 ? const_cast<int32_t*>(seg_counts) : nullptr;
   constexpr int FPI = PAIR ? 2 : 1;
   p.n_static = (early && S > 0) ? ((T + BN - 1) / BN) * ((S * I / 64 + FPI - 1) / FPI) : 0;
   p.act = act;

@@ -26,13 +26,10 @@ __host__ __device__ __forceinline__ int slot_group(int slot, int E, int S) {
 // ffn_fpi(BN) feature tiles per item.  Rows per expert come from the expert
 // offsets (compact row space: offsets must partition [0, T*k)) or, when
 // `counts` is given, from per-expert row counts of at most T (slot placement).
-// Executed by all 32 lanes of one warp.  zero_counters: also reset the
-// completion and dealing counters (otherwise the caller did, before the
-// routing began).  Inconsistent offsets or counts schedule no item and raise
-// LSV_ERR_DEVICE_INDEX.
+// Executed by all 32 lanes of one warp.  Inconsistent offsets or counts
+// schedule no item and raise LSV_ERR_DEVICE_INDEX.
 __device__ __forceinline__ void build_item_table(const int32_t* offsets, const int32_t* counts, int T, int H, int E,
-                                                 int k, int S, int I, int BN, int32_t* table, int* err,
-                                                 bool zero_counters) {
+                                                 int k, int S, int I, int BN, int32_t* table, int* err) {
   const int lane = threadIdx.x & 31;
   const int nrows = T * k;
   const int G = E + (S > 0 ? 1 : 0);
@@ -91,7 +88,6 @@ __device__ __forceinline__ void build_item_table(const int32_t* offsets, const i
       table[8 + slot] = gu_run;
       table[8 + G + 1 + slot] = dn_run;
     }
-    if (zero_counters && slot < G) table[8 + 2 * G + 2 + slot] = 0;
     gu_run += gu_loc[j];
     dn_run += dn_loc[j];
   }
@@ -99,7 +95,6 @@ __device__ __forceinline__ void build_item_table(const int32_t* offsets, const i
     table[0] = gu_incl;
     table[1] = dn_incl;
     table[2] = G;
-    if (zero_counters) table[8 + 3 * G + 2] = 0;  // next item to deal
   }
 }
 

@@ -32,20 +32,27 @@ cudaError_t device_ctx(DeviceCtx** out);
 uint64_t wait_limit_ns();
 
 // ---------------------------------------------------------------- FFN tile table
-// int32 table in the workspace, written by the prep kernel, read by the FFN kernel.
+// int32 table in the workspace, written by the kernel that completes the
+// permutation, read by the FFN kernel.
 //   [0] gate/up items  [1] down items  [2] groups G
 //   [8 .. 8+G]             gate/up item start per group slot (exclusive scan, G+1 entries)
 //   [8+G+1 .. 8+2G+1]      down item start per group slot (G+1 entries)
-//   [8+2G+2 .. 8+3G+1]     counters: completed gate/up items per group slot ...
-//   [8+3G+2]               ... and the next item to deal
-//   [8+3G+3 .. 8+3G+2+E]   rows placed per expert (slot placement, below)
-// The counters from [8+2G+2] on are contiguous so that one memset zeroes
-// them.  Group slots are the dealing order: the shared group first (when
-// S > 0), then routed experts 0..E-1.
-__host__ __device__ inline int table_counters(int G) { return 8 + 2 * G + 2; }
-__host__ __device__ inline int table_slots(int G) { return 8 + 3 * G + 3; }
-__host__ __device__ inline int table_ints(int G, int E) { return table_slots(G) + E; }
-__host__ __device__ inline int table_zeroed_ints(int G, int E) { return table_ints(G, E) - table_counters(G); }
+// Group slots are the dealing order: the shared group first (when S > 0),
+// then routed experts 0..E-1.
+__host__ __device__ inline int table_ints(int G) { return 8 + 2 * (G + 1); }
+
+// ---------------------------------------------------------------- counter block
+// The first kCounterBytes of the workspace, at the same place for every shape:
+// the counters of one layer call.  They are zero when a call begins -- the
+// caller zeroes the block once, and every call clears them when it is done
+// with them (the layer in its combine kernel, a standalone expert call in the
+// expert kernel's last CTA) -- so no launch has to clear them first.
+constexpr int kCntDone = 0;                      // [kMaxExperts + 1] finished gate/up tiles per group slot
+constexpr int kCntDeal = kMaxExperts + 1;        // next item to deal
+constexpr int kCntExit = kMaxExperts + 2;        // expert-kernel CTAs finished
+constexpr int kCntSlots = kMaxExperts + 4;       // [kMaxExperts] rows placed per expert (slot placement)
+constexpr size_t kCounterBytes = 4096;
+static_assert((kCntSlots + kMaxExperts) * 4 <= (int)kCounterBytes, "counter block");
 
 // Slot placement (token counts up to kSlotMaxTokens, where the router runs on
 // CUDA cores): inside moe_verify_layer the router itself places each routed
@@ -68,6 +75,7 @@ struct FfnGeom {
 
 // Workspace layout (byte offsets, each region 256-byte aligned).
 struct WsLayout {
+  size_t counters;  // always 0: the counter block leads the workspace
   size_t topk_idx, topk_w, counts, offsets, perm, inv, blk_counts, table, xperm, act, act_sh, y_perm, y_sh;
   size_t total;
   int nblk;  // permutation blocks
@@ -141,8 +149,10 @@ cudaError_t launch_ffn(const bf16* x, const int32_t* perm, const int32_t* offset
                        bool with_prep = true, bool early = false, int32_t* counts_out = nullptr);
 
 // rows_y: rows of y_perm (inv entries outside [0, rows_y) raise LSV_ERR_DEVICE_INDEX).
+// clear: optional int32 region of n_clear entries zeroed once the previous kernels completed.
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_sh,
-                           bool y_bf16, int T, int H, int k, int rows_y, bf16* out, int* err, cudaStream_t s);
+                           bool y_bf16, int T, int H, int k, int rows_y, bf16* out, int* err, cudaStream_t s,
+                           int32_t* clear = nullptr, int n_clear = 0);
 
 cudaError_t launch_rmsnorm_residual(bf16* x, const bf16* y, bf16* h, int T, int H, float eps, cudaStream_t s);
 

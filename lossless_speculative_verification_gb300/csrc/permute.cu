@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kPgThreads) permute_gather_kernel(
     }
     pos_s[lane] = pos;
   } else if (warp == 1 && blockIdx.x == 0) {
-    build_item_table(off, nullptr, T, H, E, k, S, I, BN, table, err, /*zero_counters=*/false);
+    build_item_table(off, nullptr, T, H, E, k, S, I, BN, table, err);
   }
   __syncthreads();
   for (int j = warp; j < s1 - s0; j += kPgThreads / 32) {

@@ -194,6 +194,23 @@ def test_layer_parity(name, nsample):
     assert_layer_close(bf16_f64(from_dev_bf16(out))[toks], ref, name)
 
 
+def test_layer_workspace_reuse_across_shapes():
+    # one workspace for calls of different shapes and paths: every call must leave the counter
+    # block at zero for the next one
+    probs = [dev_problem("decode"), pair_problem(*PAIR_SHAPES[0]), dev_problem("tiny"), dev_problem("decode")]
+    n = max(api.workspace_size(P.sh) for P in probs)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    for P in probs:
+        d, prob = P.d, P.prob
+        out = api.moe_verify_layer(P.x, P.wts, P.sh, ws)
+        torch.cuda.synchronize()
+        toks = sample_rows(d.T, 32, 7)
+        ref, _, _ = oracle.moe_layer(prob.x, prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up,
+                                     prob.ws_down, d.k, d.S, tokens=toks)
+        assert_layer_close(bf16_f64(from_dev_bf16(out))[toks], ref, "reuse T=%d" % d.T)
+    assert not ws[:4096].any()
+
+
 def test_layer_is_deterministic():
     P = dev_problem("decode")
     a = api.moe_verify_layer(P.x, P.wts, P.sh, P.ws)
@@ -242,7 +259,7 @@ def test_accept_parity_sweep(B, K):
 
 
 @pytest.mark.parametrize("B,K,V", [(4, 3, 1024), (3, 2, 1023), (5, 1, 7), (2, 0, 100), (1, 7, 129_281),
-                                   (2, 63, 64), (600, 3, 4096)])
+                                   (2, 63, 64), (600, 3, 4096), (4100, 1, 1024)])
 def test_accept_edge_shapes(B, K, V):
     logits, planted = synth.verify_logits(B, K, V, seed=V + K)
     drafts = synth.draft_tokens(planted, V, [0.9] * K, seed=B)
@@ -299,6 +316,21 @@ def test_speculative_loop_on_gpu_equals_greedy():
         _, alen, comm = run_accept(lg, np.array([drafts], np.int32))
         out.extend(int(c) for c in comm[0, :alen[0] + 1])
     assert out[2:2 + n_tok] == seq[2:2 + n_tok]
+
+
+def test_accept_workspace_reuse():
+    # one workspace across calls of different shapes: each call must leave its counters at zero
+    ws = api.spec_verify_workspace(64, 7, 129_280)
+    for B, K, V, seed in [(32, 3, 129_280, 1), (64, 7, 129_280, 2), (3, 1, 4096, 3), (32, 3, 129_280, 4)]:
+        logits, planted = synth.verify_logits(B, K, V, seed=seed)
+        drafts = synth.draft_tokens(planted, V, [0.8] * K, seed=seed)
+        argmax = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+        alen, comm = api.spec_verify_accept(to_dev(logits), torch.from_numpy(drafts).cuda(), ws, argmax=argmax)
+        torch.cuda.synchronize()
+        rg, ralen, rcomm = oracle.accept(logits, drafts)
+        np.testing.assert_array_equal(argmax.cpu().numpy(), rg)
+        np.testing.assert_array_equal(alen.cpu().numpy(), ralen)
+        np.testing.assert_array_equal(comm.cpu().numpy(), rcomm)
 
 
 def test_accept_is_deterministic():
