@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack", "lmhead"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed oracle sample (for profiler runs; the line then has no cpu_baseline)")
@@ -335,6 +335,105 @@ class DeviceStep:
         self.h_out.copy_(self.out, non_blocking=True)
 
 
+class LmHeadStep:
+    """Greedy verification with the logits made by the verifier's output layer inside the call
+    (spec_verify_lmhead): 32 sequences x (K=3)+1 positions, hidden 1280, vocabulary 129,280.
+    Same interface as DeviceStep; its `layer()` is empty."""
+
+    B, K, V, H = 32, 3, 129_280, 1280
+
+    def __init__(self, seed, dev):
+        import torch
+        import oracle
+        from lossless_speculative_verification_gb300 import api, synth
+        self.name, self.dev, self.api = "lmhead", dev, api
+        self.w = None
+        self.layers = []
+        self.T = self.B * (self.K + 1)
+        p = synth.lmhead_problem(self.B, self.K, V=self.V, H=self.H, seed=seed, judge=oracle.lmhead_judge())
+        self.problem = p
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        self.hidden, self.w_vocab = t(p.hidden), t(p.w_vocab)
+        self.drafts = torch.from_numpy(p.drafts).to(dev)
+        self.ws = api.spec_verify_lmhead_workspace(self.B, self.K, self.V, self.H, dev)
+        self.alen = torch.empty(self.B, dtype=torch.int32, device=dev)
+        self.comm = torch.empty((self.B, self.K + 1), dtype=torch.int32, device=dev)
+        self.launches = 2  # the fused output layer + greedy search, then the acceptance rule
+
+    @classmethod
+    def host_only(cls, seed):
+        """The inputs on the host only (for the CPU oracle)."""
+        import oracle
+        from lossless_speculative_verification_gb300 import synth
+        step = cls.__new__(cls)
+        step.T = cls.B * (cls.K + 1)
+        step.problem = synth.lmhead_problem(cls.B, cls.K, V=cls.V, H=cls.H, seed=seed, judge=oracle.lmhead_judge())
+        return step
+
+    def layer(self):
+        pass
+
+    def accept(self):
+        self.api.spec_verify_lmhead(self.hidden, self.w_vocab, self.drafts, self.ws, self.K, accept_len=self.alen,
+                                    committed=self.comm)
+
+    def check(self):
+        """The committed tokens against the oracle's (the parity tests cover every shape)."""
+        import oracle
+        alen, comm = oracle.accept_from_greedy(self.problem.greedy, self.problem.drafts)
+        assert np.array_equal(self.alen.cpu().numpy(), alen) and np.array_equal(self.comm.cpu().numpy(), comm)
+
+    def bytes_and_flops(self):
+        byts = self.V * self.H * 2 + self.T * self.H * 2
+        return byts, 2.0 * self.T * self.V * self.H, 0
+
+    def setup_e2e(self):
+        import torch
+        self.h_hidden = self.hidden.cpu().pin_memory()
+        self.h_drafts = self.drafts.cpu().pin_memory()
+        self.d_hidden, self.d_drafts = torch.empty_like(self.hidden), torch.empty_like(self.drafts)
+        self.h_len = torch.empty_like(self.alen, device="cpu").pin_memory()
+        self.h_comm = torch.empty_like(self.comm, device="cpu").pin_memory()
+        h2d = self.h_hidden.numel() * 2 + self.h_drafts.numel() * 4
+        d2h = self.h_len.numel() * 4 + self.h_comm.numel() * 4
+        return h2d, d2h
+
+    def e2e(self):
+        self.d_hidden.copy_(self.h_hidden, non_blocking=True)
+        self.d_drafts.copy_(self.h_drafts, non_blocking=True)
+        self.api.spec_verify_lmhead(self.d_hidden, self.w_vocab, self.d_drafts, self.ws, self.K,
+                                    accept_len=self.alen, committed=self.comm)
+        self.h_len.copy_(self.alen, non_blocking=True)
+        self.h_comm.copy_(self.comm, non_blocking=True)
+
+
+def lmhead_oracle_sampler(step):
+    """The oracle's output layer (numpy fp64 matmul over the vocabulary, chunked) on whole
+    positions, cycling over the batch, plus the acceptance rule of their sequences."""
+    import oracle
+    p = step.problem
+    state = {"n": 0}
+
+    def sample(seconds):
+        n0 = state["n"]
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            r = state["n"] % step.T
+            oracle.lmhead_argmax(p.hidden[r:r + 1], p.w_vocab)
+            if r % (step.K + 1) == step.K:
+                b = r // (step.K + 1)
+                oracle.accept_from_greedy(p.greedy[b:b + 1], p.drafts[b:b + 1])
+            state["n"] += 1
+        dt = time.perf_counter() - t0
+        n = state["n"] - n0
+        return {"value": n / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                "kind": "oracle (numpy fp64 matmul; its BLAS may use every core)",
+                "sample": "%d positions (cycling over the %d) through the oracle's output layer and greedy "
+                          "search, plus the acceptance of their sequences, %.1f s" % (n, step.T, dt)}
+
+    return sample
+
+
 def flush_l2(flush, i):
     """Evict the step's data from L2: write a buffer larger than L2, then read it back, so that the
     L2 holds only clean lines of the flush buffer and the step pays no write-back of them."""
@@ -477,7 +576,14 @@ def result_line(args, step, m, world, cpu):
     w = step.w
     byts, flops, acc_bytes = step.bytes_and_flops()
     khash = layer_source_hash()
-    if step.name == "prefill":
+    if step.name == "lmhead":
+        achieved = byts / (m["total_ms"] / args.steps / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "algorithmic_bytes": byts, "algorithmic_flops": flops,
+                "kernel": "lmhead_argmax_kernel (tcgen05 product of the output layer and the hidden rows, reduced "
+                          "to each row's (max, first index) per 128-token vocabulary tile) + accept_finalize_kernel",
+                "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}
+    elif step.name == "prefill":
         achieved = flops / (m["layer_ms"] / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s", "frac": achieved / tflops,
                 "algorithmic_flops": flops}
@@ -485,10 +591,11 @@ def result_line(args, step, m, world, cpu):
         achieved = byts / (m["layer_ms"] / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts}
-    roof.update({"kernel": "moe_verify_layer x%d: router, permute+gather, grouped SwiGLU experts (tcgen05), "
-                           "combine; one PDL-chained launch sequence per layer" % len(step.layers),
-                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "layer_ms": m["layer_ms"],
-                 "kernel_source_hash": khash})
+    if step.name != "lmhead":
+        roof.update({"kernel": "moe_verify_layer x%d: router, permute+gather, grouped SwiGLU experts (tcgen05), "
+                               "combine; one PDL-chained launch sequence per layer" % len(step.layers),
+                     "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "layer_ms": m["layer_ms"],
+                     "kernel_source_hash": khash})
     if acc_bytes:
         roof["accept"] = {"ms": m["accept_ms"], "algorithmic_bytes": acc_bytes,
                           "achieved_gbs": acc_bytes / (m["accept_ms"] / 1e3) / 1e9}
@@ -497,7 +604,10 @@ def result_line(args, step, m, world, cpu):
         "metric": METRIC, "value": tokens / (m["total_ms"] / 1e3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["total_ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s: %s" % (step.name, describe(w, len(step.layers))),
+        "config": {"workload": "%s: %s" % (step.name, describe(w, len(step.layers)) if w is not None else
+                                           "greedy verification of [%d,%d] positions with the logits made by the "
+                                           "output layer [%d,%d] inside the call (B=%d, K=%d)"
+                                           % (step.B, step.K + 1, step.V, step.H, step.B, step.K)),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MB written, then read back, outside the events)",
                    "timing": ("step replayed as one CUDA graph with CUDA events recorded as graph nodes at its "
@@ -519,6 +629,8 @@ def result_line(args, step, m, world, cpu):
 
 def workloads(name):
     from lossless_speculative_verification_gb300 import synth
+    if name == "lmhead":
+        return [("lmhead", None, 0)]
     if name == "sweep":
         return [("sweep", synth.sweep_workload(B, K), synth.sweep_seed(B, K))
                 for B in synth.SWEEP_B for K in synth.SWEEP_K]
@@ -577,7 +689,14 @@ def run_reference(args, rank, world):
         return
     for name, w, seed in workloads(args.workload):
         per_step = 2.0 if name != "sweep" else 0.5       # seconds of oracle work per timed step
-        sample = oracle_sampler(w, seed + args.seed)
+        if name == "lmhead":
+            step = LmHeadStep.host_only(seed + args.seed)
+            sample = lmhead_oracle_sampler(step)
+            w_desc = "greedy verification of [%d,%d] positions through the output layer [%d,%d]" % (
+                step.B, step.K + 1, step.V, step.H)
+        else:
+            sample = oracle_sampler(w, seed + args.seed)
+            w_desc = describe(w, w.layers)
         sample(0.2 * max(args.warmup, 1))                # warm-up
         t0 = time.perf_counter()
         res = sample(per_step * args.steps)
@@ -586,7 +705,7 @@ def run_reference(args, rank, world):
             "impl": "reference", "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "%s: %s" % (name, describe(w, w.layers)), "l2": "n/a (CPU)"},
+            "config": {"workload": "%s: %s" % (name, w_desc), "l2": "n/a (CPU)"},
             "cpu_baseline": res,
             "e2e": {"value": res["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
@@ -609,11 +728,17 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for name, w, seed in workloads(args.workload):
-        step = DeviceStep(name, w, seed + args.seed + 1000 * rank, dev)
+        if name == "lmhead":
+            step = LmHeadStep(seed + args.seed + 1000 * rank, dev)
+        else:
+            step = DeviceStep(name, w, seed + args.seed + 1000 * rank, dev)
         m = measure(step, args, local, world, flush, dist)
+        if name == "lmhead":
+            step.check()
         cpu = None
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            cpu = oracle_sampler(w, seed + args.seed)(12.0 if args.workload != "sweep" else 2.0)
+            sampler = lmhead_oracle_sampler(step) if name == "lmhead" else oracle_sampler(w, seed + args.seed)
+            cpu = sampler(12.0 if args.workload != "sweep" else 2.0)
         if rank == 0:
             print(json.dumps(result_line(args, step, m, world, cpu)), flush=True)
         del step

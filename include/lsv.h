@@ -165,6 +165,22 @@ lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t
                               int32_t *argmax_opt, int32_t *accept_len, int32_t *committed, void *ws,
                               size_t ws_bytes, lsv_stream stream);
 
+/* Greedy verification with the verify logits produced by the verifier's output
+ * layer, inside the call (the logits are never written to memory):
+ *   hidden  [B*(K+1), H] bf16: the verifier's last hidden state of every verified
+ *           position, row b*(K+1)+j for sequence b, input position j (as for the
+ *           logit rows of spec_verify_accept)
+ *   w_vocab [V, H] bf16: the output layer; logit[r,v] = sum_h hidden[r,h] * w_vocab[v,h]
+ * The greedy token is the smallest v attaining the row maximum of the logits
+ * computed from the bf16 inputs with fp32 accumulation (tensor cores); the rule,
+ * drafts and outputs are those of spec_verify_accept.  Supported: H % 64 == 0,
+ * H <= 16384, 1 <= K+1 <= 64, V >= 1, B >= 0.  Device pointers, 16-byte aligned.
+ * ws: spec_verify_lmhead_workspace_size(B,K,V,H) bytes (0: unsupported shape). */
+size_t spec_verify_lmhead_workspace_size(int32_t B, int32_t K, int32_t V, int32_t H);
+lsv_status spec_verify_lmhead(const void *hidden, const void *w_vocab, const int32_t *drafts, int32_t B, int32_t K,
+                              int32_t V, int32_t H, int32_t *argmax_opt, int32_t *accept_len, int32_t *committed,
+                              void *ws, size_t ws_bytes, lsv_stream stream);
+
 /* spec_verify_accept without a workspace, for callers that cannot allocate
  * device memory when they verify: code that must not call cudaMalloc inside a
  * stream capture or a latency-critical decode loop, and plugin-style hosts

@@ -143,6 +143,31 @@ def spec_verify_accept(logits, drafts, ws, argmax=None, accept_len=None, committ
     return accept_len, committed
 
 
+def spec_verify_lmhead_workspace(B, K, V, H, device=None) -> torch.Tensor:
+    n = _ffi.load().spec_verify_lmhead_workspace_size(B, K, V, H)
+    if n == 0:
+        raise ValueError("unsupported verify shape")
+    return torch.empty(int(n), dtype=torch.uint8, device=device or "cuda")
+
+
+def spec_verify_lmhead(hidden, w_vocab, drafts, ws, K, argmax=None, accept_len=None, committed=None, stream=None):
+    """Greedy verification with the logits produced by the output layer w_vocab [V, H] from
+    hidden [B*(K+1), H] inside the call."""
+    _need(hidden, torch.bfloat16, "hidden"); _need(w_vocab, torch.bfloat16, "w_vocab"); _need(drafts, torch.int32, "drafts")
+    R, H = hidden.shape
+    V = w_vocab.shape[0]
+    if R % (K + 1):
+        raise ValueError("hidden rows must be B*(K+1)")
+    B = R // (K + 1)
+    dev = hidden.device
+    accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
+    committed = torch.empty((B, K + 1), dtype=torch.int32, device=dev) if committed is None else committed
+    check("spec_verify_lmhead", _ffi.load().spec_verify_lmhead(
+        _ptr(hidden), _ptr(w_vocab), _ptr(drafts), B, K, V, H, _ptr(argmax), _ptr(accept_len), _ptr(committed),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return accept_len, committed
+
+
 def spec_verify_accept_noalloc(logits, drafts, argmax=None, accept_len=None, committed=None, stream=None):
     """spec_verify_accept without a workspace: its scratch is a fixed array inside the library."""
     _need(logits, torch.bfloat16, "logits"); _need(drafts, torch.int32, "drafts")

@@ -274,8 +274,14 @@ cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int 
                    pv, pi);
   }
   if (e != cudaSuccess) return e;
-  return launch_pdl(accept_finalize_kernel, dim3(B), dim3(32 * min(K + 1, kFinWarps)), 0, s, (const float*)pv,
-                    (const int*)pi, nchunk, drafts, B, K, argmax, accept_len, committed);
+  return launch_accept_finalize(pv, pi, nchunk, drafts, B, K, argmax, accept_len, committed, s);
+}
+
+cudaError_t launch_accept_finalize(const float* pv, const int* pi, int nchunk, const int32_t* drafts, int B, int K,
+                                   int32_t* argmax, int32_t* accept_len, int32_t* committed, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  return launch_pdl(accept_finalize_kernel, dim3(B), dim3(32 * min(K + 1, kFinWarps)), 0, s, pv, pi, nchunk, drafts,
+                    B, K, argmax, accept_len, committed);
 }
 
 }  // namespace lsv

@@ -366,6 +366,33 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   return from_cuda(e);
 }
 
+size_t spec_verify_lmhead_workspace_size(int32_t B, int32_t K, int32_t V, int32_t H) {
+  if (B < 0 || K < 0 || K + 1 > kMaxVerifyRows || V <= 0 || H <= 0 || H % 64 || H > kMaxHidden) return 0;
+  if ((long long)B * (K + 1) >= (1ll << 31) || (long long)B * (K + 1) * ((V + 127) / 128) >= (1ll << 31)) return 0;
+  return lmhead_ws_bytes(B, K, V);
+}
+
+lsv_status spec_verify_lmhead(const void* hidden, const void* w_vocab, const int32_t* drafts, int32_t B, int32_t K,
+                              int32_t V, int32_t H, int32_t* argmax_opt, int32_t* accept_len, int32_t* committed,
+                              void* ws, size_t ws_bytes, lsv_stream stream) {
+  if (B < 0 || K < 0 || V <= 0 || H <= 0) return LSV_ERR_INVALID_ARG;
+  if (K + 1 > kMaxVerifyRows || H % 64 || H > kMaxHidden) return LSV_ERR_UNSUPPORTED;
+  const size_t need = spec_verify_lmhead_workspace_size(B, K, V, H);
+  if (need == 0) return LSV_ERR_UNSUPPORTED;
+  if (B == 0) return LSV_OK;
+  if (!hidden || !w_vocab || !accept_len || !committed || (K > 0 && !drafts)) return LSV_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(w_vocab) || !aligned16(drafts) || !aligned16(argmax_opt) ||
+      !aligned16(accept_len) || !aligned16(committed))
+    return LSV_ERR_MISALIGNED;
+  if (!ws || ws_bytes < need) return LSV_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LSV_ERR_MISALIGNED;
+  DeviceCtx* dc = nullptr;
+  if (device_ctx(&dc) != cudaSuccess) return LSV_ERR_CUDA;
+  return from_cuda(launch_lmhead_accept(static_cast<const bf16*>(hidden), static_cast<const bf16*>(w_vocab), drafts,
+                                        B, K, V, H, argmax_opt, accept_len, committed, ws, *dc,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t spec_verify_workspace_size(int32_t B, int32_t K, int32_t V) {
   if (B < 0 || K < 0 || K + 1 > kMaxVerifyRows || V <= 0) return 0;
   if ((long long)B * (K + 1) >= (1ll << 31)) return 0;

@@ -157,6 +157,15 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* 
 cudaError_t launch_rmsnorm_residual(bf16* x, const bf16* y, bf16* h, int T, int H, float eps, cudaStream_t s);
 
 size_t accept_ws_bytes(int B, int K, int V, int num_sms);
+// Reduce per-(row, chunk) (max, first index) partials [B*(K+1), nchunk] to greedy tokens and apply
+// the acceptance rule (one CTA per sequence).
+cudaError_t launch_accept_finalize(const float* pv, const int* pi, int nchunk, const int32_t* drafts, int B, int K,
+                                   int32_t* argmax, int32_t* accept_len, int32_t* committed, cudaStream_t s);
+// The verifier's output layer fused with the greedy-token search, then acceptance.
+size_t lmhead_ws_bytes(int B, int K, int V);
+cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const int32_t* drafts, int B, int K,
+                                 int V, int H, int32_t* argmax, int32_t* accept_len, int32_t* committed, void* ws,
+                                 const DeviceCtx& dc, cudaStream_t s);
 cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int K, int V, int32_t* argmax,
                           int32_t* accept_len, int32_t* committed, void* ws, const DeviceCtx& dc,
                           cudaStream_t s);

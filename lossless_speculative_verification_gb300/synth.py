@@ -311,3 +311,50 @@ def verify_problem(w: Workload, seed: int = 0):
     logits, planted = verify_logits(w.B, w.K, w.V, seed)
     drafts = draft_tokens(planted, w.V, w.accept, seed)
     return logits, planted, drafts
+
+
+# --------------------------------------------------------------------------- verifier output layer
+@dataclass
+class LmHeadProblem:
+    B: int
+    K: int
+    V: int
+    H: int
+    hidden: np.ndarray    # [B*(K+1), H] bf16 bits: the verifier's last hidden states
+    w_vocab: np.ndarray   # [V, H] bf16 bits
+    greedy: np.ndarray    # [B, K+1] greedy tokens as the caller's judge found them
+    drafts: np.ndarray    # [B, K] int32
+    redrawn: int
+
+
+def lmhead_problem(B: int, K: int, V: int = VOCAB, H: int = 1280, seed: int = 0, judge=None,
+                   accept=PAGE_ACCEPT, max_rounds: int = 200) -> LmHeadProblem:
+    """The verifier's output layer as the source of the verify logits.
+
+    w_vocab ~ N(0, 0.02) and hidden rows = RMSNorm(N(0, 1)), both in bf16.
+    judge(hidden, w_vocab) -> (greedy [R], ok [R]) comes from the caller (this module does
+    none of the method's arithmetic): rows it rejects are redrawn, and the drafts are drawn
+    from its greedy tokens with the conditional acceptances `accept`, as for the synthetic
+    logits.  Without a judge the greedy tokens are unknown and the drafts are uniform.
+    """
+    rs = streams(seed, 3)
+    w_vocab = np.empty((V, H), dtype=np.uint16)
+    for v0 in range(0, V, 16384):             # bounded float32 temporaries
+        w_vocab[v0:v0 + 16384] = _normal_bf16(rs[0], (min(16384, V - v0), H), 0.02)
+    hidden = hidden_rows(rs[1], B * (K + 1), H, "sphere")
+    redrawn = 0
+    greedy = np.zeros(B * (K + 1), np.int32)
+    if judge is not None:
+        for _ in range(max_rounds):
+            greedy, ok = judge(hidden, w_vocab)
+            bad = np.nonzero(~np.asarray(ok, bool))[0]
+            if bad.size == 0:
+                break
+            hidden[bad] = hidden_rows(rs[1], bad.size, H, "sphere")
+            redrawn += int(bad.size)
+        else:
+            raise RuntimeError("row predicate still failing after %d rounds" % max_rounds)
+    greedy = np.asarray(greedy, np.int32).reshape(B, K + 1)
+    probs = list(accept[:K]) + [accept[-1]] * max(0, K - len(accept))
+    drafts = draft_tokens(greedy, V, probs, seed + 7)
+    return LmHeadProblem(B, K, V, H, hidden, w_vocab, greedy, drafts, redrawn)

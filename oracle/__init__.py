@@ -18,6 +18,9 @@ Pins (checked by tests marked "not gpu"):
                 tokens, torch.argmax, greedy-decoding equivalence on a toy
                 model, closed form of tokens per step vs the pages' 2.73
   rmsnorm    -- closed form on constant rows, torch rms_norm in fp64
+  lmhead     -- pure-Python brute force on tiny inputs, a planted row that is a
+                scaled copy of the hidden state, duplicated rows (first index),
+                torch fp64 matmul + argmax
 """
 from __future__ import annotations
 
@@ -189,3 +192,64 @@ def accept(logits, drafts):
     committed = np.zeros((B, K1), np.int32)
     _check(_load().oracle_accept(_p(lg), _p(d), B, K, V, _p(argmax), _p(alen), _p(committed)), "accept")
     return argmax, alen, committed
+
+
+# ----------------------------------------------------------------------------- verifier output layer
+def lmhead_argmax(hidden, w_vocab, chunk=8192):
+    """Greedy tokens of the verifier's output layer, straight from its definition.
+
+    logit[r, v] = sum_h hidden[r, h] * w_vocab[v, h], evaluated in fp64 from the exact bf16
+    inputs (numpy's matmul is the only step taken from a library); g[r] = the first index
+    attaining the row maximum; gap[r] = that maximum minus the largest logit of any other
+    index (0 when the maximum is attained twice).  hidden [R, H], w_vocab [V, H] as bf16 bits.
+    """
+    hs = _c(hidden, np.uint16)
+    wv = _c(w_vocab, np.uint16)
+    R, H = hs.shape
+    V = wv.shape[0]
+    hf = _bf16_to_f64(hs)
+    best = np.full(R, -np.inf)
+    second = np.full(R, -np.inf)
+    g = np.zeros(R, np.int64)
+    for v0 in range(0, V, chunk):
+        lg = hf @ _bf16_to_f64(wv[v0:v0 + chunk]).T              # [R, n]
+        i = np.argmax(lg, axis=1)                                # first occurrence within the chunk
+        m = lg[np.arange(R), i]
+        lg[np.arange(R), i] = -np.inf
+        m2 = lg.max(axis=1)
+        # merge with the running (best, second): the earlier chunk wins ties (lower index)
+        new = m > best
+        second = np.where(new, np.maximum(best, m2), np.maximum(second, m))
+        g = np.where(new, v0 + i, g)
+        best = np.where(new, m, best)
+    return g.astype(np.int32), best - second
+
+
+def lmhead_judge(min_gap=1e-3):
+    """For the input generator: (greedy tokens, rows whose top-2 logits are >= min_gap apart)."""
+    def judge(hidden, w_vocab):
+        g, gap = lmhead_argmax(hidden, w_vocab)
+        return g, gap >= min_gap
+    return judge
+
+
+def _bf16_to_f64(u16):
+    return (np.asarray(u16, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def accept_from_greedy(greedy, drafts):
+    """The acceptance rule of `accept` applied to given greedy tokens greedy [B, K+1]."""
+    g = np.asarray(greedy, np.int64)
+    d = np.asarray(drafts, np.int64)
+    B, K1 = g.shape
+    K = K1 - 1
+    alen = np.zeros(B, np.int32)
+    committed = np.full((B, K1), -1, np.int32)
+    for b in range(B):
+        L = 0
+        while L < K and d[b, L] == g[b, L]:
+            L += 1
+        alen[b] = L
+        committed[b, :L] = d[b, :L]
+        committed[b, L] = g[b, L]
+    return alen, committed

@@ -83,6 +83,13 @@ def test_argument_errors_return_before_any_launch(lib):
     assert lib.spec_verify_accept(None, p16, 4, 3, 1024, None, p16, p16, p16, 1 << 20, None) == 1
     assert lib.spec_verify_accept(p_odd, p16, 4, 3, 1024, None, p16, p16, p16, 1 << 20, None) == 3
     assert lib.rmsnorm_residual(p16, p16, None, 4, 256, 1e-6, None) == 1
+    # verifier output layer: unsupported hidden width, missing input, misaligned, empty batch
+    assert lib.spec_verify_lmhead_workspace_size(4, 3, 1000, 250) == 0
+    assert lib.spec_verify_lmhead(p16, p16, p16, 4, 3, 1000, 250, None, p16, p16, p16, 1 << 20, None) == 2
+    assert lib.spec_verify_lmhead(None, p16, p16, 4, 3, 1000, 256, None, p16, p16, p16, 1 << 20, None) == 1
+    assert lib.spec_verify_lmhead(p_odd, p16, p16, 4, 3, 1000, 256, None, p16, p16, p16, 1 << 20, None) == 3
+    assert lib.spec_verify_lmhead(p16, p16, p16, 4, 3, 1000, 256, None, p16, p16, p16, 16, None) == 4
+    assert lib.spec_verify_lmhead(None, None, None, 0, 3, 1000, 256, None, None, None, None, 0, None) == 0
     assert lib.lsv_set_wait_limit_ns(0) == 1
     assert lib.lsv_selftest_wait_timeout(0, None) == 1
     # empty work is a no-op that succeeds without a device

@@ -363,3 +363,73 @@ def test_rmsnorm_residual_closed_form_and_torch():
     np.testing.assert_allclose(xn, val64(bits(val64(x) + val64(y))), rtol=0, atol=0)
     ref = F.rms_norm(torch.from_numpy(xn), (H,), eps=1e-6).numpy()
     np.testing.assert_allclose(hn, ref, rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------- verifier output layer
+def _lmhead_brute(hidden, w_vocab):
+    """Pure-Python definition: every logit by a plain sum, then a scan in increasing index."""
+    hs, wv = val64(hidden), val64(w_vocab)
+    g, gap = [], []
+    for r in range(hs.shape[0]):
+        lg = [sum(float(hs[r, h]) * float(wv[v, h]) for h in range(hs.shape[1])) for v in range(wv.shape[0])]
+        best = 0
+        for v in range(1, len(lg)):
+            if lg[v] > lg[best]:
+                best = v
+        g.append(best)
+        gap.append(lg[best] - max(lg[v] for v in range(len(lg)) if v != best))
+    return np.array(g), np.array(gap)
+
+
+@pytest.mark.parametrize("chunk", [5, 7, 1000])
+def test_lmhead_argmax_brute_force(chunk):
+    rs = np.random.default_rng(11)
+    # small integers: exact products, frequent exact ties between different rows
+    hidden = bits(rs.integers(-2, 3, size=(6, 5)))
+    w_vocab = bits(rs.integers(-2, 3, size=(37, 5)))
+    # a later copy of row 0's winning row: a tie at the maximum, which the first index wins
+    w_vocab[36] = w_vocab[_lmhead_brute(hidden, w_vocab)[0][0]]
+    g, gap = oracle.lmhead_argmax(hidden, w_vocab, chunk=chunk)
+    rg, rgap = _lmhead_brute(hidden, w_vocab)
+    np.testing.assert_array_equal(g, rg)
+    np.testing.assert_allclose(gap, rgap, rtol=0, atol=1e-12)
+    assert gap[0] == 0 and g[0] != 36
+
+
+def test_lmhead_argmax_planted_and_duplicates():
+    rs = np.random.default_rng(12)
+    H, V = 64, 300
+    hidden = bits(rs.standard_normal((3, H)))
+    w_vocab = bits(rs.standard_normal((V, H)) * 0.02)
+    # row 17 is twice hidden row 0: by Cauchy-Schwarz it beats every small random row
+    w_vocab[17] = bits(2.0 * val64(hidden[0]))
+    # rows 40 and 200 are the same large copy of hidden row 1: the lower index wins, gap 0
+    w_vocab[40] = bits(3.0 * val64(hidden[1]))
+    w_vocab[200] = w_vocab[40]
+    g, gap = oracle.lmhead_argmax(hidden, w_vocab, chunk=64)
+    assert g[0] == 17 and gap[0] > 0
+    assert g[1] == 40 and gap[1] == 0
+
+
+def test_lmhead_argmax_matches_torch():
+    rs = np.random.default_rng(13)
+    H, V = 128, 5000
+    hidden = bits(rs.standard_normal((8, H)))
+    w_vocab = bits(rs.standard_normal((V, H)) * 0.02)
+    g, gap = oracle.lmhead_argmax(hidden, w_vocab, chunk=999)
+    lg = torch.from_numpy(val64(hidden)) @ torch.from_numpy(val64(w_vocab)).T
+    np.testing.assert_array_equal(g, torch.argmax(lg, dim=1).numpy())
+    top2 = torch.topk(lg, 2, dim=1).values
+    np.testing.assert_allclose(gap, (top2[:, 0] - top2[:, 1]).numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_accept_from_greedy_matches_accept():
+    # the rule on given greedy tokens equals the C oracle's rule on logits whose greedy tokens they are
+    for seed in range(5):
+        B, K, V = 50, 3, 16
+        logits, planted = synth.verify_logits(B, K, V, seed)
+        drafts = synth.draft_tokens(planted, V, [0.7, 0.6, 0.5], seed)
+        g, alen, comm = oracle.accept(logits, drafts)
+        alen2, comm2 = oracle.accept_from_greedy(g, drafts)
+        np.testing.assert_array_equal(alen, alen2)
+        np.testing.assert_array_equal(comm, comm2)
