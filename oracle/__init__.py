@@ -21,6 +21,10 @@ Pins (checked by tests marked "not gpu"):
   lmhead     -- pure-Python brute force on tiny inputs, a planted row that is a
                 scaled copy of the hidden state, duplicated rows (first index),
                 torch fp64 matmul + argmax
+  attention  -- pure-Python brute force, one visible key (the output is its
+                value), identical keys (the mean of the values), causality
+                (later keys change nothing), torch scaled_dot_product_attention
+                in fp64 with an explicit mask
 """
 from __future__ import annotations
 
@@ -253,3 +257,33 @@ def accept_from_greedy(greedy, drafts):
         committed[b, :L] = d[b, :L]
         committed[b, L] = g[b, L]
     return alen, committed
+
+
+# ----------------------------------------------------------------------------- verify attention
+def verify_attention(q, k_cache, v_cache, ctx_len, scale):
+    """Causal attention of the Q verified positions over their sequence's cache, from its
+    definition, in fp64 from the exact bf16 inputs.
+
+    q [B, Q, nh, d]; k_cache, v_cache [B, L, nh, d] (bf16 bits); ctx_len [B]: cache entries of
+    sequence b, the last Q of which belong to the verified positions.  Query j of sequence b
+    sits at position p = ctx_len[b] - Q + j and sees keys 0..p:
+        out[b, j, h] = sum_{t <= p} softmax_t(scale * q[b,j,h] . k[b,t,h]) * v[b,t,h]
+    Returns out [B, Q, nh, d] float64.
+    """
+    qf = _bf16_to_f64(_c(q, np.uint16))
+    kf = _bf16_to_f64(_c(k_cache, np.uint16))
+    vf = _bf16_to_f64(_c(v_cache, np.uint16))
+    B, Q, nh, d = qf.shape
+    out = np.zeros((B, Q, nh, d), np.float64)
+    for b in range(B):
+        n = int(ctx_len[b])
+        if n < Q or n > kf.shape[1]:
+            raise ValueError("ctx_len[%d] = %d outside [Q, L]" % (b, n))
+        for j in range(Q):
+            p = n - Q + j
+            s = np.einsum("hd,thd->ht", qf[b, j], kf[b, :p + 1]) * scale     # [nh, p+1]
+            s -= s.max(axis=1, keepdims=True)
+            w = np.exp(s)
+            w /= w.sum(axis=1, keepdims=True)
+            out[b, j] = np.einsum("ht,thd->hd", w, vf[b, :p + 1])
+    return out

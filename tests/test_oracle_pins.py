@@ -433,3 +433,69 @@ def test_accept_from_greedy_matches_accept():
         alen2, comm2 = oracle.accept_from_greedy(g, drafts)
         np.testing.assert_array_equal(alen, alen2)
         np.testing.assert_array_equal(comm, comm2)
+
+
+# ----------------------------------------------------------------------------- verify attention
+def _attn_problem(B=2, Q=3, L=9, nh=2, d=4, seed=0, lens=(9, 5)):
+    rs = np.random.default_rng(seed)
+    q = bits(rs.standard_normal((B, Q, nh, d)))
+    k = bits(rs.standard_normal((B, L, nh, d)))
+    v = bits(rs.standard_normal((B, L, nh, d)))
+    return q, k, v, np.array(lens[:B], np.int32)
+
+
+def test_attention_brute_force():
+    q, k, v, n = _attn_problem()
+    scale = 0.5
+    out = oracle.verify_attention(q, k, v, n, scale)
+    qf, kf, vf = val64(q), val64(k), val64(v)
+    B, Q, nh, d = qf.shape
+    for b in range(B):
+        for j in range(Q):
+            p = int(n[b]) - Q + j
+            for h in range(nh):
+                s = [scale * sum(float(qf[b, j, h, c]) * float(kf[b, t, h, c]) for c in range(d)) for t in range(p + 1)]
+                m = max(s)
+                e = [math.exp(x - m) for x in s]
+                z = sum(e)
+                ref = [sum(e[t] / z * float(vf[b, t, h, c]) for t in range(p + 1)) for c in range(d)]
+                np.testing.assert_allclose(out[b, j, h], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_special_cases():
+    # a sequence whose cache holds only its Q positions: query 0 sees key 0 alone (output = v_0);
+    # identical keys: uniform weights, the mean of the visible values
+    q, k, v, _ = _attn_problem(B=1, Q=3, L=6, lens=(3,))
+    out = oracle.verify_attention(q, k, v, np.array([3], np.int32), 0.7)
+    np.testing.assert_allclose(out[0, 0], val64(v[0, 0]), rtol=0, atol=0)
+    k2 = k.copy()
+    k2[0, :, :, :] = k[0, 0]
+    out2 = oracle.verify_attention(q, k2, v, np.array([6], np.int32), 0.7)
+    for j in range(3):
+        np.testing.assert_allclose(out2[0, j], val64(v[0, :4 + j]).mean(axis=0), rtol=1e-12)
+
+
+def test_attention_is_causal():
+    q, k, v, n = _attn_problem(B=1, L=9, lens=(9,))
+    out = oracle.verify_attention(q, k, v, n, 0.5)
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 8] = bits(np.full((2, 4), 9.0))     # the last key: seen only by the last query
+    v2[0, 8] = bits(np.full((2, 4), -9.0))
+    out2 = oracle.verify_attention(q, k2, v2, n, 0.5)
+    np.testing.assert_array_equal(out[0, :2], out2[0, :2])
+    assert not np.allclose(out[0, 2], out2[0, 2])
+
+
+def test_attention_matches_torch_sdpa():
+    q, k, v, n = _attn_problem(B=2, Q=4, L=40, nh=3, d=16, seed=3, lens=(40, 17))
+    scale = 0.25
+    out = oracle.verify_attention(q, k, v, n, scale)
+    for b in range(2):
+        L = int(n[b])
+        qt = torch.from_numpy(val64(q[b])).permute(1, 0, 2)          # [nh, Q, d]
+        kt = torch.from_numpy(val64(k[b, :L])).permute(1, 0, 2)      # [nh, L, d]
+        vt = torch.from_numpy(val64(v[b, :L])).permute(1, 0, 2)
+        pos = torch.arange(L - 4, L)[:, None]
+        mask = torch.arange(L)[None, :] <= pos                      # [Q, L]
+        ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+        np.testing.assert_allclose(out[b], ref.permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
