@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack", "lmhead"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack", "lmhead", "attention"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed oracle sample (for profiler runs; the line then has no cpu_baseline)")
@@ -370,6 +370,10 @@ class LmHeadStep:
         step.problem = synth.lmhead_problem(cls.B, cls.K, V=cls.V, H=cls.H, seed=seed, judge=oracle.lmhead_judge())
         return step
 
+    def describe(self):
+        return ("greedy verification of [%d,%d] positions with the logits made by the output layer [%d,%d] "
+                "inside the call (B=%d, K=%d)" % (self.B, self.K + 1, self.V, self.H, self.B, self.K))
+
     def layer(self):
         pass
 
@@ -432,6 +436,110 @@ def lmhead_oracle_sampler(step):
                           "search, plus the acceptance of their sequences, %.1f s" % (n, step.T, dt)}
 
     return sample
+
+
+class AttentionStep:
+    """Causal attention of the verified positions over their sequences' caches
+    (spec_verify_attention): 32 sequences x (K=3)+1 positions, 10 heads x 128, page-shaped
+    prefixes (visual tokens + the page's text so far).  Same interface as LmHeadStep."""
+
+    B, Q, NH, D = 32, 4, 10, 128
+
+    def __init__(self, seed, dev):
+        import torch
+        from lossless_speculative_verification_gb300 import api, synth
+        self.name, self.dev, self.api = "attention", dev, api
+        self.w = None
+        self.layers = []
+        self.T = self.B * self.Q
+        p = self.problem = synth.attention_problem(self.B, self.Q, nh=self.NH, d=self.D, seed=seed)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        self.q, self.k_cache, self.v_cache = t(p.q), t(p.k_cache), t(p.v_cache)
+        self.ctx_len = torch.from_numpy(p.ctx_len).to(dev)
+        self.ws = api.spec_verify_attention_workspace(self.B, self.Q, p.L, self.NH, self.D, dev)
+        self.out = torch.empty_like(self.q)
+        self.launches = 2  # the split-cache pass, then the combine of the splits
+
+    @classmethod
+    def host_only(cls, seed):
+        from lossless_speculative_verification_gb300 import synth
+        step = cls.__new__(cls)
+        step.T = cls.B * cls.Q
+        step.problem = synth.attention_problem(cls.B, cls.Q, nh=cls.NH, d=cls.D, seed=seed)
+        return step
+
+    def describe(self):
+        p = self.problem
+        return ("causal attention of [%d,%d] verified positions (%d heads x %d) over bf16 caches of %d..%d "
+                "entries (mean %.0f, capacity %d)" % (self.B, self.Q, self.NH, self.D, p.ctx_len.min(),
+                                                      p.ctx_len.max(), p.ctx_len.mean(), p.L))
+
+    def layer(self):
+        pass
+
+    def accept(self):
+        self.api.spec_verify_attention(self.q, self.k_cache, self.v_cache, self.ctx_len, self.ws, out=self.out)
+
+    def check(self):
+        """Sampled sequences against the oracle (the parity tests cover the whole batch)."""
+        import oracle
+        from lossless_speculative_verification_gb300 import synth
+        p = self.problem
+        got = self.out.float().cpu().numpy()
+        for b in (0, self.B // 2, self.B - 1):
+            ref = oracle.verify_attention(p.q[b:b + 1], p.k_cache[b:b + 1], p.v_cache[b:b + 1], p.ctx_len[b:b + 1],
+                                          1.0 / np.sqrt(self.D))
+            err = np.abs(got[b:b + 1] - ref).max()
+            assert err <= 2e-2, ("attention sample", b, err)
+
+    def bytes_and_flops(self):
+        p = self.problem
+        kv = int(p.ctx_len.astype(np.int64).sum()) * self.NH * self.D * 2 * 2
+        byts = kv + 2 * self.T * self.NH * self.D * 2 + self.B * 4
+        flops = 4.0 * self.Q * self.NH * self.D * float(p.ctx_len.astype(np.int64).sum())
+        return byts, flops, 0
+
+    def setup_e2e(self):
+        import torch
+        self.h_q = self.q.cpu().pin_memory()
+        self.h_len = self.ctx_len.cpu().pin_memory()
+        self.d_q, self.d_len = torch.empty_like(self.q), torch.empty_like(self.ctx_len)
+        self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
+        return self.h_q.numel() * 2 + self.h_len.numel() * 4, self.h_out.numel() * 2
+
+    def e2e(self):
+        self.d_q.copy_(self.h_q, non_blocking=True)
+        self.d_len.copy_(self.h_len, non_blocking=True)
+        self.api.spec_verify_attention(self.d_q, self.k_cache, self.v_cache, self.d_len, self.ws, out=self.out)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+def attention_oracle_sampler(step):
+    """The oracle's attention (numpy fp64 einsum) on whole sequences, cycling over the batch."""
+    import oracle
+    p = step.problem
+    state = {"n": 0}
+
+    def sample(seconds):
+        n0 = state["n"]
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            b = state["n"] % p.B
+            oracle.verify_attention(p.q[b:b + 1], p.k_cache[b:b + 1], p.v_cache[b:b + 1], p.ctx_len[b:b + 1],
+                                    1.0 / np.sqrt(p.d))
+            state["n"] += 1
+        dt = time.perf_counter() - t0
+        n = state["n"] - n0
+        return {"value": n * p.Q / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                "kind": "oracle (numpy fp64 einsum; its BLAS may use every core)",
+                "sample": "%d sequences x %d verified positions (cycling over the %d) through the oracle's "
+                          "attention, %.1f s" % (n, p.Q, p.B, dt)}
+
+    return sample
+
+
+# workloads outside the MoE layer: name -> (step class, oracle sampler)
+SIDE_STEPS = {"lmhead": (LmHeadStep, lmhead_oracle_sampler), "attention": (AttentionStep, attention_oracle_sampler)}
 
 
 def flush_l2(flush, i):
@@ -576,12 +684,14 @@ def result_line(args, step, m, world, cpu):
     w = step.w
     byts, flops, acc_bytes = step.bytes_and_flops()
     khash = layer_source_hash()
-    if step.name == "lmhead":
+    if step.name in SIDE_STEPS:
         achieved = byts / (m["total_ms"] / args.steps / 1e3) / 1e9
+        kernel = ("lmhead_argmax_kernel (tcgen05 product of the output layer and the hidden rows, reduced "
+                  "to each row's (max, first index) per 128-token vocabulary tile) + accept_finalize_kernel"
+                  if step.name == "lmhead" else
+                  "attn_split_kernel (512 cached positions per CTA, online softmax in fp32) + attn_combine_kernel")
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "algorithmic_bytes": byts, "algorithmic_flops": flops,
-                "kernel": "lmhead_argmax_kernel (tcgen05 product of the output layer and the hidden rows, reduced "
-                          "to each row's (max, first index) per 128-token vocabulary tile) + accept_finalize_kernel",
+                "algorithmic_bytes": byts, "algorithmic_flops": flops, "kernel": kernel,
                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}
     elif step.name == "prefill":
         achieved = flops / (m["layer_ms"] / 1e3) / 1e12
@@ -591,7 +701,7 @@ def result_line(args, step, m, world, cpu):
         achieved = byts / (m["layer_ms"] / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts}
-    if step.name != "lmhead":
+    if step.name not in SIDE_STEPS:
         roof.update({"kernel": "moe_verify_layer x%d: router, permute+gather, grouped SwiGLU experts (tcgen05), "
                                "combine; one PDL-chained launch sequence per layer" % len(step.layers),
                      "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "layer_ms": m["layer_ms"],
@@ -605,9 +715,7 @@ def result_line(args, step, m, world, cpu):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["total_ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "%s: %s" % (step.name, describe(w, len(step.layers)) if w is not None else
-                                           "greedy verification of [%d,%d] positions with the logits made by the "
-                                           "output layer [%d,%d] inside the call (B=%d, K=%d)"
-                                           % (step.B, step.K + 1, step.V, step.H, step.B, step.K)),
+                                           step.describe()),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MB written, then read back, outside the events)",
                    "timing": ("step replayed as one CUDA graph with CUDA events recorded as graph nodes at its "
@@ -629,8 +737,8 @@ def result_line(args, step, m, world, cpu):
 
 def workloads(name):
     from lossless_speculative_verification_gb300 import synth
-    if name == "lmhead":
-        return [("lmhead", None, 0)]
+    if name in SIDE_STEPS:
+        return [(name, None, 0)]
     if name == "sweep":
         return [("sweep", synth.sweep_workload(B, K), synth.sweep_seed(B, K))
                 for B in synth.SWEEP_B for K in synth.SWEEP_K]
@@ -689,11 +797,11 @@ def run_reference(args, rank, world):
         return
     for name, w, seed in workloads(args.workload):
         per_step = 2.0 if name != "sweep" else 0.5       # seconds of oracle work per timed step
-        if name == "lmhead":
-            step = LmHeadStep.host_only(seed + args.seed)
-            sample = lmhead_oracle_sampler(step)
-            w_desc = "greedy verification of [%d,%d] positions through the output layer [%d,%d]" % (
-                step.B, step.K + 1, step.V, step.H)
+        if name in SIDE_STEPS:
+            cls, sampler = SIDE_STEPS[name]
+            step = cls.host_only(seed + args.seed)
+            sample = sampler(step)
+            w_desc = step.describe()
         else:
             sample = oracle_sampler(w, seed + args.seed)
             w_desc = describe(w, w.layers)
@@ -728,16 +836,16 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for name, w, seed in workloads(args.workload):
-        if name == "lmhead":
-            step = LmHeadStep(seed + args.seed + 1000 * rank, dev)
+        if name in SIDE_STEPS:
+            step = SIDE_STEPS[name][0](seed + args.seed + 1000 * rank, dev)
         else:
             step = DeviceStep(name, w, seed + args.seed + 1000 * rank, dev)
         m = measure(step, args, local, world, flush, dist)
-        if name == "lmhead":
+        if name in SIDE_STEPS:
             step.check()
         cpu = None
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            sampler = lmhead_oracle_sampler(step) if name == "lmhead" else oracle_sampler(w, seed + args.seed)
+            sampler = SIDE_STEPS[name][1](step) if name in SIDE_STEPS else oracle_sampler(w, seed + args.seed)
             cpu = sampler(12.0 if args.workload != "sweep" else 2.0)
         if rank == 0:
             print(json.dumps(result_line(args, step, m, world, cpu)), flush=True)

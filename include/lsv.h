@@ -165,6 +165,25 @@ lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t
                               int32_t *argmax_opt, int32_t *accept_len, int32_t *committed, void *ws,
                               size_t ws_bytes, lsv_stream stream);
 
+/* Causal attention of the verified positions over their sequences' caches
+ * (the verify pass presents every sequence's K+1 positions at once):
+ *   q       [B, Q, nh, d] bf16: queries of the Q = K+1 verified positions
+ *   k_cache [B, L, nh, d] bf16, v_cache [B, L, nh, d] bf16: per-sequence caches of
+ *           capacity L; entries 0..ctx_len[b]-1 are valid and the last Q of them
+ *           belong to the verified positions themselves
+ *   ctx_len [B] int32 (device): Q <= ctx_len[b] <= L
+ *   out     [B, Q, nh, d] bf16:
+ *     out[b,j,h] = sum_{t <= p} softmax_t(scale * q[b,j,h].k[b,t,h]) v[b,t,h],
+ *     p = ctx_len[b] - Q + j (query j sees the cache up to and including itself)
+ * fp32 scores and accumulation.  Supported: d in {64, 128}, 1 <= Q <= 8,
+ * B, nh <= 65535, scale > 0.  A ctx_len outside [Q, L] raises
+ * LSV_ERR_DEVICE_INDEX (that sequence's output is zero).
+ * ws: spec_verify_attention_workspace_size(B,Q,L,nh,d) bytes (0: unsupported). */
+size_t spec_verify_attention_workspace_size(int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d);
+lsv_status spec_verify_attention(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
+                                 int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d, float scale, void *out,
+                                 void *ws, size_t ws_bytes, lsv_stream stream);
+
 /* Greedy verification with the verify logits produced by the verifier's output
  * layer, inside the call (the logits are never written to memory):
  *   hidden  [B*(K+1), H] bf16: the verifier's last hidden state of every verified

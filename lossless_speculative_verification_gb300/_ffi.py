@@ -48,6 +48,8 @@ SIGNATURES = {
     "spec_verify_accept": (I32, [P, P, I32, I32, I32, P, P, P, P, SZ, P]),
     "spec_verify_accept_noalloc": (I32, [P, P, I32, I32, I32, P, P, P, P]),
     "spec_verify_lmhead_workspace_size": (SZ, [I32, I32, I32, I32]),
+    "spec_verify_attention_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
+    "spec_verify_attention": (I32, [P, P, P, P, I32, I32, I32, I32, I32, ctypes.c_float, P, P, SZ, P]),
     "spec_verify_lmhead": (I32, [P, P, P, I32, I32, I32, I32, P, P, P, P, SZ, P]),
     "rmsnorm_residual": (I32, [P, P, P, I32, I32, ctypes.c_float, P]),
     "lsv_get_device_error": (I32, [ctypes.POINTER(I32), P]),

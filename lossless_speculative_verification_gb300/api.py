@@ -8,6 +8,7 @@ computation runs in the library's kernels.  Workspaces are passed explicitly
 from __future__ import annotations
 
 import ctypes
+import math
 
 import torch
 
@@ -141,6 +142,27 @@ def spec_verify_accept(logits, drafts, ws, argmax=None, accept_len=None, committ
         _ptr(logits), _ptr(drafts), B, K, V, _ptr(argmax), _ptr(accept_len), _ptr(committed), _ptr(ws),
         ws.numel(), _stream(stream)))
     return accept_len, committed
+
+
+def spec_verify_attention_workspace(B, Q, L, nh, d, device=None) -> torch.Tensor:
+    n = _ffi.load().spec_verify_attention_workspace_size(B, Q, L, nh, d)
+    if n == 0:
+        raise ValueError("unsupported attention shape")
+    return torch.empty(int(n), dtype=torch.uint8, device=device or "cuda")
+
+
+def spec_verify_attention(q, k_cache, v_cache, ctx_len, ws, scale=None, out=None, stream=None):
+    """Causal attention of the verified positions q [B, Q, nh, d] over the caches [B, L, nh, d]."""
+    _need(q, torch.bfloat16, "q"); _need(k_cache, torch.bfloat16, "k_cache"); _need(v_cache, torch.bfloat16, "v_cache")
+    _need(ctx_len, torch.int32, "ctx_len")
+    B, Q, nh, d = q.shape
+    L = k_cache.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    check("spec_verify_attention", _ffi.load().spec_verify_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(ctx_len), B, Q, L, nh, d, scale, _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out
 
 
 def spec_verify_lmhead_workspace(B, K, V, H, device=None) -> torch.Tensor:

@@ -366,6 +366,34 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
   return from_cuda(e);
 }
 
+size_t spec_verify_attention_workspace_size(int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d) {
+  if (B < 0 || Q < 1 || Q > kMaxAttnQ || L < Q || nh < 1 || (d != 64 && d != 128)) return 0;
+  if ((long long)B * L * nh * d >= (1ll << 40) || (long long)B * nh >= 65535ll * 65535ll || nh > 65535 ||
+      B > 65535)
+    return 0;
+  return attention_ws_bytes(B, Q, L, nh, d);
+}
+
+lsv_status spec_verify_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
+                                 int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d, float scale, void* out,
+                                 void* ws, size_t ws_bytes, lsv_stream stream) {
+  if (B < 0 || Q < 1 || L < 1 || nh < 1 || d < 1 || !(scale > 0.f) || !std::isfinite(scale))
+    return LSV_ERR_INVALID_ARG;
+  const size_t need = spec_verify_attention_workspace_size(B, Q, L, nh, d);
+  if (need == 0) return LSV_ERR_UNSUPPORTED;
+  if (B == 0) return LSV_OK;
+  if (!q || !k_cache || !v_cache || !ctx_len || !out) return LSV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(ctx_len) || !aligned16(out))
+    return LSV_ERR_MISALIGNED;
+  if (!ws || ws_bytes < need) return LSV_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LSV_ERR_MISALIGNED;
+  DeviceCtx* dc = nullptr;
+  if (device_ctx(&dc) != cudaSuccess) return LSV_ERR_CUDA;
+  return from_cuda(launch_attention(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
+                                    static_cast<const bf16*>(v_cache), ctx_len, B, Q, L, nh, d, scale,
+                                    static_cast<bf16*>(out), ws, *dc, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t spec_verify_lmhead_workspace_size(int32_t B, int32_t K, int32_t V, int32_t H) {
   if (B < 0 || K < 0 || K + 1 > kMaxVerifyRows || V <= 0 || H <= 0 || H % 64 || H > kMaxHidden) return 0;
   if ((long long)B * (K + 1) >= (1ll << 31) || (long long)B * (K + 1) * ((V + 127) / 128) >= (1ll << 31)) return 0;

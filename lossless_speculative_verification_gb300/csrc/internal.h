@@ -20,6 +20,7 @@ constexpr int kMaxTopK = 8;
 constexpr int kMaxShared = 8;
 constexpr int kMaxHidden = 16384;
 constexpr int kMaxVerifyRows = 64;  // K + 1 per sequence
+constexpr int kMaxAttnQ = 8;        // verified positions per sequence in the attention
 
 // Per-device state: the error word's device address and the SM count.
 struct DeviceCtx {
@@ -161,6 +162,12 @@ size_t accept_ws_bytes(int B, int K, int V, int num_sms);
 // the acceptance rule (one CTA per sequence).
 cudaError_t launch_accept_finalize(const float* pv, const int* pi, int nchunk, const int32_t* drafts, int B, int K,
                                    int32_t* argmax, int32_t* accept_len, int32_t* committed, cudaStream_t s);
+// Causal attention of Q verified positions per sequence over the cache.
+int attention_splits(int L);
+size_t attention_ws_bytes(int B, int Q, int L, int nh, int d);
+cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, const int32_t* ctx_len, int B, int Q,
+                             int L, int nh, int d, float scale, bf16* out, void* ws, const DeviceCtx& dc,
+                             cudaStream_t s);
 // The verifier's output layer fused with the greedy-token search, then acceptance.
 size_t lmhead_ws_bytes(int B, int K, int V);
 cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const int32_t* drafts, int B, int K,

@@ -358,3 +358,58 @@ def lmhead_problem(B: int, K: int, V: int = VOCAB, H: int = 1280, seed: int = 0,
     probs = list(accept[:K]) + [accept[-1]] * max(0, K - len(accept))
     drafts = draft_tokens(greedy, V, probs, seed + 7)
     return LmHeadProblem(B, K, V, H, hidden, w_vocab, greedy, drafts, redrawn)
+
+
+# --------------------------------------------------------------------------- verify attention
+# Decoder prefix of a page: 256 visual tokens for the 1024x1024 view plus up to nine local
+# tiles of 100 tokens (at most 1,156), then the page's text so far (about 1,085 output tokens
+# per page); jina-ocr-v1 coverage on kg.zhiyong.dev, "The first layer is the visual input" and
+# the throughput paragraph.
+VISUAL_BASE, VISUAL_TILE, VISUAL_MAX_TILES = 256, 100, 9
+PAGE_TEXT_TOKENS = 1_085
+ATTN_HEADS, ATTN_HEAD_DIM = 10, 128   # hidden 1280 = 10 heads x 128
+
+
+@dataclass
+class AttentionProblem:
+    B: int
+    Q: int
+    L: int
+    nh: int
+    d: int
+    q: np.ndarray         # [B, Q, nh, d] bf16 bits
+    k_cache: np.ndarray   # [B, L, nh, d] bf16 bits
+    v_cache: np.ndarray   # [B, L, nh, d] bf16 bits
+    ctx_len: np.ndarray   # [B] int32, Q <= ctx_len <= L
+
+
+def page_context_lengths(rng, B: int, Q: int) -> np.ndarray:
+    """Cache entries per sequence in the verify pass: the visual prefix (256 + 100 x a uniform
+    number of tiles in 0..9), a uniform point of the page's ~1,085 text tokens, and the Q
+    verified positions themselves."""
+    vis = VISUAL_BASE + VISUAL_TILE * rng.integers(0, VISUAL_MAX_TILES + 1, size=B)
+    txt = rng.integers(0, PAGE_TEXT_TOKENS + 1, size=B)
+    return (vis + txt + Q).astype(np.int32)
+
+
+def page_cache_capacity(Q: int, align: int = 64) -> int:
+    n = VISUAL_BASE + VISUAL_TILE * VISUAL_MAX_TILES + PAGE_TEXT_TOKENS + Q
+    return (n + align - 1) // align * align
+
+
+def attention_problem(B: int, Q: int, nh: int = ATTN_HEADS, d: int = ATTN_HEAD_DIM, L: int | None = None,
+                      ctx_len=None, seed: int = 0, qk_std: float = 1.0) -> AttentionProblem:
+    """q, k ~ N(0, qk_std) and v ~ N(0, 1) in bf16 (at scale 1/sqrt(d) the scores have a standard
+    deviation of about qk_std^2).  The cache past each sequence's length holds the same draws; the
+    attention must not read it.
+    ctx_len defaults to the page recipe above and L to its capacity."""
+    rs = streams(seed, 4)
+    if ctx_len is None:
+        ctx_len = page_context_lengths(rs[3], B, Q)
+    ctx_len = np.asarray(ctx_len, np.int32)
+    if L is None:
+        L = page_cache_capacity(Q)
+    q = _normal_bf16(rs[0], (B, Q, nh, d), qk_std)
+    k = _normal_bf16(rs[1], (B, L, nh, d), qk_std)
+    v = _normal_bf16(rs[2], (B, L, nh, d), 1.0)
+    return AttentionProblem(B, Q, L, nh, d, q, k, v, ctx_len)

@@ -90,6 +90,20 @@ def test_argument_errors_return_before_any_launch(lib):
     assert lib.spec_verify_lmhead(p_odd, p16, p16, 4, 3, 1000, 256, None, p16, p16, p16, 1 << 20, None) == 3
     assert lib.spec_verify_lmhead(p16, p16, p16, 4, 3, 1000, 256, None, p16, p16, p16, 16, None) == 4
     assert lib.spec_verify_lmhead(None, None, None, 0, 3, 1000, 256, None, None, None, None, 0, None) == 0
+    # attention: d outside {64, 128} and Q above 8 are unsupported; null, misaligned, small workspace
+    assert lib.spec_verify_attention_workspace_size(4, 4, 1024, 10, 96) == 0
+    assert lib.spec_verify_attention_workspace_size(4, 9, 1024, 10, 128) == 0
+    assert lib.spec_verify_attention_workspace_size(4, 4, 3, 10, 128) == 0
+    need = lib.spec_verify_attention_workspace_size(4, 4, 1024, 10, 128)
+    assert need >= 4 * 10 * 2 * 4 * (128 * 4 + 8)
+    att = lambda q, B, Q, d, scale, ws_bytes: lib.spec_verify_attention(q, p16, p16, p16, B, Q, 1024, 10, d, scale,
+                                                                        p16, p16, ws_bytes, None)
+    assert att(p16, 4, 4, 96, 0.1, need) == 2
+    assert att(p16, 4, 4, 128, 0.0, need) == 1
+    assert att(None, 4, 4, 128, 0.1, need) == 1
+    assert att(p_odd, 4, 4, 128, 0.1, need) == 3
+    assert att(p16, 4, 4, 128, 0.1, need - 1) == 4
+    assert lib.spec_verify_attention(None, None, None, None, 0, 4, 1024, 10, 128, 0.1, None, None, 0, None) == 0
     assert lib.lsv_set_wait_limit_ns(0) == 1
     assert lib.lsv_selftest_wait_timeout(0, None) == 1
     # empty work is a no-op that succeeds without a device
