@@ -141,9 +141,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def layer_source_hash():
+# per workload: the sources its kernels come from, and the first and last kernel of one step
+STEP_SOURCES = {
+    "layer": ("ffn.cu", "ptx.cuh", "route.cu", "permute.cu", "combine.cu", "ffn_plan.cuh", "api.cu", "tmap.h"),
+    "lmhead": ("lmhead.cu", "accept.cu", "ptx.cuh", "api.cu", "tmap.h"),
+    "attention": ("attention.cu", "ptx.cuh", "api.cu"),
+}
+STEP_BOUNDS = {"layer": ("route", "combine_kernel"), "lmhead": ("lmhead_argmax_kernel", "accept_finalize_kernel"),
+               "attention": ("attn_split_kernel", "attn_combine_kernel")}
+
+
+def step_kind(workload):
+    return workload if workload in STEP_SOURCES else "layer"
+
+
+def layer_source_hash(workload="decode"):
     h = hashlib.sha256()
-    for f in ("ffn.cu", "ptx.cuh", "route.cu", "permute.cu", "combine.cu", "ffn_plan.cuh", "api.cu", "tmap.h"):
+    for f in STEP_SOURCES[step_kind(workload)]:
         with open(os.path.join(ROOT, "lossless_speculative_verification_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -183,27 +197,28 @@ def record_traffic(args):
                 e[r["Metric Name"]] = float(r["Metric Value"].replace(",", "")) * scale
             except ValueError:
                 pass
+    first, last_k = STEP_BOUNDS[step_kind(args.workload)]
     layers, cur = [], None
     for i in sorted(launches):
         e = launches[i]
         base = e["name"].split("<")[0]
-        if base.startswith("route"):
+        if base.startswith(first):
             cur = []
         if cur is None:
             continue
         cur.append(e)
-        if base == "combine_kernel":
+        if base == last_k:
             layers.append(cur)
             cur = None
     if not layers:
-        raise SystemExit("no complete layer (router ... combine) in %s" % args.record_traffic)
+        raise SystemExit("no complete step (%s ... %s) in %s" % (first, last_k, args.record_traffic))
     per_layer = [sum(e.get("dram__bytes_read.sum", 0) + e.get("dram__bytes_write.sum", 0) for e in L) for L in layers]
     last = {e["name"]: {"read": int(e.get("dram__bytes_read.sum", 0)), "write": int(e.get("dram__bytes_write.sum", 0)),
                         "ns": int(e.get("gpu__time_duration.sum", 0))} for e in layers[-1]}
     out = {"workload": args.workload, "command": args.ncu_command,
            "note": "sum of DRAM read+write bytes over one layer's launches, mean over the %d layers in the "
                    "capture; the writes include write-backs of the benchmark's own L2-flush buffer" % len(layers),
-           "kernel_source_hash": layer_source_hash(), "dram_bytes_per_layer": int(sum(per_layer) / len(per_layer)),
+           "kernel_source_hash": layer_source_hash(args.workload), "dram_bytes_per_layer": int(sum(per_layer) / len(per_layer)),
            "per_kernel_last_layer": last}
     path = os.path.join(ROOT, "profiles", "layer_%s_traffic.json" % args.workload)
     with open(path, "w") as f:
@@ -683,7 +698,7 @@ def result_line(args, step, m, world, cpu):
     hbm, tflops, peak_src = peaks()
     w = step.w
     byts, flops, acc_bytes = step.bytes_and_flops()
-    khash = layer_source_hash()
+    khash = layer_source_hash(step.name)
     if step.name in SIDE_STEPS:
         achieved = byts / (m["total_ms"] / args.steps / 1e3) / 1e9
         kernel = ("lmhead_argmax_kernel (tcgen05 product of the output layer and the hidden rows, reduced "

@@ -178,7 +178,11 @@ lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t
  * fp32 scores and accumulation.  Supported: d in {64, 128}, 1 <= Q <= 8,
  * B, nh <= 65535, scale > 0.  A ctx_len outside [Q, L] raises
  * LSV_ERR_DEVICE_INDEX (that sequence's output is zero).
- * ws: spec_verify_attention_workspace_size(B,Q,L,nh,d) bytes (0: unsupported). */
+ * ws: spec_verify_attention_workspace_size(B,Q,L,nh,d) bytes (0: unsupported),
+ * all zero before its first use; every call that raises no device error leaves
+ * its counters zero again, so it serves any later call whose size fits.
+ * One launch; a call may start before the previous work on the stream ends
+ * (programmatic dependent launch) but reads nothing before that work is done. */
 size_t spec_verify_attention_workspace_size(int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d);
 lsv_status spec_verify_attention(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
                                  int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d, float scale, void *out,

@@ -145,10 +145,12 @@ def spec_verify_accept(logits, drafts, ws, argmax=None, accept_len=None, committ
 
 
 def spec_verify_attention_workspace(B, Q, L, nh, d, device=None) -> torch.Tensor:
+    """Workspace of spec_verify_attention, zeroed (its counters must start at zero; every call
+    leaves them zero)."""
     n = _ffi.load().spec_verify_attention_workspace_size(B, Q, L, nh, d)
     if n == 0:
         raise ValueError("unsupported attention shape")
-    return torch.empty(int(n), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(int(n), dtype=torch.uint8, device=device or "cuda")
 
 
 def spec_verify_attention(q, k_cache, v_cache, ctx_len, ws, scale=None, out=None, stream=None):

@@ -144,6 +144,39 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// ----------------------------------------------------------------------------- warp-level MMA
+// Four 8x8 b16 matrices from shared memory; lane 8j+r gives the address of row r
+// of matrix j.  Lane (g = lane/4, t = lane%4) receives in r[j] row g, columns
+// 2t and 2t+1 of matrix j (.trans: row 2t and 2t+1 of column g).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// D[16x8] = A[16x16] * B[16x8] + C, bf16 inputs, fp32 accumulation.  Only the
+// accumulator rows 0..7 are kept: the caller's A rows 8..15 are zero, so rows
+// 8..15 of C are passed as zero and those of D are dropped.
+__device__ __forceinline__ void mma_bf16_m16n8k16_top(float (&c)[2], uint32_t a0, uint32_t a2, uint32_t b0,
+                                                      uint32_t b1) {
+  float d2, d3;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %11, %12, %13};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(d2), "=f"(d3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(0.f), "f"(0.f));
+  (void)d2;
+  (void)d3;
+}
+
 // ----------------------------------------------------------------------------- tcgen05
 // TMEM allocation: executed by one whole warp; the base address is written to *dst.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
