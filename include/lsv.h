@@ -176,11 +176,15 @@ lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t
  *     out[b,j,h] = sum_{t <= p} softmax_t(scale * q[b,j,h].k[b,t,h]) v[b,t,h],
  *     p = ctx_len[b] - Q + j (query j sees the cache up to and including itself)
  * fp32 scores and accumulation.  Supported: d in {64, 128}, 1 <= Q <= 8,
- * B, nh <= 65535, scale > 0.  A ctx_len outside [Q, L] raises
+ * B, nh <= 65535, B*nh <= 262144, scale > 0.  Cache entries at or past
+ * ctx_len[b] are never used, whatever they hold.  A ctx_len outside [Q, L] raises
  * LSV_ERR_DEVICE_INDEX (that sequence's output is zero).
- * ws: spec_verify_attention_workspace_size(B,Q,L,nh,d) bytes (0: unsupported),
- * all zero before its first use; every call that raises no device error leaves
- * its counters zero again, so it serves any later call whose size fits.
+ * Device pointers, 16-byte aligned.
+ * ws: spec_verify_attention_workspace_size(B,Q,L,nh,d) bytes (0: unsupported).
+ * Its first 1 MiB holds per-(sequence, head) counters at the same place for
+ * every shape: all zero before the first use; every call that raises no device
+ * error leaves them zero again, so one workspace serves any later call whose
+ * size fits (zero them again after an error).
  * One launch; a call may start before the previous work on the stream ends
  * (programmatic dependent launch) but reads nothing before that work is done. */
 size_t spec_verify_attention_workspace_size(int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d);

@@ -341,9 +341,14 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 int attention_splits(int L) { return L <= 0 ? 1 : (L + kAtChunk - 1) / kAtChunk; }
 
+// The split counters sit in a block of fixed size at the start of every workspace, so that
+// calls of different shapes sharing one workspace never write partials over another shape's
+// counters (each call leaves its own counters zero).
+constexpr size_t kAttnCounterBytes = (size_t)kAttnMaxPairs * 4;
+
 size_t attention_ws_bytes(int B, int Q, int L, int nh, int d) {
   const size_t parts = (size_t)B * nh * attention_splits(L) * Q;
-  return round256((size_t)B * nh * 4) + round256(parts * d * 4) + round256(parts * 2 * 4);
+  return kAttnCounterBytes + round256(parts * d * 4) + round256(parts * 2 * 4);
 }
 
 cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, const int32_t* ctx_len, int B, int Q,
@@ -373,8 +378,8 @@ cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, cons
   const size_t parts = (size_t)B * nh * p.nsplit * Q;
   uint8_t* w = reinterpret_cast<uint8_t*>(ws);
   p.cnt = reinterpret_cast<int*>(w);
-  p.o_part = reinterpret_cast<float*>(w + round256((size_t)B * nh * 4));
-  p.ml_part = reinterpret_cast<float*>(w + round256((size_t)B * nh * 4) + round256(parts * d * 4));
+  p.o_part = reinterpret_cast<float*>(w + kAttnCounterBytes);
+  p.ml_part = reinterpret_cast<float*>(w + kAttnCounterBytes + round256(parts * d * 4));
   p.out = out;
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();

@@ -21,6 +21,7 @@ constexpr int kMaxShared = 8;
 constexpr int kMaxHidden = 16384;
 constexpr int kMaxVerifyRows = 64;  // K + 1 per sequence
 constexpr int kMaxAttnQ = 8;        // verified positions per sequence in the attention
+constexpr int kAttnMaxPairs = 1 << 18;  // (sequence, head) pairs per attention call
 
 // Per-device state: the error word's device address and the SM count.
 struct DeviceCtx {

@@ -167,14 +167,14 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4
 // 8..15 of C are passed as zero and those of D are dropped.
 __device__ __forceinline__ void mma_bf16_m16n8k16_top(float (&c)[2], uint32_t a0, uint32_t a2, uint32_t b0,
                                                       uint32_t b1) {
-  float d2, d3;
-  asm volatile(
+  float d[4];
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%10, %11, %12, %13};"
-      : "=f"(c[0]), "=f"(c[1]), "=f"(d2), "=f"(d3)
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(0.f), "f"(0.f));
-  (void)d2;
-  (void)d3;
+  c[0] = d[0];
+  c[1] = d[1];
 }
 
 // ----------------------------------------------------------------------------- tcgen05

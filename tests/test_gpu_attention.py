@@ -68,13 +68,15 @@ def test_attention_peaked_scores():
 
 
 def test_attention_reads_no_masked_entries():
-    # the cache past each length and the positions after each query are filled with huge values:
-    # any read of them would show in the output
-    p = problem(2, 4, 2, 128, 1024, (600, 1024), seed=9)
+    # the cache past a sequence's length holds NaN (keys) and huge values (values) in one sequence
+    # and NaN in both in another: none of it may reach the output
+    p = problem(3, 4, 2, 128, 1024, (600, 1024, 77), seed=9)
     k, v = p.k_cache.copy(), p.v_cache.copy()
-    big = synth.bf16_bits(np.float32(1e4))
-    k[0, 600:] = big
-    v[0, 600:] = big
+    nan = np.uint16(0x7FC0)
+    k[0, 600:] = nan
+    v[0, 600:] = synth.bf16_bits(np.float32(1e4))
+    k[2, 77:] = nan
+    v[2, 77:] = nan
     p2 = synth.AttentionProblem(p.B, p.Q, p.L, p.nh, p.d, p.q, k, v, p.ctx_len)
     got = check(p2, what="masked")
     ref = run(p)
@@ -91,6 +93,23 @@ def test_attention_empty_batch_and_determinism():
     a = run(p)
     b = run(p)
     np.testing.assert_array_equal(a, b)
+
+
+def test_attention_workspace_reuse_across_shapes():
+    # one workspace (sized for the largest call) through calls of different shapes: the split
+    # counters each call leaves behind must be zero for the next
+    big = problem(8, 4, 3, 128, 1300, (1300, 4, 600, 1200, 513, 512, 1024, 77), seed=5)
+    small = problem(3, 2, 5, 64, 2100, (2100, 1025, 2), seed=6)
+    ws = api.spec_verify_attention_workspace(8, 8, 2100, 5, 128)
+    a1 = run(big, ws=ws)
+    b1 = run(small, ws=ws)
+    a2 = run(big, ws=ws)
+    b2 = run(small, ws=ws)
+    np.testing.assert_array_equal(a1, a2)
+    np.testing.assert_array_equal(b1, b2)
+    np.testing.assert_array_equal(a1, run(big))
+    assert_layer_close(bf16_f64(b1), oracle.verify_attention(small.q, small.k_cache, small.v_cache, small.ctx_len,
+                                                             1 / 8), "small after big")
 
 
 def test_attention_bad_length_sets_the_error_word():
