@@ -8,21 +8,27 @@
 // positions, the step is a stream of the cache through the SMs: per cached
 // position and head it reads 2*d bf16 values and does 4*Q*d flops.
 //
-// One CTA takes one (split, head, sequence): up to kAtChunk cached positions.
-//   warp 4 (producer): TMA loads of 64-position key and value tiles (the head's
-//     d columns of 64 cache rows, 128-byte swizzle) into a kAtStages ring;
+// attn_split_kernel: persistent CTAs (as many as fit on the GPU) take work
+// items (split, sequence, head) -- up to kAtChunk cached positions of one
+// head of one sequence -- from an atomic dealer, split-major so that the
+// short last splits come last.
+//   warp 4 (producer): deals items and streams their 64-position key and value
+//     tiles (the head's d columns of 64 cache rows, 128-byte swizzle) by TMA
+//     into a kAtStages ring, without a gap between items; the first tile of
+//     an item also carries the item's query rows.  A small record per stage
+//     tells the consumers what the stage holds.
 //   warps 0-3 (consumers): each takes 16 positions of every tile.  Scores
 //     S = q K^T and the weighted values P V run on the tensor cores as
 //     m16n8k16 warp MMAs whose 16 rows are the queries (rows >= Q are zero):
 //     S stays in registers, the online softmax (running maximum and sum per
 //     query, in fp32, exp2 of log2e-scaled scores) turns it into P in the
 //     register layout the second MMA takes as its A operand, and the
-//     fragments of K (ldmatrix) and V (ldmatrix.trans) come from the swizzled
-//     tiles without bank conflicts.
-// The four warps' states merge in shared memory into the split's partial
-// (running maximum, sum, unnormalised output).  The last CTA of a
-// (sequence, head) to finish -- a counter per (sequence, head), which it resets
-// -- merges the splits and writes the bf16 output, so one launch does it all.
+//     fragments of q and K (ldmatrix) and V (ldmatrix.trans) come from the
+//     swizzled tiles without bank conflicts.  At the end of an item each
+//     warp writes its state (running maximum, sum, unnormalised output).
+// attn_combine_kernel (programmatic dependent launch): per (sequence, head),
+// the warps' and splits' states rescaled to their common maximum and summed;
+// out = sum / normaliser in bf16.  It also rewinds the dealer.
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -33,36 +39,42 @@ namespace {
 constexpr int kAtConsumers = 4;
 constexpr int kAtThreads = 32 * (kAtConsumers + 1);
 constexpr int kAtTile = 64;  // positions per ring stage (16 per consumer warp)
-constexpr int kAtStages = 3;
-#ifndef LSV_ATTN_CHUNK
-#define LSV_ATTN_CHUNK 512
+#ifndef LSV_ATTN_STAGES
+#define LSV_ATTN_STAGES 3
 #endif
-constexpr int kAtChunk = LSV_ATTN_CHUNK;  // cached positions per CTA
-static_assert(kAtChunk % kAtTile == 0, "a split is a whole number of tiles");
+constexpr int kAtStages = LSV_ATTN_STAGES;
+#ifndef LSV_ATTN_CHUNK
+#define LSV_ATTN_CHUNK 256
+#endif
+constexpr int kAtChunk = LSV_ATTN_CHUNK;  // cached positions per item
+static_assert(kAtChunk % kAtTile == 0, "an item is a whole number of tiles");
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kAtBarMerge = 1;  // named barrier of the consumer warps
+constexpr int kAttnCtlInts = 64;  // dealer at [0]; the rest reserved
 
 template <int D>
 struct AtSmem {
-  static constexpr int kBox = kAtTile * 128;          // 64 columns x 64 rows of bf16
-  static constexpr int kStage = 2 * (D / 64) * kBox;  // key boxes, then value boxes
+  static constexpr int kBox = kAtTile * 128;       // 64 columns x 64 rows of bf16
+  static constexpr int kQBox = kMaxAttnQ * 128;    // 64 columns x 8 query rows
+  static constexpr int kKV = 2 * (D / 64) * kBox;  // key boxes, then value boxes
+  static constexpr int kStage = kKV + (D / 64) * kQBox;
   static constexpr int kRing = kAtStages * kStage;
-  // merge buffers (in the ring once the stream is done)
-  static constexpr int kMergeO = kAtConsumers * kMaxAttnQ * D * 4;
-  static_assert(kMergeO + 2 * kAtConsumers * kMaxAttnQ * 4 <= kRing, "merge buffers fit in the ring");
+  static constexpr int kMeta = kAtStages * 32;
   static constexpr int kBars = 2 * kAtStages * 8;
-  static constexpr int kTotal = 1024 + kRing + kBars + 16;
+  static constexpr int kTotal = 1024 + kRing + kMeta + kBars + 16;
+};
+
+struct AtMeta {
+  int b, h, split, i, ntiles, n, end, pad;
 };
 
 struct AtParams {
-  const bf16* q;           // [B, Q, nh, D]
   const int32_t* ctx_len;  // [B]
-  int Q, L, nh, nsplit;
+  int B, Q, L, nh, nsplit;
+  int total;       // nsplit * B * nh items
   float qk_scale;  // scale * log2(e)
-  float* o_part;   // [B, nh, nsplit, Q, D]
-  float* ml_part;  // [B, nh, nsplit, Q, 2]: running maximum (log2 units), sum
-  int* cnt;        // [B * nh] splits finished; zero between launches
-  bf16* out;       // [B, Q, nh, D]
+  float* o_part;   // [B*nh, nsplit, warps, Q, D]
+  float* ml_part;  // [B*nh, nsplit, warps, Q, 2]: running maximum (log2 units), sum
+  int* dealer;     // zero before the launch; the combine rewinds it
   int* err;
   uint64_t wait_ns;
 };
@@ -79,38 +91,19 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^
 template <int D>
 __global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
+                                                                const __grid_constant__ CUtensorMap qmap,
                                                                 const AtParams p) {
   using SM = AtSmem<D>;
   constexpr int NB = D / 64;  // boxes per tensor per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kRing);
+  volatile AtMeta* meta = reinterpret_cast<volatile AtMeta*>(smem + SM::kRing);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kRing + SM::kMeta);
   uint64_t* empty = full + kAtStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kAtStages);
-  volatile int* last_flag = abort_flag + 1;
-  volatile int* issued_s = abort_flag + 2;
-  int* done_s = const_cast<int*>(abort_flag + 3);
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  volatile int* issued_s = abort_flag + 1;
+  int* done_s = const_cast<int*>(abort_flag + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  pdl_wait();  // q, the lengths and the caches may come from the preceding kernel
-  pdl_trigger();
-  const int n = p.ctx_len[b];
-  if (n < p.Q || n > p.L) {
-    if (split == 0) {
-      if (threadIdx.x == 0) set_error(p.err, kErrDeviceIndex);
-      for (int i = threadIdx.x; i < p.Q * D; i += kAtThreads) {
-        const int j = i / D, c = i - j * D;
-        p.out[(((size_t)b * p.Q + j) * p.nh + h) * D + c] = __float2bfloat16_rn(0.f);
-      }
-    }
-    return;
-  }
-  const int t_begin = split * kAtChunk;
-  if (t_begin >= n) return;  // no cached position of this sequence in the split
-  const int t_end = min(n, t_begin + kAtChunk);
-  const int ntiles = (t_end - t_begin + kAtTile - 1) / kAtTile;
-  const int nactive = (n + kAtChunk - 1) / kAtChunk;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAtStages; ++s) {
@@ -119,75 +112,124 @@ __global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_con
     }
     *abort_flag = 0;
     *issued_s = 0;
-    *done_s = ntiles;
+    *done_s = 1 << 30;
     fence_barrier_init();
   }
   if (threadIdx.x == 32 * kAtConsumers) {
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&qmap);
   }
   __syncthreads();
+  pdl_wait();  // q, the lengths, the caches and the dealer come from earlier work on the stream
+  pdl_trigger();
 
   if (warp == kAtConsumers) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ dealer + TMA producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      const int row0 = b * p.L + t_begin;
-      int i = 0;
-      for (; i < ntiles; ++i) {
-        const int s = i % kAtStages;
-        if (!mbar_wait(&empty[s], ((i / kAtStages) & 1) ^ 1u, p.wait_ns)) {
-          set_error(p.err, kErrTimeout);
-          *abort_flag = 1;
-          break;
-        }
-        uint8_t* st = smem + s * SM::kStage;
-        mbar_arrive_expect_tx(&full[s], SM::kStage);
+      const int per_split = p.B * p.nh;
+      int k = 0;  // tiles (and the end record) put in the ring so far
+      bool ok = true;
+      while (ok) {
+        const int item = atomicAdd(p.dealer, 1);
+        if (item >= p.total) break;
+        const int split = item / per_split;
+        const int bh = item - split * per_split;
+        const int b = bh / p.nh, h = bh - b * p.nh;
+        const int n = p.ctx_len[b];
+        const int t_begin = split * kAtChunk;
+        if (n < p.Q || n > p.L || t_begin >= n) continue;  // nothing to stream (the combine reports bad lengths)
+        const int ntiles = (min(n, t_begin + kAtChunk) - t_begin + kAtTile - 1) / kAtTile;
+        const int row0 = b * p.L + t_begin;
+        for (int i = 0; i < ntiles; ++i, ++k) {
+          const int s = k % kAtStages;
+          if (!mbar_wait(&empty[s], ((k / kAtStages) & 1) ^ 1u, p.wait_ns)) {
+            set_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          meta[s].b = b;
+          meta[s].h = h;
+          meta[s].split = split;
+          meta[s].i = i;
+          meta[s].ntiles = ntiles;
+          meta[s].n = n;
+          meta[s].end = 0;
+          uint8_t* st = smem + s * SM::kStage;
+          mbar_arrive_expect_tx(&full[s], SM::kKV + (i == 0 ? NB * SM::kQBox : 0));
 #pragma unroll
-        for (int c = 0; c < NB; ++c) {
-          tma_load_2d(st + c * SM::kBox, &kmap, &full[s], h * D + 64 * c, row0 + i * kAtTile, pol);
-          tma_load_2d(st + (NB + c) * SM::kBox, &vmap, &full[s], h * D + 64 * c, row0 + i * kAtTile, pol);
+          for (int c = 0; c < NB; ++c) {
+            tma_load_2d(st + c * SM::kBox, &kmap, &full[s], h * D + 64 * c, row0 + i * kAtTile, pol);
+            tma_load_2d(st + (NB + c) * SM::kBox, &vmap, &full[s], h * D + 64 * c, row0 + i * kAtTile, pol);
+            if (i == 0) tma_load_2d(st + SM::kKV + c * SM::kQBox, &qmap, &full[s], h * D + 64 * c, b * p.Q, pol);
+          }
         }
       }
-      *issued_s = i;
+      if (ok) {
+        // end record
+        const int s = k % kAtStages;
+        if (mbar_wait(&empty[s], ((k / kAtStages) & 1) ^ 1u, p.wait_ns)) {
+          meta[s].end = 1;
+          mbar_arrive(&full[s]);
+        } else {
+          set_error(p.err, kErrTimeout);
+          *abort_flag = 1;
+        }
+      }
+      *issued_s = k;
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers
     const int g = lane >> 2, t = lane & 3;
     const bool row_ok = g < p.Q;
-    // q as the A operand: row g = query g, k-step s covers dims [16s, 16s+16)
-    uint32_t qa[D / 16][2];
-    {
-      const bf16* qr = p.q + (((size_t)b * p.Q + (row_ok ? g : 0)) * p.nh + h) * D;
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        qa[s][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qr + 16 * s + 2 * t) : 0u;
-        qa[s][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qr + 16 * s + 2 * t + 8) : 0u;
-      }
-    }
-    const int lim = row_ok ? n - p.Q + g : -1;  // last position query g sees
-    float m_run = -INFINITY, l_run = 0.f;
-    float o[D / 8][2];
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = 0.f;
-    // ldmatrix addressing: lane supplies row (lane & 7) of matrix (lane >> 3)
-    const int mi = lane >> 3, mr = lane & 7;
+    const int mi = lane >> 3, mr = lane & 7;            // ldmatrix: lane gives row mr of matrix mi
     const int k_row = 16 * warp + 8 * (mi >> 1) + mr;  // S: matrices (n-tile, k half) = (mi>>1, mi&1)
     const int k_half = mi & 1;
     const int v_row = 16 * warp + 8 * (mi & 1) + mr;  // PV: matrices (k half, n-tile) = (mi&1, mi>>1)
     const int v_half = mi >> 1;
-    int done = 0;
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i % kAtStages;
+    uint32_t qa[D / 16][2];
+    float o[D / 8][2];
+    float m_run = -INFINITY, l_run = 0.f;
+    int lim = -1;
+    for (int k = 0;; ++k) {
+      const int s = k % kAtStages;
       // every lane waits; the warp leaves together if any lane ran out of time
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / kAtStages) & 1, p.wait_ns))) {
-        if (lane == 0) set_error(p.err, kErrTimeout);
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / kAtStages) & 1, p.wait_ns))) {
+        if (lane == 0) {
+          set_error(p.err, kErrTimeout);
+          atomicMin(done_s, k);
+        }
         *abort_flag = 1;
         break;
       }
+      if (meta[s].end) break;
+      const int b = meta[s].b, h = meta[s].h, split = meta[s].split, i = meta[s].i, n = meta[s].n;
+      const int ntiles = meta[s].ntiles;
       const uint32_t kb = smem_u32(smem + s * SM::kStage);
       const uint32_t vb = kb + NB * SM::kBox;
+      if (i == 0) {
+        // a new item: its queries as the A operand (row g = query g; k-step ks covers dims [16ks, 16ks+16))
+        const uint32_t qb = kb + SM::kKV;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ks += 2) {
+          // matrices (k-step ks + (mi>>1), k half mi&1), rows = queries 0..7
+          const int ch = 2 * ks + mi;
+          uint32_t r[4];
+          ldmatrix_x4(qb + (ch >> 3) * SM::kQBox + sw128(mr, ch & 7), r);
+          qa[ks][0] = row_ok ? r[0] : 0u;
+          qa[ks][1] = row_ok ? r[1] : 0u;
+          qa[ks + 1][0] = row_ok ? r[2] : 0u;
+          qa[ks + 1][1] = row_ok ? r[3] : 0u;
+        }
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = 0.f;
+        m_run = -INFINITY;
+        l_run = 0.f;
+        lim = row_ok ? n - p.Q + g : -1;  // last position query g sees
+      }
       // scores of this warp's 16 positions: two n-tiles of 8
       float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
@@ -199,7 +241,7 @@ __global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_con
         mma_bf16_m16n8k16_top(sc[1], qa[ks][0], qa[ks][1], r[2], r[3]);
       }
       // online softmax of row g over its columns 2t, 2t+1 of both n-tiles
-      const int pos0 = t_begin + i * kAtTile + 16 * warp + 2 * t;  // absolute position of sc[0][0]
+      const int pos0 = split * kAtChunk + i * kAtTile + 16 * warp + 2 * t;  // position of sc[0][0]
       float sv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -245,85 +287,17 @@ __global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_con
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      done = i + 1;
-    }
-    if (done < ntiles && lane == 0) atomicMin(done_s, done);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-
-    named_bar_sync(kAtBarMerge, 32 * kAtConsumers);  // every consumer is done with the ring
-    if (!*abort_flag) {
-      float* o_s = reinterpret_cast<float*>(smem);  // [warp][row][D]
-      float* m_s = o_s + kAtConsumers * kMaxAttnQ * D;
-      float* l_s = m_s + kAtConsumers * kMaxAttnQ;
-      if (row_ok) {
+      if (i == ntiles - 1) {
+        // the item's last tile: write this warp's state
+        float l = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        const size_t row = ((((size_t)b * p.nh + h) * p.nsplit + split) * kAtConsumers + warp) * p.Q + g;
+        if (row_ok) {
+          float* op = p.o_part + row * D + 2 * t;
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-          o_s[(warp * kMaxAttnQ + g) * D + 8 * nt + 2 * t] = o[nt][0];
-          o_s[(warp * kMaxAttnQ + g) * D + 8 * nt + 2 * t + 1] = o[nt][1];
-        }
-        if (t == 0) {
-          m_s[warp * kMaxAttnQ + g] = m_run;
-          l_s[warp * kMaxAttnQ + g] = l_run;
-        }
-      }
-      named_bar_sync(kAtBarMerge, 32 * kAtConsumers);
-      // the split's state: the warps' states rescaled to their common maximum
-      const size_t bh = (size_t)b * p.nh + h;
-      const size_t part = (bh * p.nsplit + split) * p.Q;
-      for (int e = threadIdx.x; e < p.Q * D; e += 32 * kAtConsumers) {
-        const int j = e / D, c = e - j * D;
-        float mm = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kAtConsumers; ++w) mm = fmaxf(mm, m_s[w * kMaxAttnQ + j]);
-        float ls = 0.f, os = 0.f;
-        if (mm != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kAtConsumers; ++w) {
-            const float mw = m_s[w * kMaxAttnQ + j];
-            if (mw == -INFINITY) continue;
-            const float f = exp2f(mw - mm);
-            ls += l_s[w * kMaxAttnQ + j] * f;
-            os += o_s[(w * kMaxAttnQ + j) * D + c] * f;
-          }
-        }
-        if (nactive == 1) {
-          p.out[(((size_t)b * p.Q + j) * p.nh + h) * D + c] = __float2bfloat16_rn(ls > 0.f ? os / ls : 0.f);
-        } else {
-          p.o_part[(part + j) * D + c] = os;
-          if (c == 0) {
-            p.ml_part[(part + j) * 2] = mm;
-            p.ml_part[(part + j) * 2 + 1] = ls;
-          }
-        }
-      }
-      if (nactive > 1) {
-        // the last split of (b, h) to finish merges all of them
-        __threadfence();
-        named_bar_sync(kAtBarMerge, 32 * kAtConsumers);
-        if (threadIdx.x == 0) *last_flag = atomicAdd(&p.cnt[bh], 1) == nactive - 1;
-        named_bar_sync(kAtBarMerge, 32 * kAtConsumers);
-        if (*last_flag) {
-          __threadfence();
-          const size_t part0 = bh * p.nsplit * p.Q;
-          for (int e = threadIdx.x; e < p.Q * D; e += 32 * kAtConsumers) {
-            const int j = e / D, c = e - j * D;
-            float mm = -INFINITY;
-            for (int sp = 0; sp < nactive; ++sp) mm = fmaxf(mm, __ldcg(&p.ml_part[(part0 + sp * p.Q + j) * 2]));
-            float ls = 0.f, os = 0.f;
-            if (mm != -INFINITY) {
-              for (int sp = 0; sp < nactive; ++sp) {
-                const size_t at = part0 + sp * p.Q + j;
-                const float ms = __ldcg(&p.ml_part[at * 2]);
-                if (ms == -INFINITY) continue;
-                const float f = exp2f(ms - mm);
-                ls += __ldcg(&p.ml_part[at * 2 + 1]) * f;
-                os += __ldcg(&p.o_part[at * D + c]) * f;
-              }
-            }
-            p.out[(((size_t)b * p.Q + j) * p.nh + h) * D + c] = __float2bfloat16_rn(ls > 0.f ? os / ls : 0.f);
-          }
-          if (threadIdx.x == 0) p.cnt[bh] = 0;  // ready for the next launch
+          for (int nt = 0; nt < D / 8; ++nt)
+            *reinterpret_cast<float2*>(op + 8 * nt) = make_float2(o[nt][0], o[nt][1]);
+          if (t == 0) *reinterpret_cast<float2*>(p.ml_part + row * 2) = make_float2(m_run, l);
         }
       }
     }
@@ -331,67 +305,107 @@ __global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_con
   __syncthreads();
   if (*abort_flag && threadIdx.x == 0) {
     // let the copies already issued land before the CTA's shared memory goes away
-    for (int i = *done_s; i < *issued_s; ++i) mbar_wait(&full[i % kAtStages], (i / kAtStages) & 1, p.wait_ns);
+    for (int kk = *done_s; kk < *issued_s; ++kk) mbar_wait(&full[kk % kAtStages], (kk / kAtStages) & 1, p.wait_ns);
+  }
+}
+
+// Per (head, sequence): merge the warps' and splits' states and write the output.
+template <int D>
+__global__ void __launch_bounds__(D) attn_combine_kernel(const float* __restrict__ o_part,
+                                                         const float* __restrict__ ml_part,
+                                                         const int32_t* __restrict__ ctx_len, int Q, int L, int nh,
+                                                         int nsplit, bf16* __restrict__ out, int* dealer, int* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
+  if (h == 0 && b == 0 && c == 0) *dealer = 0;  // the split kernel is done with it
+  const int n = ctx_len[b];
+  const bool bad = n < Q || n > L;
+  if (bad && h == 0 && c == 0) set_error(err, kErrDeviceIndex);
+  const int nparts = bad ? 0 : (n + kAtChunk - 1) / kAtChunk * kAtConsumers;
+  const size_t base = ((size_t)b * nh + h) * nsplit * kAtConsumers;  // first state of (b, h)
+  for (int j = 0; j < Q; ++j) {
+    float mm = -INFINITY;
+    for (int s = 0; s < nparts; ++s) mm = fmaxf(mm, ml_part[((base + s) * Q + j) * 2]);
+    float ls = 0.f, os = 0.f;
+    if (mm != -INFINITY) {
+      for (int s = 0; s < nparts; ++s) {
+        const size_t at = (base + s) * Q + j;
+        const float ms = ml_part[at * 2];
+        if (ms == -INFINITY) continue;
+        const float f = exp2f(ms - mm);
+        ls += ml_part[at * 2 + 1] * f;
+        os += o_part[at * D + c] * f;
+      }
+    }
+    out[(((size_t)b * Q + j) * nh + h) * D + c] = __float2bfloat16_rn(ls > 0.f ? os / ls : 0.f);
   }
 }
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+template <int D>
+cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, const int32_t* ctx_len, int B, int Q,
+                               int L, int nh, float scale, bf16* out, void* ws, const DeviceCtx& dc,
+                               cudaStream_t s) {
+  static int grid_per_sm[64] = {0};
+  if (dc.device < 0 || dc.device >= 64) return cudaErrorInvalidDevice;
+  if (!grid_per_sm[dc.device]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, AtSmem<D>::kTotal);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_kernel<D>, kAtThreads, AtSmem<D>::kTotal);
+    if (e != cudaSuccess) return e;
+    grid_per_sm[dc.device] = per_sm > 0 ? per_sm : 1;
+  }
+  AtParams p;
+  p.ctx_len = ctx_len;
+  p.B = B;
+  p.Q = Q;
+  p.L = L;
+  p.nh = nh;
+  p.nsplit = attention_splits(L);
+  p.total = p.nsplit * B * nh;
+  p.qk_scale = scale * kLog2e;
+  const size_t parts = (size_t)B * nh * p.nsplit * kAtConsumers * Q;
+  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+  p.dealer = reinterpret_cast<int*>(w);
+  p.o_part = reinterpret_cast<float*>(w + round256(kAttnCtlInts * 4));
+  p.ml_part = reinterpret_cast<float*>(w + round256(kAttnCtlInts * 4) + round256(parts * D * 4));
+  p.err = dc.err;
+  p.wait_ns = wait_limit_ns();
+  // the caches as [B*L rows, nh*d columns] (a tile: d columns of 64 rows), the queries as
+  // [B*Q rows, nh*d columns] (a sequence's queries: d columns of 8 rows from its first)
+  CUtensorMap kmap, vmap, qmap;
+  if (!make_map(&kmap, kc, (uint64_t)B * L, (uint64_t)nh * D, kAtTile) ||
+      !make_map(&vmap, vc, (uint64_t)B * L, (uint64_t)nh * D, kAtTile) ||
+      !make_map(&qmap, q, (uint64_t)B * Q, (uint64_t)nh * D, kMaxAttnQ))
+    return cudaErrorInvalidValue;
+  const long long cap = (long long)grid_per_sm[dc.device] * dc.num_sms;
+  const int grid = (int)(p.total < cap ? p.total : cap);
+  cudaError_t e = launch_pdl(attn_split_kernel<D>, dim3(grid), dim3(kAtThreads), AtSmem<D>::kTotal, s, kmap, vmap,
+                             qmap, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_combine_kernel<D>, dim3(nh, B), dim3(D), 0, s, (const float*)p.o_part,
+                    (const float*)p.ml_part, ctx_len, Q, L, nh, p.nsplit, out, p.dealer, dc.err);
+}
+
 }  // namespace
 
 int attention_splits(int L) { return L <= 0 ? 1 : (L + kAtChunk - 1) / kAtChunk; }
 
-// The split counters sit in a block of fixed size at the start of every workspace, so that
-// calls of different shapes sharing one workspace never write partials over another shape's
-// counters (each call leaves its own counters zero).
-constexpr size_t kAttnCounterBytes = (size_t)kAttnMaxPairs * 4;
-
 size_t attention_ws_bytes(int B, int Q, int L, int nh, int d) {
-  const size_t parts = (size_t)B * nh * attention_splits(L) * Q;
-  return kAttnCounterBytes + round256(parts * d * 4) + round256(parts * 2 * 4);
+  const size_t parts = (size_t)B * nh * attention_splits(L) * kAtConsumers * Q;
+  return round256(kAttnCtlInts * 4) + round256(parts * d * 4) + round256(parts * 2 * 4);
 }
 
 cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, const int32_t* ctx_len, int B, int Q,
                              int L, int nh, int d, float scale, bf16* out, void* ws, const DeviceCtx& dc,
                              cudaStream_t s) {
   if (B == 0) return cudaSuccess;
-  static int attr_done[64][2] = {{0}};
-  if (dc.device < 0 || dc.device >= 64) return cudaErrorInvalidDevice;
-  const int di = d == 128 ? 1 : 0;
-  if (!attr_done[dc.device][di]) {
-    const cudaError_t e =
-        d == 128 ? cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        AtSmem<128>::kTotal)
-                 : cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        AtSmem<64>::kTotal);
-    if (e != cudaSuccess) return e;
-    attr_done[dc.device][di] = 1;
-  }
-  AtParams p;
-  p.q = q;
-  p.ctx_len = ctx_len;
-  p.Q = Q;
-  p.L = L;
-  p.nh = nh;
-  p.nsplit = attention_splits(L);
-  p.qk_scale = scale * kLog2e;
-  const size_t parts = (size_t)B * nh * p.nsplit * Q;
-  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
-  p.cnt = reinterpret_cast<int*>(w);
-  p.o_part = reinterpret_cast<float*>(w + kAttnCounterBytes);
-  p.ml_part = reinterpret_cast<float*>(w + kAttnCounterBytes + round256(parts * d * 4));
-  p.out = out;
-  p.err = dc.err;
-  p.wait_ns = wait_limit_ns();
-  // the caches as [B*L rows, nh*d columns]; a tile is d columns of 64 rows
-  CUtensorMap kmap, vmap;
-  if (!make_map(&kmap, kc, (uint64_t)B * L, (uint64_t)nh * d, kAtTile) ||
-      !make_map(&vmap, vc, (uint64_t)B * L, (uint64_t)nh * d, kAtTile))
-    return cudaErrorInvalidValue;
-  const dim3 grid(p.nsplit, nh, B);
-  if (d == 128)
-    return launch_pdl(attn_split_kernel<128>, grid, dim3(kAtThreads), AtSmem<128>::kTotal, s, kmap, vmap, p);
-  return launch_pdl(attn_split_kernel<64>, grid, dim3(kAtThreads), AtSmem<64>::kTotal, s, kmap, vmap, p);
+  if (d == 128) return launch_attention_d<128>(q, kc, vc, ctx_len, B, Q, L, nh, scale, out, ws, dc, s);
+  return launch_attention_d<64>(q, kc, vc, ctx_len, B, Q, L, nh, scale, out, ws, dc, s);
 }
 
 }  // namespace lsv
