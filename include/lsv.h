@@ -176,7 +176,7 @@ lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t
  *     out[b,j,h] = sum_{t <= p} softmax_t(scale * q[b,j,h].k[b,t,h]) v[b,t,h],
  *     p = ctx_len[b] - Q + j (query j sees the cache up to and including itself)
  * fp32 scores and accumulation.  Supported: d in {64, 128}, 1 <= Q <= 8,
- * B, nh <= 65535, B*nh <= 262144, scale > 0.  Cache entries at or past
+ * L <= 65536, B, nh <= 65535, B*nh <= 262144, scale > 0.  Cache entries at or past
  * ctx_len[b] are never used, whatever they hold.  A ctx_len outside [Q, L] raises
  * LSV_ERR_DEVICE_INDEX (that sequence's output is zero).
  * Device pointers, 16-byte aligned.

@@ -367,7 +367,7 @@ lsv_status moe_verify_layer(const void* x, const lsv_moe_weights* wt, const lsv_
 }
 
 size_t spec_verify_attention_workspace_size(int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d) {
-  if (B < 0 || Q < 1 || Q > kMaxAttnQ || L < Q || nh < 1 || (d != 64 && d != 128)) return 0;
+  if (B < 0 || Q < 1 || Q > kMaxAttnQ || L < Q || L > kAttnMaxL || nh < 1 || (d != 64 && d != 128)) return 0;
   if ((long long)B * L * nh * d >= (1ll << 40) || (long long)B * nh > kAttnMaxPairs || nh > 65535 || B > 65535)
     return 0;
   return attention_ws_bytes(B, Q, L, nh, d);

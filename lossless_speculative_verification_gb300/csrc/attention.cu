@@ -131,13 +131,14 @@ __global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_con
       const int per_split = p.B * p.nh;
       int k = 0;  // tiles (and the end record) put in the ring so far
       bool ok = true;
-      while (ok) {
-        const int item = atomicAdd(p.dealer, 1);
-        if (item >= p.total) break;
-        const int split = item / per_split;
-        const int bh = item - split * per_split;
+      int item = atomicAdd(p.dealer, 1);
+      for (; ok && item < p.total;) {
+        const int cur = item;
+        item = atomicAdd(p.dealer, 1);  // dealt one ahead: its latency hides behind this item's tiles
+        const int split = cur / per_split;
+        const int bh = cur - split * per_split;
         const int b = bh / p.nh, h = bh - b * p.nh;
-        const int n = p.ctx_len[b];
+        const int n = __ldg(p.ctx_len + b);
         const int t_begin = split * kAtChunk;
         if (n < p.Q || n > p.L || t_begin >= n) continue;  // nothing to stream (the combine reports bad lengths)
         const int ntiles = (min(n, t_begin + kAtChunk) - t_begin + kAtTile - 1) / kAtTile;
@@ -310,35 +311,67 @@ __global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_con
 }
 
 // Per (head, sequence): merge the warps' and splits' states and write the output.
+// Warp j finds query j's common maximum, the rescale factor of every state and
+// the normaliser; then every thread sums four output columns of one query over
+// the states (independent 16-byte loads).
+constexpr int kAcThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(D) attn_combine_kernel(const float* __restrict__ o_part,
-                                                         const float* __restrict__ ml_part,
-                                                         const int32_t* __restrict__ ctx_len, int Q, int L, int nh,
-                                                         int nsplit, bf16* __restrict__ out, int* dealer, int* err) {
+__global__ void __launch_bounds__(kAcThreads) attn_combine_kernel(const float* __restrict__ o_part,
+                                                                  const float* __restrict__ ml_part,
+                                                                  const int32_t* __restrict__ ctx_len, int Q, int L,
+                                                                  int nh, int nsplit, bf16* __restrict__ out,
+                                                                  int* dealer, int* err) {
+  extern __shared__ float fs[];  // [nparts][Q] rescale factors, then [Q] normalisers
   pdl_wait();
   pdl_trigger();
-  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
-  if (h == 0 && b == 0 && c == 0) *dealer = 0;  // the split kernel is done with it
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (h == 0 && b == 0 && threadIdx.x == 0) *dealer = 0;  // the split kernel is done with it
   const int n = ctx_len[b];
   const bool bad = n < Q || n > L;
-  if (bad && h == 0 && c == 0) set_error(err, kErrDeviceIndex);
+  if (bad && h == 0 && threadIdx.x == 0) set_error(err, kErrDeviceIndex);
   const int nparts = bad ? 0 : (n + kAtChunk - 1) / kAtChunk * kAtConsumers;
   const size_t base = ((size_t)b * nh + h) * nsplit * kAtConsumers;  // first state of (b, h)
-  for (int j = 0; j < Q; ++j) {
+  const float2* ml = reinterpret_cast<const float2*>(ml_part) + base * Q;
+  float* lsum = fs + nparts * Q;
+  for (int j = warp; j < Q; j += kAcThreads / 32) {
     float mm = -INFINITY;
-    for (int s = 0; s < nparts; ++s) mm = fmaxf(mm, ml_part[((base + s) * Q + j) * 2]);
-    float ls = 0.f, os = 0.f;
-    if (mm != -INFINITY) {
-      for (int s = 0; s < nparts; ++s) {
-        const size_t at = (base + s) * Q + j;
-        const float ms = ml_part[at * 2];
-        if (ms == -INFINITY) continue;
-        const float f = exp2f(ms - mm);
-        ls += ml_part[at * 2 + 1] * f;
-        os += o_part[at * D + c] * f;
-      }
+    for (int s = lane; s < nparts; s += 32) mm = fmaxf(mm, ml[s * Q + j].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+    float ls = 0.f;
+    for (int s = lane; s < nparts; s += 32) {
+      const float2 v = ml[s * Q + j];
+      const float f = v.x == -INFINITY ? 0.f : exp2f(v.x - mm);
+      fs[s * Q + j] = f;
+      ls += v.y * f;
     }
-    out[(((size_t)b * Q + j) * nh + h) * D + c] = __float2bfloat16_rn(ls > 0.f ? os / ls : 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    if (lane == 0) lsum[j] = ls;
+  }
+  __syncthreads();
+  const float4* o4 = reinterpret_cast<const float4*>(o_part) + base * Q * (D / 4);
+  for (int e = threadIdx.x; e < Q * (D / 4); e += kAcThreads) {
+    const int j = e / (D / 4), c4 = e - j * (D / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = 0; s < nparts; ++s) {
+      const float f = fs[s * Q + j];  // 0 for a state that saw no position (its sums are 0 too)
+      const float4 v = o4[(s * Q + j) * (D / 4) + c4];
+      acc.x = fmaf(v.x, f, acc.x);
+      acc.y = fmaf(v.y, f, acc.y);
+      acc.z = fmaf(v.z, f, acc.z);
+      acc.w = fmaf(v.w, f, acc.w);
+    }
+    const float inv = lsum[j] > 0.f ? 1.f / lsum[j] : 0.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + (((size_t)b * Q + j) * nh + h) * D + 4 * c4) = pk;
   }
 }
 
@@ -387,7 +420,8 @@ cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, co
   cudaError_t e = launch_pdl(attn_split_kernel<D>, dim3(grid), dim3(kAtThreads), AtSmem<D>::kTotal, s, kmap, vmap,
                              qmap, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_combine_kernel<D>, dim3(nh, B), dim3(D), 0, s, (const float*)p.o_part,
+  const size_t comb_smem = ((size_t)p.nsplit * kAtConsumers * Q + Q) * sizeof(float);
+  return launch_pdl(attn_combine_kernel<D>, dim3(nh, B), dim3(kAcThreads), comb_smem, s, (const float*)p.o_part,
                     (const float*)p.ml_part, ctx_len, Q, L, nh, p.nsplit, out, p.dealer, dc.err);
 }
 

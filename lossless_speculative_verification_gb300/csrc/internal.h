@@ -22,6 +22,7 @@ constexpr int kMaxHidden = 16384;
 constexpr int kMaxVerifyRows = 64;  // K + 1 per sequence
 constexpr int kMaxAttnQ = 8;        // verified positions per sequence in the attention
 constexpr int kAttnMaxPairs = 1 << 18;  // (sequence, head) pairs per attention call
+constexpr int kAttnMaxL = 1 << 16;      // cache capacity per sequence in the attention
 
 // Per-device state: the error word's device address and the SM count.
 struct DeviceCtx {
