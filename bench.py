@@ -148,7 +148,7 @@ STEP_SOURCES = {
     "attention": ("attention.cu", "ptx.cuh", "api.cu"),
 }
 STEP_BOUNDS = {"layer": ("route", "combine_kernel"), "lmhead": ("lmhead_argmax_kernel", "accept_finalize_kernel"),
-               "attention": ("attn_split_kernel", "attn_combine_kernel")}
+               "attention": ("attn_kernel", "attn_kernel")}
 
 
 def step_kind(workload):
@@ -473,7 +473,7 @@ class AttentionStep:
         self.ctx_len = torch.from_numpy(p.ctx_len).to(dev)
         self.ws = api.spec_verify_attention_workspace(self.B, self.Q, p.L, self.NH, self.D, dev)
         self.out = torch.empty_like(self.q)
-        self.launches = 2  # the split-cache pass, then the combine of the splits
+        self.launches = 1  # one persistent kernel: the stream over the caches and the merges
 
     @classmethod
     def host_only(cls, seed):
@@ -704,7 +704,8 @@ def result_line(args, step, m, world, cpu):
         kernel = ("lmhead_argmax_kernel (tcgen05 product of the output layer and the hidden rows, reduced "
                   "to each row's (max, first index) per 128-token vocabulary tile) + accept_finalize_kernel"
                   if step.name == "lmhead" else
-                  "attn_split_kernel (512 cached positions per CTA, online softmax in fp32) + attn_combine_kernel")
+                  "attn_kernel (persistent: TMA key/value tiles, warp MMAs for scores and weighted values, online "
+                  "softmax in fp32, merges of the split states in the same launch)")
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts, "algorithmic_flops": flops, "kernel": kernel,
                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}

@@ -181,12 +181,11 @@ lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t
  * LSV_ERR_DEVICE_INDEX (that sequence's output is zero).
  * Device pointers, 16-byte aligned.
  * ws: spec_verify_attention_workspace_size(B,Q,L,nh,d) bytes (0: unsupported).
- * Its first 256 bytes hold a work counter, at the same place for every shape:
- * zero before the first use; every call that raises no device error leaves it
- * zero again, so one workspace serves any later call whose size fits (zero it
- * again after an error).
- * Two launches (the stream over the caches, then the merge of its partial
- * states); a call may start before the previous work on the stream ends
+ * Its first 1 MiB + 256 bytes hold work counters, at the same place for every
+ * shape: zero before the first use; every call that raises no device error
+ * leaves them zero again, so one workspace serves any later call whose size
+ * fits (zero them again after an error).
+ * One launch; it may start before the previous work on the stream ends
  * (programmatic dependent launch) but reads nothing before that work is done. */
 size_t spec_verify_attention_workspace_size(int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d);
 lsv_status spec_verify_attention(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
