@@ -6,7 +6,7 @@ grouped SwiGLU experts, shared experts, combine) followed by greedy
 acceptance over the verifier's [32, 4, 129280] bf16 logits.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|prefill|sweep|stack]
+                    [--workload decode|prefill|sweep|stack|lmhead|attention]
 
 Prints one JSON line per measured configuration (rank 0; the default run
 prints exactly one).  `value` is tokens/s with all inputs resident in HBM;
@@ -19,8 +19,12 @@ same workload.
 
 Other workloads (not the default line):
   prefill  8 pages x (1,156 visual + 64 prompt) = 9,760 tokens through the layer
-  sweep    B in {1,4,8,16,32,64} x K in {1,2,3}: layer + acceptance, one line each
+  sweep    B in {1,4,8,16,32,64} x K in {0,1,2,3}: layer + acceptance, one line each, then one
+           "k_policy" line: per B, the K that maximises tau(K) * t(K=0) / t(K) with the pages'
+           conditional acceptances and the measured step times t (spec_k_policy)
   stack    11 layers (Zipf-skewed routing, residual + RMSNorm) at 64 x 4 tokens + acceptance
+  lmhead   the verifier's output layer fused with greedy verification at 32 x 4 positions
+  attention  causal attention of 32 x 4 verified positions over page-shaped caches
 """
 from __future__ import annotations
 
@@ -148,7 +152,7 @@ STEP_SOURCES = {
     "attention": ("attention.cu", "ptx.cuh", "api.cu"),
 }
 STEP_BOUNDS = {"layer": ("route", "combine_kernel"), "lmhead": ("lmhead_argmax_kernel", "accept_finalize_kernel"),
-               "attention": ("attn_kernel", "attn_kernel")}
+               "attention": ("attn_split_kernel", "attn_combine_kernel")}
 
 
 def step_kind(workload):
@@ -473,7 +477,7 @@ class AttentionStep:
         self.ctx_len = torch.from_numpy(p.ctx_len).to(dev)
         self.ws = api.spec_verify_attention_workspace(self.B, self.Q, p.L, self.NH, self.D, dev)
         self.out = torch.empty_like(self.q)
-        self.launches = 1  # one persistent kernel: the stream over the caches and the merges
+        self.launches = 2  # the persistent stream over the caches, then the merge of the splits
 
     @classmethod
     def host_only(cls, seed):
@@ -704,8 +708,8 @@ def result_line(args, step, m, world, cpu):
         kernel = ("lmhead_argmax_kernel (tcgen05 product of the output layer and the hidden rows, reduced "
                   "to each row's (max, first index) per 128-token vocabulary tile) + accept_finalize_kernel"
                   if step.name == "lmhead" else
-                  "attn_kernel (persistent: TMA key/value tiles, warp MMAs for scores and weighted values, online "
-                  "softmax in fp32, merges of the split states in the same launch)")
+                  "attn_split_kernel (persistent: TMA key/value tiles, warp MMAs for scores and weighted values, "
+                  "online softmax in fp32, one state per 512-position split) + attn_combine_kernel")
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts, "algorithmic_flops": flops, "kernel": kernel,
                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}
@@ -808,6 +812,24 @@ def oracle_sampler(w, seed):
     return sample
 
 
+def k_policy_line(step_ms):
+    """Per batch size, the number of drafts the library's policy picks from the measured verify
+    step times (K = 0 is the plain greedy step) and the pages' conditional acceptances."""
+    from lossless_speculative_verification_gb300 import api, synth
+    out = {}
+    for B in sorted({b for b, _ in step_ms}):
+        ks = sorted(k for b, k in step_ms if b == B)
+        if ks != list(range(len(ks))) or len(ks) < 2:
+            continue
+        cost = [step_ms[(B, k)] for k in ks]
+        a = list(synth.PAGE_ACCEPT[:len(ks) - 1])
+        k_best, tau, sp = api.spec_k_policy(a, cost)
+        out[str(B)] = {"step_ms": cost, "tau": [round(x, 4) for x in tau], "speedup": [round(x, 4) for x in sp],
+                       "k_best": k_best}
+    return {"metric": "k_policy", "note": "cost = one verify step of the MoE layer plus acceptance (no draft "
+            "block, no attention); acceptances 0.830/0.663/0.636 from the pages", "per_batch": out}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -851,6 +873,7 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.barrier()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    step_ms = {}
     for name, w, seed in workloads(args.workload):
         if name in SIDE_STEPS:
             step = SIDE_STEPS[name][0](seed + args.seed + 1000 * rank, dev)
@@ -865,8 +888,12 @@ def run_ours(args, rank, world, local):
             cpu = sampler(12.0 if args.workload != "sweep" else 2.0)
         if rank == 0:
             print(json.dumps(result_line(args, step, m, world, cpu)), flush=True)
+        if name == "sweep":
+            step_ms[(w.B, w.K)] = m["total_ms"] / args.steps
         del step
         torch.cuda.empty_cache()
+    if rank == 0 and step_ms:
+        print(json.dumps(k_policy_line(step_ms)), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

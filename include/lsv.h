@@ -181,11 +181,12 @@ lsv_status spec_verify_accept(const void *logits, const int32_t *drafts, int32_t
  * LSV_ERR_DEVICE_INDEX (that sequence's output is zero).
  * Device pointers, 16-byte aligned.
  * ws: spec_verify_attention_workspace_size(B,Q,L,nh,d) bytes (0: unsupported).
- * Its first 1 MiB + 256 bytes hold work counters, at the same place for every
- * shape: zero before the first use; every call that raises no device error
- * leaves them zero again, so one workspace serves any later call whose size
- * fits (zero them again after an error).
- * One launch; it may start before the previous work on the stream ends
+ * Its first 256 bytes hold a work counter, at the same place for every shape:
+ * zero before the first use; every call that raises no device error leaves it
+ * zero again, so one workspace serves any later call whose size fits (zero it
+ * again after an error).
+ * Two launches (the stream over the caches, then the merge of its partial
+ * states); a call may start before the previous work on the stream ends
  * (programmatic dependent launch) but reads nothing before that work is done. */
 size_t spec_verify_attention_workspace_size(int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d);
 lsv_status spec_verify_attention(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
@@ -207,6 +208,29 @@ size_t spec_verify_lmhead_workspace_size(int32_t B, int32_t K, int32_t V, int32_
 lsv_status spec_verify_lmhead(const void *hidden, const void *w_vocab, const int32_t *drafts, int32_t B, int32_t K,
                               int32_t V, int32_t H, int32_t *argmax_opt, int32_t *accept_len, int32_t *committed,
                               void *ws, size_t ws_bytes, lsv_stream stream);
+
+/* Choice of the number of drafts K (the pages' decomposition S = tau / c).
+ *   cond_accept [kmax] (host): a_i = P(draft i accepted | drafts 1..i-1 accepted), in [0, 1]
+ *   step_cost [kmax+1] (host): cost of one step with K drafts (drafting plus
+ *             verification), K = 0 being a plain greedy step; > 0, any unit
+ * tau(K) = sum_{i=0..K} prod_{j<=i} a_j is the mean number of tokens a step
+ * commits; speedup(K) = tau(K) * step_cost[0] / step_cost[K].  *k_best is the K
+ * of the largest speedup (the smaller K on equal values); tau_out and
+ * speedup_out (host, kmax+1 entries each) are optional.  Host only, no device
+ * work; 0 <= kmax <= 63. */
+lsv_status spec_k_policy(const double *cond_accept, int32_t kmax, const double *step_cost, int32_t *k_best,
+                         double *tau_out, double *speedup_out);
+
+/* Accumulate the accepted lengths of a batch (accept_len [B] int32, device, as
+ * spec_verify_accept writes them) into hist [K+1] int64 (device, 8-byte aligned):
+ * hist[L] += #{b : accept_len[b] == L}.  Not cleared by the call.  A length
+ * outside [0, K] raises LSV_ERR_DEVICE_INDEX and is not counted.  One launch. */
+lsv_status spec_accept_histogram(const int32_t *accept_len, int32_t B, int32_t K, int64_t *hist,
+                                 lsv_stream stream);
+
+/* Conditional acceptances from such a histogram (host copy):
+ * cond[i-1] = #(L >= i) / #(L >= i-1) for i = 1..K, 0 where nothing reached draft i. */
+lsv_status spec_cond_accept_from_histogram(const int64_t *hist, int32_t K, double *cond);
 
 /* spec_verify_accept without a workspace, for callers that cannot allocate
  * device memory when they verify: code that must not call cudaMalloc inside a

@@ -49,6 +49,9 @@ SIGNATURES = {
     "spec_verify_accept_noalloc": (I32, [P, P, I32, I32, I32, P, P, P, P]),
     "spec_verify_lmhead_workspace_size": (SZ, [I32, I32, I32, I32]),
     "spec_verify_attention_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
+    "spec_k_policy": (I32, [P, I32, P, P, P, P]),
+    "spec_accept_histogram": (I32, [P, I32, I32, P, P]),
+    "spec_cond_accept_from_histogram": (I32, [P, I32, P]),
     "spec_verify_attention": (I32, [P, P, P, P, I32, I32, I32, I32, I32, ctypes.c_float, P, P, SZ, P]),
     "spec_verify_lmhead": (I32, [P, P, P, I32, I32, I32, I32, P, P, P, P, SZ, P]),
     "rmsnorm_residual": (I32, [P, P, P, I32, I32, ctypes.c_float, P]),

@@ -167,6 +167,43 @@ def spec_verify_attention(q, k_cache, v_cache, ctx_len, ws, scale=None, out=None
     return out
 
 
+def spec_k_policy(cond_accept, step_cost):
+    """(k_best, tau [kmax+1], speedup [kmax+1]) from conditional acceptances and step costs."""
+    import numpy as np
+    a = np.ascontiguousarray(cond_accept, dtype=np.float64)
+    c = np.ascontiguousarray(step_cost, dtype=np.float64)
+    kmax = a.size
+    if c.size != kmax + 1:
+        raise ValueError("step_cost needs one entry per K = 0..kmax")
+    k = ctypes.c_int32(0)
+    tau = np.zeros(kmax + 1, np.float64)
+    sp = np.zeros(kmax + 1, np.float64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    check("spec_k_policy", _ffi.load().spec_k_policy(
+        a.ctypes.data_as(dp) if kmax else None, kmax, c.ctypes.data_as(dp), ctypes.byref(k),
+        tau.ctypes.data_as(dp), sp.ctypes.data_as(dp)))
+    return int(k.value), tau, sp
+
+
+def spec_accept_histogram(accept_len, K, hist=None, stream=None):
+    """Add the batch's accepted lengths to hist [K+1] int64 (device; created zeroed if None)."""
+    _need(accept_len, torch.int32, "accept_len")
+    if hist is None:
+        hist = torch.zeros(K + 1, dtype=torch.int64, device=accept_len.device)
+    check("spec_accept_histogram", _ffi.load().spec_accept_histogram(
+        _ptr(accept_len), accept_len.numel(), K, _ptr(hist), _stream(stream)))
+    return hist
+
+
+def spec_cond_accept_from_histogram(hist, K):
+    import numpy as np
+    h = np.ascontiguousarray(hist.cpu().numpy() if isinstance(hist, torch.Tensor) else hist, dtype=np.int64)
+    cond = np.zeros(max(K, 1), np.float64)
+    check("spec_cond_accept_from_histogram", _ffi.load().spec_cond_accept_from_histogram(
+        h.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), K, cond.ctypes.data_as(ctypes.POINTER(ctypes.c_double))))
+    return cond[:K]
+
+
 def spec_verify_lmhead_workspace(B, K, V, H, device=None) -> torch.Tensor:
     n = _ffi.load().spec_verify_lmhead_workspace_size(B, K, V, H)
     if n == 0:

@@ -8,20 +8,15 @@
 // positions, the step is a stream of the cache through the SMs: per cached
 // position and head it reads 2*d bf16 values and does 4*Q*d flops.
 //
-// One persistent kernel (as many CTAs as fit on the GPU) does it all.  Work
-// comes from two atomic dealers in the workspace:
-//   split items (split, sequence, head): up to kAtChunk cached positions of
-//     one head of one sequence, dealt split-major so the short last splits
-//     come last;
-//   merge items (sequence, head), dealt once the split items run out: the
-//     merge of that pair's partial states into the output, started when all
-//     of them are published (a counter per pair that every writing lane
-//     release-adds to).
-//   warp 4 (producer): deals items.  A split item's 64-position key and value
-//     tiles (the head's d columns of 64 cache rows, 128-byte swizzle) stream
-//     by TMA into a kAtStages ring without a gap between items; the first
-//     tile of an item also carries the item's query rows.  A merge item goes
-//     into the ring as a record once its states are complete.
+// attn_split_kernel: persistent CTAs (as many as fit on the GPU) take work
+// items (split, sequence, head) -- up to kAtChunk cached positions of one
+// head of one sequence -- from an atomic dealer, split-major so that the
+// short last splits come last.
+//   warp 4 (producer): deals items (one ahead) and streams their 64-position
+//     key and value tiles (the head's d columns of 64 cache rows, 128-byte
+//     swizzle) by TMA into a kAtStages ring, without a gap between items; the
+//     first tile of an item also carries the item's query rows.  A small
+//     record per stage tells the consumers what the stage holds.
 //   warps 0-3 (consumers): each takes 16 positions of every tile.  Scores
 //     S = q K^T and the weighted values P V run on the tensor cores as
 //     m16n8k16 warp MMAs whose 16 rows are the queries (rows >= Q are zero):
@@ -29,11 +24,12 @@
 //     query, in fp32, exp2 of log2e-scaled scores) turns it into P in the
 //     register layout the second MMA takes as its A operand, and the
 //     fragments of q and K (ldmatrix) and V (ldmatrix.trans) come from the
-//     swizzled tiles without bank conflicts.  At the end of a split item each
-//     warp writes its state (running maximum, sum, unnormalised output).  On
-//     a merge record they rescale the pair's states to their common maximum,
-//     sum them and write out = sum / normaliser in bf16.
-// The last CTA to leave rewinds the dealers; each merge clears its counter.
+//     swizzled tiles without bank conflicts.  At the end of an item the four
+//     warps put their states (running maximum, sum, unnormalised output) in
+//     the freed stage buffer and merge them into the item's one partial state.
+// attn_combine_kernel (programmatic dependent launch): per (sequence, head),
+// the splits' states rescaled to their common maximum and summed;
+// out = sum / normaliser in bf16.  It also rewinds the dealer.
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -49,16 +45,12 @@ constexpr int kAtTile = 64;  // positions per ring stage (16 per consumer warp)
 #endif
 constexpr int kAtStages = LSV_ATTN_STAGES;
 #ifndef LSV_ATTN_CHUNK
-#define LSV_ATTN_CHUNK 256
+#define LSV_ATTN_CHUNK 512
 #endif
-constexpr int kAtChunk = LSV_ATTN_CHUNK;  // cached positions per split item
+constexpr int kAtChunk = LSV_ATTN_CHUNK;  // cached positions per item
 static_assert(kAtChunk % kAtTile == 0, "an item is a whole number of tiles");
 constexpr float kLog2e = 1.4426950408889634f;
-// Control block at the start of the workspace: [0] split dealer, [1] merge dealer,
-// [2] CTAs finished, then one published-state counter per (sequence, head).
-constexpr int kAttnCtlInts = 64;
-constexpr size_t kAttnCtlBytes = ((size_t)kAttnCtlInts + kAttnMaxPairs) * 4;
-enum : int { kRecTile = 0, kRecMerge = 1, kRecEnd = 2 };
+constexpr int kAttnCtlInts = 64;  // dealer at [0]; the rest reserved
 
 template <int D>
 struct AtSmem {
@@ -66,25 +58,25 @@ struct AtSmem {
   static constexpr int kQBox = kMaxAttnQ * 128;    // 64 columns x 8 query rows
   static constexpr int kKV = 2 * (D / 64) * kBox;  // key boxes, then value boxes
   static constexpr int kStage = kKV + (D / 64) * kQBox;
+  static_assert(kAtConsumers * kMaxAttnQ * (D + 2) * 4 <= kStage, "the warps' states fit in a stage");
   static constexpr int kRing = kAtStages * kStage;
   static constexpr int kMeta = kAtStages * 32;
-  static constexpr int kBars = 2 * kAtStages * 8;
+  static constexpr int kBars = (2 * kAtStages + 1) * 8;
   static constexpr int kTotal = 1024 + kRing + kMeta + kBars + 16;
 };
 
 struct AtMeta {
-  int type, b, h, split, i, ntiles, n, pad;
+  int b, h, split, i, ntiles, n, end, pad;
 };
 
 struct AtParams {
   const int32_t* ctx_len;  // [B]
-  bf16* out;               // [B, Q, nh, D]
   int B, Q, L, nh, nsplit;
-  int total;       // nsplit * B * nh split items
+  int total;       // nsplit * B * nh items
   float qk_scale;  // scale * log2(e)
-  float* o_part;   // [B*nh, nsplit, warps, Q, D]
-  float* ml_part;  // [B*nh, nsplit, warps, Q, 2]: running maximum (log2 units), sum
-  int* ctl;        // control block; zero before the launch, zero after it
+  float* o_part;   // [B*nh, nsplit, Q, D]
+  float* ml_part;  // [B*nh, nsplit, Q, 2]: running maximum (log2 units), sum
+  int* dealer;     // zero before the launch; the combine rewinds it
   int* err;
   uint64_t wait_ns;
 };
@@ -98,13 +90,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // (128-byte swizzle: chunk c of row r sits at c ^ (r mod 8)).
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
-__device__ __forceinline__ int splits_of(int n) { return (n + kAtChunk - 1) / kAtChunk; }
-
 template <int D>
-__global__ void __launch_bounds__(kAtThreads) attn_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                          const __grid_constant__ CUtensorMap vmap,
-                                                          const __grid_constant__ CUtensorMap qmap,
-                                                          const AtParams p) {
+__global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                const __grid_constant__ CUtensorMap vmap,
+                                                                const __grid_constant__ CUtensorMap qmap,
+                                                                const AtParams p) {
   using SM = AtSmem<D>;
   constexpr int NB = D / 64;  // boxes per tensor per tile
   extern __shared__ uint8_t smem_raw[];
@@ -112,20 +102,18 @@ __global__ void __launch_bounds__(kAtThreads) attn_kernel(const __grid_constant_
   volatile AtMeta* meta = reinterpret_cast<volatile AtMeta*>(smem + SM::kRing);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kRing + SM::kMeta);
   uint64_t* empty = full + kAtStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kAtStages);
+  uint64_t* merge_bar = empty + kAtStages;  // the consumer warps meet here at the end of an item
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(merge_bar + 1);
   volatile int* issued_s = abort_flag + 1;
   int* done_s = const_cast<int*>(abort_flag + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* split_dealer = p.ctl;
-  int* merge_dealer = p.ctl + 1;
-  int* exit_count = p.ctl + 2;
-  int* published = p.ctl + kAttnCtlInts;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAtStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kAtConsumers);
     }
+    mbar_init(merge_bar, kAtConsumers);
     *abort_flag = 0;
     *issued_s = 0;
     *done_s = 1 << 30;
@@ -137,7 +125,7 @@ __global__ void __launch_bounds__(kAtThreads) attn_kernel(const __grid_constant_
     tma_prefetch_desc(&qmap);
   }
   __syncthreads();
-  pdl_wait();  // q, the lengths, the caches and the control block come from earlier work on the stream
+  pdl_wait();  // q, the lengths, the caches and the dealer come from earlier work on the stream
   pdl_trigger();
 
   if (warp == kAtConsumers) {
@@ -145,37 +133,35 @@ __global__ void __launch_bounds__(kAtThreads) attn_kernel(const __grid_constant_
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       const int per_split = p.B * p.nh;
-      int k = 0;  // records put in the ring so far
+      int k = 0;  // tiles (and the end record) put in the ring so far
       bool ok = true;
-      // claim the ring slot of record k (false: timed out)
-      auto claim = [&](int kk) {
-        if (mbar_wait(&empty[kk % kAtStages], ((kk / kAtStages) & 1) ^ 1u, p.wait_ns)) return true;
-        set_error(p.err, kErrTimeout);
-        *abort_flag = 1;
-        return false;
-      };
-      int item = atomicAdd(split_dealer, 1);
+      int item = atomicAdd(p.dealer, 1);
       while (ok && item < p.total) {
         const int cur = item;
-        item = atomicAdd(split_dealer, 1);  // dealt one ahead: its latency hides behind this item's tiles
+        item = atomicAdd(p.dealer, 1);  // dealt one ahead: its latency hides behind this item's tiles
         const int split = cur / per_split;
         const int bh = cur - split * per_split;
         const int b = bh / p.nh, h = bh - b * p.nh;
         const int n = __ldg(p.ctx_len + b);
         const int t_begin = split * kAtChunk;
-        if (n < p.Q || n > p.L || t_begin >= n) continue;  // nothing to stream (the merge reports bad lengths)
+        if (n < p.Q || n > p.L || t_begin >= n) continue;  // nothing to stream (the combine reports bad lengths)
         const int ntiles = (min(n, t_begin + kAtChunk) - t_begin + kAtTile - 1) / kAtTile;
         const int row0 = b * p.L + t_begin;
         for (int i = 0; i < ntiles; ++i, ++k) {
-          if (!(ok = claim(k))) break;
           const int s = k % kAtStages;
-          meta[s].type = kRecTile;
+          if (!mbar_wait(&empty[s], ((k / kAtStages) & 1) ^ 1u, p.wait_ns)) {
+            set_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
           meta[s].b = b;
           meta[s].h = h;
           meta[s].split = split;
           meta[s].i = i;
           meta[s].ntiles = ntiles;
           meta[s].n = n;
+          meta[s].end = 0;
           uint8_t* st = smem + s * SM::kStage;
           mbar_arrive_expect_tx(&full[s], SM::kKV + (i == 0 ? NB * SM::kQBox : 0));
 #pragma unroll
@@ -186,36 +172,16 @@ __global__ void __launch_bounds__(kAtThreads) attn_kernel(const __grid_constant_
           }
         }
       }
-      // merges, once every split item has been dealt
-      int m = ok ? atomicAdd(merge_dealer, 1) : per_split;
-      while (ok && m < per_split) {
-        const int cur = m;
-        m = atomicAdd(merge_dealer, 1);
-        const int b = cur / p.nh, h = cur - b * p.nh;
-        const int n = __ldg(p.ctx_len + b);
-        const bool bad = n < p.Q || n > p.L;
-        if (bad && h == 0) set_error(p.err, kErrDeviceIndex);
-        // every writing lane of every warp of every split of the pair publishes once
-        const int target = bad ? 0 : splits_of(n) * kAtConsumers * 4 * p.Q;
-        if (!wait_counter_geq(published + cur, target, p.wait_ns)) {
+      if (ok) {
+        // end record
+        const int s = k % kAtStages;
+        if (mbar_wait(&empty[s], ((k / kAtStages) & 1) ^ 1u, p.wait_ns)) {
+          meta[s].end = 1;
+          mbar_arrive(&full[s]);
+        } else {
           set_error(p.err, kErrTimeout);
           *abort_flag = 1;
-          ok = false;
-          break;
         }
-        published[cur] = 0;  // complete: nothing else adds to it in this launch
-        if (!(ok = claim(k))) break;
-        const int s = k % kAtStages;
-        meta[s].type = kRecMerge;
-        meta[s].b = b;
-        meta[s].h = h;
-        meta[s].n = bad ? 0 : n;
-        mbar_arrive(&full[s]);
-        ++k;
-      }
-      if (ok && claim(k)) {
-        meta[k % kAtStages].type = kRecEnd;
-        mbar_arrive(&full[k % kAtStages]);
       }
       *issued_s = k;
     }
@@ -233,6 +199,15 @@ __global__ void __launch_bounds__(kAtThreads) attn_kernel(const __grid_constant_
     float o[D / 8][2];
     float m_run = -INFINITY, l_run = 0.f;
     int lim = -1;
+    uint32_t merge_phase = 0;
+    // the consumer warps meet at the end of an item (bounded; false: timed out)
+    auto meet = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(merge_bar);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(merge_bar, merge_phase, p.wait_ns));
+      merge_phase ^= 1u;
+      return ok;
+    };
     for (int k = 0;; ++k) {
       const int s = k % kAtStages;
       // every lane waits; the warp leaves together if any lane ran out of time
@@ -244,72 +219,11 @@ __global__ void __launch_bounds__(kAtThreads) attn_kernel(const __grid_constant_
         *abort_flag = 1;
         break;
       }
-      const int type = meta[s].type;
-      if (type == kRecEnd) break;
-      const int b = meta[s].b, h = meta[s].h, n = meta[s].n;
-      if (type == kRecMerge) {
-        // ---------------------------------------------------- merge of (b, h)
-        // Every warp finds each query's common maximum and normaliser itself (no
-        // barrier between the warps), then sums its share of the output columns.
-        const int nparts = n == 0 ? 0 : splits_of(n) * kAtConsumers;
-        const size_t base = ((size_t)b * p.nh + h) * p.nsplit * kAtConsumers * p.Q;  // first state row
-        const float2* ml = reinterpret_cast<const float2*>(p.ml_part) + base;
-        float mmq[kMaxAttnQ], inv_l[kMaxAttnQ];
-#pragma unroll
-        for (int j = 0; j < kMaxAttnQ; ++j) {
-          mmq[j] = -INFINITY;
-          inv_l[j] = 0.f;
-          if (j >= p.Q) continue;
-          float mm = -INFINITY;
-          for (int sp = lane; sp < nparts; sp += 32) mm = fmaxf(mm, __ldcg(&ml[sp * p.Q + j].x));
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
-          float ls = 0.f;
-          if (mm != -INFINITY)
-            for (int sp = lane; sp < nparts; sp += 32) {
-              const float2 v = __ldcg(&ml[sp * p.Q + j]);
-              if (v.x != -INFINITY) ls += v.y * exp2f(v.x - mm);
-            }
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
-          mmq[j] = mm;
-          inv_l[j] = ls > 0.f ? 1.f / ls : 0.f;
-        }
-        const float4* o4 = reinterpret_cast<const float4*>(p.o_part) + base * (D / 4);
-        for (int e = threadIdx.x; e < p.Q * (D / 4); e += 32 * kAtConsumers) {
-          const int j = e / (D / 4), c4 = e - j * (D / 4);
-          float mm = -INFINITY, il = 0.f;
-#pragma unroll
-          for (int jj = 0; jj < kMaxAttnQ; ++jj)
-            if (jj == j) {
-              mm = mmq[jj];
-              il = inv_l[jj];
-            }
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (mm != -INFINITY) {
-#pragma unroll 4
-            for (int sp = 0; sp < nparts; ++sp) {
-              const float ms = __ldcg(&ml[sp * p.Q + j].x);
-              const float4 v = __ldcg(&o4[(sp * p.Q + j) * (D / 4) + c4]);
-              const float f = ms == -INFINITY ? 0.f : exp2f(ms - mm);  // a state that saw no position adds 0
-              acc.x = fmaf(v.x, f, acc.x);
-              acc.y = fmaf(v.y, f, acc.y);
-              acc.z = fmaf(v.z, f, acc.z);
-              acc.w = fmaf(v.w, f, acc.w);
-            }
-          }
-          uint2 pk;
-          pk.x = pack_bf16(acc.x * il, acc.y * il);
-          pk.y = pack_bf16(acc.z * il, acc.w * il);
-          *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.Q + j) * p.nh + h) * D + 4 * c4) = pk;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        continue;
-      }
-      // ------------------------------------------------------ a tile of a split item
-      const int split = meta[s].split, i = meta[s].i, ntiles = meta[s].ntiles;
-      const uint32_t kb = smem_u32(smem + s * SM::kStage);
+      if (meta[s].end) break;
+      const int b = meta[s].b, h = meta[s].h, split = meta[s].split, i = meta[s].i, n = meta[s].n;
+      const int ntiles = meta[s].ntiles;
+      uint8_t* stage = smem + s * SM::kStage;
+      const uint32_t kb = smem_u32(stage);
       const uint32_t vb = kb + NB * SM::kBox;
       if (i == 0) {
         // a new item: its queries as the A operand (row g = query g; k-step ks covers dims [16ks, 16ks+16))
@@ -386,38 +300,129 @@ __global__ void __launch_bounds__(kAtThreads) attn_kernel(const __grid_constant_
         mma_bf16_m16n8k16_top(o[2 * u], pa0, pa2, r[0], r[1]);
         mma_bf16_m16n8k16_top(o[2 * u + 1], pa0, pa2, r[2], r[3]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
       if (i == ntiles - 1) {
-        // the item's last tile: write this warp's state and publish it
+        // the item's last tile: merge the four warps' states through the stage buffer, once
+        // every warp is done reading the tile, into the item's one partial state
+        float* o_s = reinterpret_cast<float*>(stage);  // [warp][row][D]
+        float* ml_s = o_s + kAtConsumers * kMaxAttnQ * D;   // [warp][row][2]
+        if (!meet()) {
+          if (lane == 0) set_error(p.err, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
         float l = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
-        const size_t row = ((((size_t)b * p.nh + h) * p.nsplit + split) * kAtConsumers + warp) * p.Q + g;
         if (row_ok) {
-          float* op = p.o_part + row * D + 2 * t;
+          float* op = o_s + (warp * kMaxAttnQ + g) * D + 2 * t;
 #pragma unroll
-          for (int nt = 0; nt < D / 8; ++nt)
-            *reinterpret_cast<float2*>(op + 8 * nt) = make_float2(o[nt][0], o[nt][1]);
-          if (t == 0) *reinterpret_cast<float2*>(p.ml_part + row * 2) = make_float2(m_run, l);
-          red_release_gpu_add(published + b * p.nh + h, 1);
+          for (int nt = 0; nt < D / 8; ++nt) *reinterpret_cast<float2*>(op + 8 * nt) = make_float2(o[nt][0], o[nt][1]);
+          if (t == 0) *reinterpret_cast<float2*>(ml_s + (warp * kMaxAttnQ + g) * 2) = make_float2(m_run, l);
         }
+        if (!meet()) {
+          if (lane == 0) set_error(p.err, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        const size_t part = (((size_t)b * p.nh + h) * p.nsplit + split) * p.Q;
+        for (int e = threadIdx.x; e < p.Q * (D / 4); e += 32 * kAtConsumers) {
+          const int j = e / (D / 4), c4 = e - j * (D / 4);
+          float mw[kAtConsumers], mm = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kAtConsumers; ++w) {
+            mw[w] = ml_s[(w * kMaxAttnQ + j) * 2];
+            mm = fmaxf(mm, mw[w]);
+          }
+          float ls = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < kAtConsumers; ++w) {
+            const float f = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - mm);  // a warp that saw no position adds 0
+            const float4 v = *reinterpret_cast<const float4*>(o_s + (w * kMaxAttnQ + j) * D + 4 * c4);
+            ls += ml_s[(w * kMaxAttnQ + j) * 2 + 1] * f;
+            acc.x = fmaf(v.x, f, acc.x);
+            acc.y = fmaf(v.y, f, acc.y);
+            acc.z = fmaf(v.z, f, acc.z);
+            acc.w = fmaf(v.w, f, acc.w);
+          }
+          *reinterpret_cast<float4*>(p.o_part + (part + j) * D + 4 * c4) = acc;
+          if (c4 == 0) *reinterpret_cast<float2*>(p.ml_part + (part + j) * 2) = make_float2(mm, ls);
+        }
+        fence_proxy_async_shared();  // the states written here come before the next TMA fill of the stage
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
   __syncthreads();
-  if (*abort_flag) {
-    if (threadIdx.x == 0) {
-      // let the copies already issued land before the CTA's shared memory goes away
-      for (int kk = *done_s; kk < *issued_s; ++kk)
-        mbar_wait(&full[kk % kAtStages], (kk / kAtStages) & 1, p.wait_ns);
-    }
-    return;  // the control block needs zeroing again after an error
+  if (*abort_flag && threadIdx.x == 0) {
+    // let the copies already issued land before the CTA's shared memory goes away
+    for (int kk = *done_s; kk < *issued_s; ++kk) mbar_wait(&full[kk % kAtStages], (kk / kAtStages) & 1, p.wait_ns);
   }
-  if (threadIdx.x == 0 && atomicAdd(exit_count, 1) == (int)gridDim.x - 1) {
-    // every CTA is past its dealing: rewind for the next launch
-    *split_dealer = 0;
-    *merge_dealer = 0;
-    *exit_count = 0;
+}
+
+// Per (head, sequence): merge the splits' states and write the output.  Each
+// thread takes four output columns of one query and reads every split's state
+// of them (independent loads, issued together).
+constexpr int kAcThreads = 256;
+constexpr int kAcUnroll = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kAcThreads) attn_combine_kernel(const float* __restrict__ o_part,
+                                                                  const float* __restrict__ ml_part,
+                                                                  const int32_t* __restrict__ ctx_len, int Q, int L,
+                                                                  int nh, int nsplit, bf16* __restrict__ out,
+                                                                  int* dealer, int* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int h = blockIdx.x, b = blockIdx.y;
+  if (h == 0 && b == 0 && threadIdx.x == 0) *dealer = 0;  // the split kernel is done with it
+  const int n = ctx_len[b];
+  const bool bad = n < Q || n > L;
+  if (bad && h == 0 && threadIdx.x == 0) set_error(err, kErrDeviceIndex);
+  const int nparts = bad ? 0 : (n + kAtChunk - 1) / kAtChunk;
+  const size_t base = ((size_t)b * nh + h) * nsplit * Q;  // first state row of (b, h)
+  const float2* ml = reinterpret_cast<const float2*>(ml_part) + base;
+  const float4* o4 = reinterpret_cast<const float4*>(o_part) + base * (D / 4);
+  for (int e = threadIdx.x; e < Q * (D / 4); e += kAcThreads) {
+    const int j = e / (D / 4), c4 = e - j * (D / 4);
+    float mm = -INFINITY, ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nparts; s0 += kAcUnroll) {
+      float2 mlv[kAcUnroll];
+      float4 v[kAcUnroll];
+#pragma unroll
+      for (int u = 0; u < kAcUnroll; ++u) {
+        const bool in = s0 + u < nparts;
+        mlv[u] = in ? ml[(s0 + u) * Q + j] : make_float2(-INFINITY, 0.f);
+        v[u] = in ? o4[((s0 + u) * Q + j) * (D / 4) + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      // fold this group into the running (maximum, sum, output)
+      float gm = mm;
+#pragma unroll
+      for (int u = 0; u < kAcUnroll; ++u) gm = fmaxf(gm, mlv[u].x);
+      if (gm == -INFINITY) continue;
+      const float r = mm == -INFINITY ? 0.f : exp2f(mm - gm);
+      ls *= r;
+      acc.x *= r;
+      acc.y *= r;
+      acc.z *= r;
+      acc.w *= r;
+#pragma unroll
+      for (int u = 0; u < kAcUnroll; ++u) {
+        const float f = mlv[u].x == -INFINITY ? 0.f : exp2f(mlv[u].x - gm);
+        ls = fmaf(mlv[u].y, f, ls);
+        acc.x = fmaf(v[u].x, f, acc.x);
+        acc.y = fmaf(v[u].y, f, acc.y);
+        acc.z = fmaf(v[u].z, f, acc.z);
+        acc.w = fmaf(v[u].w, f, acc.w);
+      }
+      mm = gm;
+    }
+    const float inv = ls > 0.f ? 1.f / ls : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+    pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(out + (((size_t)b * Q + j) * nh + h) * D + 4 * c4) = pk;
   }
 }
 
@@ -431,16 +436,15 @@ cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, co
   if (dc.device < 0 || dc.device >= 64) return cudaErrorInvalidDevice;
   if (!grid_per_sm[dc.device]) {
     cudaError_t e =
-        cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, AtSmem<D>::kTotal);
+        cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, AtSmem<D>::kTotal);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_kernel<D>, kAtThreads, AtSmem<D>::kTotal);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_kernel<D>, kAtThreads, AtSmem<D>::kTotal);
     if (e != cudaSuccess) return e;
     grid_per_sm[dc.device] = per_sm > 0 ? per_sm : 1;
   }
   AtParams p;
   p.ctx_len = ctx_len;
-  p.out = out;
   p.B = B;
   p.Q = Q;
   p.L = L;
@@ -448,11 +452,11 @@ cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, co
   p.nsplit = attention_splits(L);
   p.total = p.nsplit * B * nh;
   p.qk_scale = scale * kLog2e;
-  const size_t parts = (size_t)B * nh * p.nsplit * kAtConsumers * Q;
+  const size_t parts = (size_t)B * nh * p.nsplit * Q;
   uint8_t* w = reinterpret_cast<uint8_t*>(ws);
-  p.ctl = reinterpret_cast<int*>(w);
-  p.o_part = reinterpret_cast<float*>(w + round256(kAttnCtlBytes));
-  p.ml_part = reinterpret_cast<float*>(w + round256(kAttnCtlBytes) + round256(parts * D * 4));
+  p.dealer = reinterpret_cast<int*>(w);
+  p.o_part = reinterpret_cast<float*>(w + round256(kAttnCtlInts * 4));
+  p.ml_part = reinterpret_cast<float*>(w + round256(kAttnCtlInts * 4) + round256(parts * D * 4));
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();
   // the caches as [B*L rows, nh*d columns] (a tile: d columns of 64 rows), the queries as
@@ -462,11 +466,13 @@ cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, co
       !make_map(&vmap, vc, (uint64_t)B * L, (uint64_t)nh * D, kAtTile) ||
       !make_map(&qmap, q, (uint64_t)B * Q, (uint64_t)nh * D, kMaxAttnQ))
     return cudaErrorInvalidValue;
-  // every CTA must be resident at once: a merge waits for split items held by other CTAs
   const long long cap = (long long)grid_per_sm[dc.device] * dc.num_sms;
-  const long long want = (long long)p.total + (long long)B * nh;
-  const int grid = (int)(want < cap ? want : cap);
-  return launch_pdl(attn_kernel<D>, dim3(grid), dim3(kAtThreads), AtSmem<D>::kTotal, s, kmap, vmap, qmap, p);
+  const int grid = (int)(p.total < cap ? p.total : cap);
+  cudaError_t e = launch_pdl(attn_split_kernel<D>, dim3(grid), dim3(kAtThreads), AtSmem<D>::kTotal, s, kmap, vmap,
+                             qmap, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_combine_kernel<D>, dim3(nh, B), dim3(kAcThreads), 0, s, (const float*)p.o_part,
+                    (const float*)p.ml_part, ctx_len, Q, L, nh, p.nsplit, out, p.dealer, dc.err);
 }
 
 }  // namespace
@@ -474,8 +480,8 @@ cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, co
 int attention_splits(int L) { return L <= 0 ? 1 : (L + kAtChunk - 1) / kAtChunk; }
 
 size_t attention_ws_bytes(int B, int Q, int L, int nh, int d) {
-  const size_t parts = (size_t)B * nh * attention_splits(L) * kAtConsumers * Q;
-  return round256(kAttnCtlBytes) + round256(parts * d * 4) + round256(parts * 2 * 4);
+  const size_t parts = (size_t)B * nh * attention_splits(L) * Q;
+  return round256(kAttnCtlInts * 4) + round256(parts * d * 4) + round256(parts * 2 * 4);
 }
 
 cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, const int32_t* ctx_len, int B, int Q,

@@ -170,6 +170,9 @@ size_t attention_ws_bytes(int B, int Q, int L, int nh, int d);
 cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, const int32_t* ctx_len, int B, int Q,
                              int L, int nh, int d, float scale, bf16* out, void* ws, const DeviceCtx& dc,
                              cudaStream_t s);
+// Counts of the accepted lengths of a batch into hist [K+1].
+cudaError_t launch_accept_histogram(const int32_t* accept_len, int B, int K, int64_t* hist, int* err,
+                                    cudaStream_t s);
 // The verifier's output layer fused with the greedy-token search, then acceptance.
 size_t lmhead_ws_bytes(int B, int K, int V);
 cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const int32_t* drafts, int B, int K,

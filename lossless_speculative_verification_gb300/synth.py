@@ -36,7 +36,7 @@ PAGE_ACCEPT = (0.830, 0.663, 0.636)
 
 VOCAB = 129_280          # decoder vocabulary of the DeepSeek-OCR family decoder
 SWEEP_B = (1, 4, 8, 16, 32, 64)
-SWEEP_K = (1, 2, 3)
+SWEEP_K = (0, 1, 2, 3)   # K = 0: the plain greedy step
 
 
 # --------------------------------------------------------------------------- bf16 bits

@@ -25,6 +25,12 @@ Pins (checked by tests marked "not gpu"):
                 value), identical keys (the mean of the values), causality
                 (later keys change nothing), torch scaled_dot_product_attention
                 in fp64 with an explicit mask
+  k_policy   -- the pages' tau = 2.73 / 2.74 from their conditional
+                acceptances; a Monte Carlo decode loop (Bernoulli draft
+                acceptances, per-K step costs) whose measured tokens per unit
+                cost and best K match S = tau / c; the acceptance estimate
+                recovers the simulated acceptances and tau equals the mean
+                committed count
 """
 from __future__ import annotations
 
@@ -287,3 +293,39 @@ def verify_attention(q, k_cache, v_cache, ctx_len, scale):
             w /= w.sum(axis=1, keepdims=True)
             out[b, j] = np.einsum("ht,thd->hd", w, vf[b, :p + 1])
     return out
+
+
+# ----------------------------------------------------------------------------- K policy
+def k_policy(cond_accept, step_cost):
+    """The number of drafts K that maximises the speedup S = tau / c (evolve.pub review,
+    Table 8 decomposition), from conditional acceptances a_1..a_kmax and the costs c_0..c_kmax
+    of a step with K drafts (c_0: a plain greedy step).
+
+    tau(K) = 1 + a_1 + a_1 a_2 + ... + a_1 ... a_K (tokens a step commits on average: the
+    accepted prefix plus the correction or bonus token), S(K) = tau(K) c_0 / c_K.
+    Returns (k_best, tau [kmax+1], S [kmax+1]); equal speedups keep the smaller K.
+    """
+    a = [float(x) for x in cond_accept]
+    c = [float(x) for x in step_cost]
+    assert len(c) == len(a) + 1
+    tau = []
+    for K in range(len(c)):
+        prefix_probs = [float(np.prod(a[:i])) for i in range(K + 1)]   # P(first i drafts accepted)
+        tau.append(sum(prefix_probs))
+    S = [tau[K] * c[0] / c[K] for K in range(len(c))]
+    k_best = 0
+    for K in range(1, len(c)):
+        if S[K] > S[k_best]:
+            k_best = K
+    return k_best, np.array(tau), np.array(S)
+
+
+def cond_accept_from_lengths(lengths, K):
+    """a_i = P(draft i accepted | drafts 1..i-1 accepted), counted from accepted lengths L:
+    #(L >= i) / #(L >= i-1) for i = 1..K (0 where no step reached draft i)."""
+    L = np.asarray(lengths, np.int64)
+    out = []
+    for i in range(1, K + 1):
+        reached = int(np.count_nonzero(L >= i - 1))
+        out.append(np.count_nonzero(L >= i) / reached if reached else 0.0)
+    return np.array(out)

@@ -194,6 +194,22 @@ def test_layer_parity(name, nsample):
     assert_layer_close(bf16_f64(from_dev_bf16(out))[toks], ref, name)
 
 
+@pytest.mark.parametrize("B,K", [(1, 0), (4, 0), (1, 1)])
+def test_layer_parity_smallest_batches(B, K):
+    # the plain greedy step (K = 0) of the sweep: one to four tokens through the decode layer
+    w = synth.sweep_workload(B, K)
+    d = w.dims
+    prob = synth.moe_problem(w, seed=synth.sweep_seed(B, K), row_ok=oracle.gap_ok(d.k))
+    P = DevProblem(prob)
+    idx = torch.empty((d.T, d.k), dtype=torch.int32, device="cuda")
+    out = api.moe_verify_layer(P.x, P.wts, P.sh, P.ws, topk_idx=idx)
+    torch.cuda.synchronize()
+    ref, ref_idx, _ = oracle.moe_layer(prob.x, prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up,
+                                       prob.ws_down, d.k, d.S)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    assert_layer_close(bf16_f64(from_dev_bf16(out)), ref, "T=%d" % d.T)
+
+
 def test_layer_workspace_reuse_across_shapes():
     # one workspace for calls of different shapes and paths: every call must leave the counter
     # block at zero for the next one

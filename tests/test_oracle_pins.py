@@ -499,3 +499,53 @@ def test_attention_matches_torch_sdpa():
         mask = torch.arange(L)[None, :] <= pos                      # [Q, L]
         ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
         np.testing.assert_allclose(out[b], ref.permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- K policy
+def test_k_policy_tau_matches_the_pages():
+    page = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_numbers.json")))
+    a = page["conditional_accept_k3"]["value"]
+    _, tau, S = oracle.k_policy(a, [1.0, 1.0, 1.0, 1.0])
+    assert abs(tau[3] - page["tau_k3"]["value"]) < 0.005
+    assert abs(tau[3] - page["tau_k3_graph"]["value"]) < 0.011
+    assert tau[0] == 1.0 and abs(tau[1] - (1 + a[0])) < 1e-15
+    np.testing.assert_allclose(S, tau)      # equal costs: the speedup is tau itself
+
+
+def _simulate(a, cost, K, steps, rng):
+    """Speculative decoding with Bernoulli conditional acceptances: tokens per unit cost."""
+    L = np.zeros(steps, np.int64)
+    alive = np.ones(steps, bool)
+    for i in range(K):
+        alive &= rng.random(steps) < a[i]
+        L += alive
+    return (L + 1).sum() / (steps * cost[K]), L
+
+
+def test_k_policy_matches_a_simulated_decode_loop():
+    rng = np.random.default_rng(11)
+    a = [0.83, 0.663, 0.636]
+    for cost in ([1.0, 1.3, 1.6, 1.9], [1.0, 1.05, 1.3, 2.2], [1.0, 1.8, 2.6, 3.4]):
+        k_best, tau, S = oracle.k_policy(a, cost)
+        greedy = 1.0 / cost[0]
+        emp = []
+        for K in range(4):
+            rate, _ = _simulate(a, cost, K, 200_000, rng)
+            emp.append(rate / greedy)
+        emp = np.array(emp)
+        np.testing.assert_allclose(emp, S, rtol=0.01)
+        assert int(np.argmax(emp)) == k_best
+    # the graph-mode finding: with dear drafts K = 1 wins although tau grows with K
+    k_best, tau, S = oracle.k_policy(a, [1.0, 1.56, 2.2, 2.5])
+    assert k_best == 1 and tau[3] > tau[1]
+
+
+def test_cond_accept_estimate():
+    rng = np.random.default_rng(12)
+    a = [0.83, 0.663, 0.636]
+    _, L = _simulate(a, [1, 1, 1, 1], 3, 400_000, rng)
+    est = oracle.cond_accept_from_lengths(L, 3)
+    np.testing.assert_allclose(est, a, atol=0.004)
+    _, tau, _ = oracle.k_policy(est, [1, 1, 1, 1])
+    assert abs(tau[3] - (L + 1).mean()) < 1e-12   # tau of the estimate = the mean committed count
+    assert list(oracle.cond_accept_from_lengths(np.zeros(5, int), 2)) == [0.0, 0.0]
