@@ -709,7 +709,7 @@ def result_line(args, step, m, world, cpu):
                   "to each row's (max, first index) per 128-token vocabulary tile) + accept_finalize_kernel"
                   if step.name == "lmhead" else
                   "attn_split_kernel (persistent: TMA key/value tiles, warp MMAs for scores and weighted values, "
-                  "online softmax in fp32, one state per 512-position split) + attn_combine_kernel")
+                  "online softmax in fp32, one state per 256-position split) + attn_combine_kernel")
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts, "algorithmic_flops": flops, "kernel": kernel,
                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}

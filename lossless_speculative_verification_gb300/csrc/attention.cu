@@ -45,7 +45,7 @@ constexpr int kAtTile = 64;  // positions per ring stage (16 per consumer warp)
 #endif
 constexpr int kAtStages = LSV_ATTN_STAGES;
 #ifndef LSV_ATTN_CHUNK
-#define LSV_ATTN_CHUNK 512
+#define LSV_ATTN_CHUNK 256
 #endif
 constexpr int kAtChunk = LSV_ATTN_CHUNK;  // cached positions per item
 static_assert(kAtChunk % kAtTile == 0, "an item is a whole number of tiles");
