@@ -31,6 +31,11 @@ Pins (checked by tests marked "not gpu"):
                 cost and best K match S = tau / c; the acceptance estimate
                 recovers the simulated acceptances and tau equals the mean
                 committed count
+  draft_block -- torch fp64 formulation (rms_norm, linear,
+                scaled_dot_product_attention, silu, argmax); with attention
+                and FFN switched off it is the (pinned) output-layer oracle;
+                zero queries give the mean of the visible values; the K-step
+                loop is the chained block
 """
 from __future__ import annotations
 
@@ -329,3 +334,101 @@ def cond_accept_from_lengths(lengths, K):
         reached = int(np.count_nonzero(L >= i - 1))
         out.append(np.count_nonzero(L >= i) / reached if reached else 0.0)
     return np.array(out)
+
+
+# ----------------------------------------------------------------------------- FastMTP draft block
+def _rms64(x, eps=1e-6):
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+
+
+def _silu64(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def _round_bf16(x, on):
+    """bf16 round-to-nearest-even of a float64 array through float32 (the storage points of the
+    draft block's kernels), or x unchanged."""
+    if not on:
+        return x
+    f = np.asarray(x, np.float64).astype(np.float32)
+    u = f.view(np.uint32)
+    u = ((u + (((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF))) >> np.uint32(16)) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=True, eps=1e-6):
+    """One application of the shared FastMTP draft block to every sequence (kg.zhiyong.dev, "The
+    speed comes from three layers working together": one dense draft block proposes the drafts;
+    evolve.pub review, "Scope & Claims": one shared block applied recursively).
+
+    The pages fix no more than that; the reading (an MTP module of the decoder's family):
+        u  = W_p [RMSNorm(h_prev); RMSNorm(E[tok_prev])]
+        a  = RMSNorm(u);  q, k, v = W_q a, W_k a, W_v a       (nh heads of d = H / nh)
+        the block's cache of the sequence gets k, v at position ctx_len[b]; q attends to
+        positions 0..ctx_len[b] (softmax with scale 1/sqrt(d))
+        u  = u + W_o attn
+        f  = RMSNorm(u);  u = u + W_down (silu(W_gate f) * (W_up f))
+        h_next = u;  draft = argmax_v (W_vocab RMSNorm(u))_v   (the first index of the maximum)
+    RMSNorm has unit weight.  With round_bf16 the values the kernels store (the normalised
+    input, u, a, q, k, v, the attention output, f, the activation, the final normalised state)
+    are rounded to bf16; every sum is exact in float64.
+
+    h_prev [B, H] float64 or bf16 bits; tok_prev [B] int; w: dict of bf16-bit arrays emb [V, H],
+    w_proj [H, 2H], w_q, w_k, w_v, w_o [H, H], w_gate_up [2I, H] (gate rows, then up rows),
+    w_down [H, I], w_vocab [V, H]; k_cache, v_cache [B, L, nh, d] float64 (updated in place at
+    position ctx_len[b]); ctx_len [B].
+    Returns (h_next [B, H] float64, draft [B] int32, gap [B]: top-two logit difference).
+    """
+    R = lambda x: _round_bf16(x, round_bf16)
+    f64 = lambda u: _bf16_to_f64(w[u]) if w[u].dtype == np.uint16 else np.asarray(w[u], np.float64)
+    h = np.asarray(h_prev, np.float64) if np.asarray(h_prev).dtype != np.uint16 else _bf16_to_f64(h_prev)
+    B, H = h.shape
+    d = H // nh
+    E = f64("emb")
+    Wp, Wq, Wk, Wv, Wo = f64("w_proj"), f64("w_q"), f64("w_k"), f64("w_v"), f64("w_o")
+    Wgu, Wd, Wv_out = f64("w_gate_up"), f64("w_down"), f64("w_vocab")
+    I = Wd.shape[1]
+    tok = np.asarray(tok_prev, np.int64)
+    inp = R(np.concatenate([_rms64(h, eps), _rms64(E[tok], eps)], axis=1))      # [B, 2H]
+    u = R(inp @ Wp.T)
+    a = R(_rms64(u, eps))
+    q, k, v = R(a @ Wq.T), R(a @ Wk.T), R(a @ Wv.T)
+    attn = np.zeros((B, H))
+    for b in range(B):
+        n = int(ctx_len[b])
+        k_cache[b, n] = k[b].reshape(nh, d)
+        v_cache[b, n] = v[b].reshape(nh, d)
+        qs = q[b].reshape(nh, d)
+        s = np.einsum("hd,thd->ht", qs, k_cache[b, :n + 1]) / np.sqrt(d)
+        s -= s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=1, keepdims=True)
+        attn[b] = np.einsum("ht,thd->hd", p, v_cache[b, :n + 1]).reshape(H)
+    attn = R(attn)
+    u = R(u + attn @ Wo.T)
+    f = R(_rms64(u, eps))
+    act = R(_silu64(f @ Wgu[:I].T) * (f @ Wgu[I:].T))
+    u = R(u + act @ Wd.T)
+    hn = R(_rms64(u, eps))
+    logits = hn @ Wv_out.T
+    draft = np.argmax(logits, axis=1).astype(np.int32)
+    top2 = np.sort(logits, axis=1)[:, -2:] if logits.shape[1] > 1 else np.concatenate([logits, logits], 1)
+    return u, draft, top2[:, 1] - top2[:, 0]
+
+
+def draft_loop(h0, t0, w, k_cache, v_cache, ctx_len, nh, K, round_bf16=True):
+    """K recursive applications of the draft block: step i takes step i-1's output state and
+    draft token (step 1: the verifier's last hidden state and the last committed token), and
+    appends to the block's cache at ctx_len + i - 1.  Returns (drafts [B, K], gaps [B, K])."""
+    h = h0
+    t = np.asarray(t0, np.int64)
+    n = np.asarray(ctx_len, np.int64).copy()
+    B = n.size
+    drafts = np.zeros((B, K), np.int32)
+    gaps = np.zeros((B, K))
+    for i in range(K):
+        h, t, g = draft_block(h, t, w, k_cache, v_cache, n, nh, round_bf16=round_bf16)
+        drafts[:, i] = t
+        gaps[:, i] = g
+        n += 1
+    return drafts, gaps

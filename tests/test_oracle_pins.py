@@ -549,3 +549,94 @@ def test_cond_accept_estimate():
     _, tau, _ = oracle.k_policy(est, [1, 1, 1, 1])
     assert abs(tau[3] - (L + 1).mean()) < 1e-12   # tau of the estimate = the mean committed count
     assert list(oracle.cond_accept_from_lengths(np.zeros(5, int), 2)) == [0.0, 0.0]
+
+
+# ----------------------------------------------------------------------------- FastMTP draft block
+def _draft_weights(H=64, I=96, V=50, seed=0, std=0.1):
+    rs = np.random.default_rng(seed)
+    g = lambda *s: bits(rs.standard_normal(s) * std)
+    return dict(emb=bits(rs.standard_normal((V, H))), w_proj=g(H, 2 * H), w_q=g(H, H), w_k=g(H, H), w_v=g(H, H),
+                w_o=g(H, H), w_gate_up=g(2 * I, H), w_down=g(H, I), w_vocab=g(V, H))
+
+
+def _draft_inputs(B=3, H=64, nh=4, L=12, lens=(3, 7, 0), seed=1):
+    rs = np.random.default_rng(seed)
+    d = H // nh
+    h = val64(bits(rs.standard_normal((B, H))))
+    kc = val64(bits(rs.standard_normal((B, L, nh, d))))
+    vc = val64(bits(rs.standard_normal((B, L, nh, d))))
+    return h, rs.integers(0, 50, size=B), kc, vc, np.array(lens[:B])
+
+
+def test_draft_block_matches_torch_formulation():
+    w = _draft_weights()
+    h, t, kc, vc, n = _draft_inputs()
+    nh = 4
+    h1, draft, _ = oracle.draft_block(h, t, w, kc.copy(), vc.copy(), n, nh, round_bf16=False)
+    T = lambda u: torch.from_numpy(val64(w[u]))
+    rms = lambda x: F.rms_norm(x, (x.shape[-1],), eps=1e-6)
+    x = torch.cat([rms(torch.from_numpy(h)), rms(T("emb")[torch.from_numpy(t)])], dim=1)
+    u = F.linear(x, T("w_proj"))
+    a = rms(u)
+    q, k, v = F.linear(a, T("w_q")), F.linear(a, T("w_k")), F.linear(a, T("w_v"))
+    B, H = u.shape
+    d = H // nh
+    att = torch.zeros(B, H, dtype=torch.float64)
+    for b in range(B):
+        m = int(n[b])
+        ks = torch.cat([torch.from_numpy(kc[b, :m]), k[b].view(1, nh, d)]).permute(1, 0, 2)   # [nh, m+1, d]
+        vs = torch.cat([torch.from_numpy(vc[b, :m]), v[b].view(1, nh, d)]).permute(1, 0, 2)
+        att[b] = F.scaled_dot_product_attention(q[b].view(nh, 1, d), ks, vs).reshape(H)
+    u = u + F.linear(att, T("w_o"))
+    f = rms(u)
+    I = w["w_down"].shape[1]
+    u = u + F.linear(F.silu(F.linear(f, T("w_gate_up")[:I])) * F.linear(f, T("w_gate_up")[I:]), T("w_down"))
+    logits = F.linear(rms(u), T("w_vocab"))
+    np.testing.assert_allclose(h1, u.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(draft, torch.argmax(logits, dim=1).numpy())
+
+
+def test_draft_block_without_attention_and_ffn_is_the_output_layer():
+    # W_p = [I | 0], W_o = 0, W_down = 0: the block passes RMSNorm(h) through, so its draft is the
+    # output layer's greedy token of RMSNorm(RMSNorm(h)) -- the (separately pinned) lmhead oracle
+    H = 64
+    w = _draft_weights(H=H)
+    w["w_proj"] = bits(np.concatenate([np.eye(H), np.zeros((H, H))], axis=1))
+    w["w_o"] = bits(np.zeros((H, H)))
+    w["w_down"] = bits(np.zeros((H, 96)))
+    h, t, kc, vc, n = _draft_inputs(H=H)
+    h1, draft, _ = oracle.draft_block(h, t, w, kc, vc, n, 4)
+    hn = oracle._round_bf16(oracle._rms64(h1), True)
+    g, _ = oracle.lmhead_argmax(bits(hn), w["w_vocab"])
+    np.testing.assert_array_equal(draft, g)
+    np.testing.assert_array_equal(h1, oracle._round_bf16(oracle._rms64(h), True))
+
+
+def test_draft_block_attention_with_zero_queries_is_the_mean_value():
+    # W_q = 0: every visible cache entry gets the same weight; W_o = I and W_down = 0 expose the
+    # attention output as h_next - u
+    H, nh = 64, 4
+    w = _draft_weights(H=H)
+    w["w_q"] = bits(np.zeros((H, H)))
+    w["w_o"] = bits(np.eye(H))
+    w["w_down"] = bits(np.zeros((H, 96)))
+    h, t, kc, vc, n = _draft_inputs(H=H)
+    kc2, vc2 = kc.copy(), vc.copy()
+    h1, _, _ = oracle.draft_block(h, t, w, kc2, vc2, n, nh, round_bf16=False)
+    x = np.concatenate([oracle._rms64(h), oracle._rms64(val64(w["emb"])[t])], axis=1)
+    u = x @ val64(w["w_proj"]).T
+    for b in range(3):
+        m = int(n[b])
+        mean_v = vc2[b, :m + 1].mean(axis=0).reshape(H)     # includes the entry the step appended
+        np.testing.assert_allclose(h1[b] - u[b], mean_v, rtol=1e-9, atol=1e-12)
+
+
+def test_draft_loop_chains_the_block():
+    w = _draft_weights()
+    h, t, kc, vc, n = _draft_inputs()
+    drafts, _ = oracle.draft_loop(h, t, w, kc.copy(), vc.copy(), n, 4, K=3)
+    kc2, vc2, hh, tt, nn = kc.copy(), vc.copy(), h, t, n.copy()
+    for i in range(3):
+        hh, tt, _ = oracle.draft_block(hh, tt, w, kc2, vc2, nn, 4)
+        np.testing.assert_array_equal(drafts[:, i], tt)
+        nn = nn + 1
