@@ -38,7 +38,7 @@ def _worker(rank, world, port, out):
 
 def test_slowest_replica_sets_the_job_time():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert out[0] == out[1] == [11.0, 30.0]
 
