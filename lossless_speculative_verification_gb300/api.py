@@ -159,8 +159,17 @@ def spec_verify_attention(q, k_cache, v_cache, ctx_len, ws, scale=None, out=None
     _need(ctx_len, torch.int32, "ctx_len")
     B, Q, nh, d = q.shape
     L = k_cache.shape[1]
+    if tuple(k_cache.shape) != (B, L, nh, d) or tuple(v_cache.shape) != (B, L, nh, d):
+        raise ValueError("k_cache and v_cache must be [B, L, nh, d] = [%d, L, %d, %d]" % (B, nh, d))
+    if tuple(ctx_len.shape) != (B,):
+        raise ValueError("ctx_len must be [B]")
+    for t, name in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     out = torch.empty_like(q) if out is None else out
+    if tuple(out.shape) != (B, Q, nh, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 [B, Q, nh, d] tensor")
     check("spec_verify_attention", _ffi.load().spec_verify_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(ctx_len), B, Q, L, nh, d, scale, _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream)))
