@@ -413,3 +413,46 @@ def attention_problem(B: int, Q: int, nh: int = ATTN_HEADS, d: int = ATTN_HEAD_D
     k = _normal_bf16(rs[1], (B, L, nh, d), qk_std)
     v = _normal_bf16(rs[2], (B, L, nh, d), 1.0)
     return AttentionProblem(B, Q, L, nh, d, q, k, v, ctx_len)
+
+
+# --------------------------------------------------------------------------- FastMTP draft block
+DRAFT_FFN = 7_168   # (top-6 + 2 shared) x 896: the width the MoE layer activates per token
+
+
+@dataclass
+class DraftProblem:
+    B: int
+    K: int
+    H: int
+    nh: int
+    I: int
+    V: int
+    L: int
+    weights: dict        # bf16 bits: emb, w_proj, w_q, w_k, w_v, w_o, w_gate_up, w_down, w_vocab
+    h0: np.ndarray       # [B, H] bf16 bits: the verifier's last hidden state of every sequence
+    t0: np.ndarray       # [B] int32: the last committed token
+    k_cache: np.ndarray  # [B, L, nh, d] bf16 bits: the draft block's own cache
+    v_cache: np.ndarray
+    ctx_len: np.ndarray  # [B] int32 entries already in the block's cache (room for K more)
+
+
+def draft_problem(B: int, K: int = 3, H: int = 1280, nh: int = ATTN_HEADS, I: int = DRAFT_FFN, V: int = VOCAB,
+                  seed: int = 0, lens=None, std: float = 0.02) -> DraftProblem:
+    """Synthetic inputs of the recursive draft block: weights N(0, std) (the embedding N(0, 1)),
+    unit-RMS hidden states, uniform last tokens, block caches N(0, 1) with the page recipe's
+    lengths (visual prefix + text so far) and room for the K appended entries."""
+    rs = streams(seed, 14)
+    names = ["w_proj", "w_q", "w_k", "w_v", "w_o", "w_gate_up", "w_down", "w_vocab"]
+    shapes = [(H, 2 * H), (H, H), (H, H), (H, H), (H, H), (2 * I, H), (H, I), (V, H)]
+    wts = {n: _normal_bf16(r, s, std) for n, s, r in zip(names, shapes, rs[:8])}
+    wts["emb"] = _normal_bf16(rs[8], (V, H), 1.0)
+    h0 = hidden_rows(rs[9], B, H, "sphere")
+    t0 = rs[10].integers(0, V, size=B).astype(np.int32)
+    if lens is None:
+        lens = page_context_lengths(rs[11], B, 1) - 1
+    lens = np.asarray(lens, np.int32)
+    L = (int(lens.max()) + K + 63) // 64 * 64
+    d = H // nh
+    kc = _normal_bf16(rs[12], (B, L, nh, d), 1.0)
+    vc = _normal_bf16(rs[13], (B, L, nh, d), 1.0)
+    return DraftProblem(B, K, H, nh, I, V, L, wts, h0, t0, kc, vc, lens)

@@ -640,3 +640,17 @@ def test_draft_loop_chains_the_block():
         hh, tt, _ = oracle.draft_block(hh, tt, w, kc2, vc2, nn, 4)
         np.testing.assert_array_equal(drafts[:, i], tt)
         nn = nn + 1
+
+
+def test_draft_problem_shapes_and_oracle_run():
+    p = synth.draft_problem(2, K=3, H=128, nh=2, I=256, V=300, seed=4)
+    assert p.k_cache.shape == (2, p.L, 2, 64) and p.L >= int(p.ctx_len.max()) + 3
+    kc, vc = val64(p.k_cache), val64(p.v_cache)
+    drafts, gaps = oracle.draft_loop(p.h0, p.t0, p.weights, kc, vc, p.ctx_len, p.nh, p.K)
+    assert drafts.shape == (2, 3) and np.all((drafts >= 0) & (drafts < 300)) and np.all(gaps >= 0)
+    # the loop appended K entries per sequence to the block's cache and left the rest alone
+    for b in range(2):
+        n = int(p.ctx_len[b])
+        np.testing.assert_array_equal(kc[b, :n], val64(p.k_cache[b, :n]))
+        assert not np.array_equal(kc[b, n:n + 3], val64(p.k_cache[b, n:n + 3]))
+        np.testing.assert_array_equal(kc[b, n + 3:], val64(p.k_cache[b, n + 3:]))
