@@ -232,6 +232,50 @@ lsv_status spec_accept_histogram(const int32_t *accept_len, int32_t B, int32_t K
  * cond[i-1] = #(L >= i) / #(L >= i-1) for i = 1..K, 0 where nothing reached draft i. */
 lsv_status spec_cond_accept_from_histogram(const int64_t *hist, int32_t K, double *cond);
 
+/* Dense product y [M, N] = bf16(x [M, K] w [N, K]^T), bf16 inputs, fp32 accumulation
+ * (tcgen05).  Device pointers, 16-byte aligned; K % 64 == 0, K <= 16384,
+ * N % 8 == 0.  No workspace.  One launch. */
+lsv_status dense_matmul(const void *x, const void *w, void *y, int32_t M, int32_t N, int32_t K, lsv_stream stream);
+
+/* Weights of the FastMTP draft block (bf16, device, 16-byte aligned):
+ *   emb [V, H] (token embedding), w_proj [H, 2H], w_q, w_k, w_v, w_o [H, H],
+ *   w_gate_up [2I, H] (rows 0..I-1 gate, I..2I-1 up), w_down [H, I],
+ *   w_vocab [V, H] (the output layer, shared with the verifier). */
+typedef struct {
+  const void *emb;
+  const void *w_proj;
+  const void *w_q;
+  const void *w_k;
+  const void *w_v;
+  const void *w_o;
+  const void *w_gate_up;
+  const void *w_down;
+  const void *w_vocab;
+} lsv_draft_weights;
+
+/* K recursive applications of the shared draft block (one dense block that
+ * proposes the drafts the verify pass checks).  Step i takes the previous
+ * state h and token t (step 1: h0 [B, H] bf16, the verifier's last hidden
+ * state, and t0 [B] int32, the last committed token):
+ *   u = W_p [RMSNorm(h); RMSNorm(emb[t])];  a = RMSNorm(u)
+ *   q, k, v = W_q a, W_k a, W_v a;  k, v are written to the block's caches
+ *     k_cache, v_cache [B, L, nh, H/nh] bf16 at position ctx_len[b] + i - 1, and
+ *     q attends to positions 0..ctx_len[b] + i - 1 (scale 1/sqrt(H/nh))
+ *   u = u + W_o attn;  f = RMSNorm(u);  u = u + W_down (silu(W_gate f) * W_up f)
+ *   t = argmax_v (W_vocab RMSNorm(u))_v (the smallest index of the maximum), h = u
+ * RMSNorm: unit weight, eps 1e-6.  Every value between kernels is bf16.
+ * drafts [B, K] int32 (device) receives t of every step; h_out [B, H] bf16
+ * (optional) the last u.  ctx_len [B] int32 (device) is read, not written;
+ * ctx_len[b] + K <= L.  Supported: H % 64 == 0, H <= 16384, H/nh in {64, 128},
+ * I % 64 == 0, I <= 16384, 1 <= K <= 63.
+ * ws: spec_draft_workspace_size(B, H, nh, I, V, L) bytes, zero before the first
+ * use; calls that raise no device error leave it fit for the next call. */
+size_t spec_draft_workspace_size(int32_t B, int32_t H, int32_t nh, int32_t I, int32_t V, int32_t L);
+lsv_status spec_draft_loop(const lsv_draft_weights *weights, const void *h0, const int32_t *t0, void *k_cache,
+                           void *v_cache, const int32_t *ctx_len, int32_t B, int32_t K, int32_t H, int32_t nh,
+                           int32_t I, int32_t V, int32_t L, int32_t *drafts, void *h_out, void *ws, size_t ws_bytes,
+                           lsv_stream stream);
+
 /* spec_verify_accept without a workspace, for callers that cannot allocate
  * device memory when they verify: code that must not call cudaMalloc inside a
  * stream capture or a latency-critical decode loop, and plugin-style hosts

@@ -33,8 +33,14 @@ class MoeWeights(ctypes.Structure):
     _fields_ = [("w_router", P), ("w_gate_up", P), ("w_down", P), ("ws_gate_up", P), ("ws_down", P)]
 
 
+class DraftWeights(ctypes.Structure):
+    _fields_ = [("emb", P), ("w_proj", P), ("w_q", P), ("w_k", P), ("w_v", P), ("w_o", P), ("w_gate_up", P),
+                ("w_down", P), ("w_vocab", P)]
+
+
 SHAPE_P = ctypes.POINTER(MoeShape)
 WEIGHTS_P = ctypes.POINTER(MoeWeights)
+DRAFT_P = ctypes.POINTER(DraftWeights)
 
 SIGNATURES = {
     "lsv_workspace_size": (SZ, [SHAPE_P]),
@@ -50,6 +56,9 @@ SIGNATURES = {
     "spec_verify_lmhead_workspace_size": (SZ, [I32, I32, I32, I32]),
     "spec_verify_attention_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
     "spec_k_policy": (I32, [P, I32, P, P, P, P]),
+    "dense_matmul": (I32, [P, P, P, I32, I32, I32, P]),
+    "spec_draft_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32]),
+    "spec_draft_loop": (I32, [DRAFT_P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, P, P, P, SZ, P]),
     "spec_accept_histogram": (I32, [P, I32, I32, P, P]),
     "spec_cond_accept_from_histogram": (I32, [P, I32, P]),
     "spec_verify_attention": (I32, [P, P, P, P, I32, I32, I32, I32, I32, ctypes.c_float, P, P, SZ, P]),

@@ -176,6 +176,49 @@ def spec_verify_attention(q, k_cache, v_cache, ctx_len, ws, scale=None, out=None
     return out
 
 
+def dense_matmul(x, w, out=None, stream=None):
+    """out [M, N] = bf16(x [M, K] w [N, K]^T) on the tensor cores."""
+    _need(x, torch.bfloat16, "x"); _need(w, torch.bfloat16, "w")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or not x.is_contiguous() or not w.is_contiguous():
+        raise ValueError("x [M, K] and w [N, K] must be contiguous with the same K")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if out is None else out
+    check("dense_matmul", _ffi.load().dense_matmul(_ptr(x), _ptr(w), _ptr(out), M, N, K, _stream(stream)))
+    return out
+
+
+DRAFT_WEIGHTS = ("emb", "w_proj", "w_q", "w_k", "w_v", "w_o", "w_gate_up", "w_down", "w_vocab")
+
+
+def spec_draft_workspace(B, H, nh, I, V, L, device=None) -> torch.Tensor:
+    """Workspace of spec_draft_loop, zeroed (its sub-workspaces need zero on first use)."""
+    n = _ffi.load().spec_draft_workspace_size(B, H, nh, I, V, L)
+    if n == 0:
+        raise ValueError("unsupported draft-block shape")
+    return torch.zeros(int(n), dtype=torch.uint8, device=device or "cuda")
+
+
+def spec_draft_loop(weights, h0, t0, k_cache, v_cache, ctx_len, K, ws, h_out=None, stream=None):
+    """K recursive draft-block steps; returns drafts [B, K] int32 (the caches get the K new entries)."""
+    for n in DRAFT_WEIGHTS:
+        _need(weights[n], torch.bfloat16, n)
+    _need(h0, torch.bfloat16, "h0"); _need(t0, torch.int32, "t0"); _need(ctx_len, torch.int32, "ctx_len")
+    _need(k_cache, torch.bfloat16, "k_cache"); _need(v_cache, torch.bfloat16, "v_cache")
+    B, H = h0.shape
+    _, L, nh, d = k_cache.shape
+    V = weights["w_vocab"].shape[0]
+    I = weights["w_down"].shape[1]
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or nh * d != H or k_cache.shape[0] != B:
+        raise ValueError("caches must be [B, L, nh, H/nh]")
+    w = _ffi.DraftWeights(*[_ptr(weights[n]) for n in DRAFT_WEIGHTS])
+    drafts = torch.empty((B, K), dtype=torch.int32, device=h0.device)
+    check("spec_draft_loop", _ffi.load().spec_draft_loop(
+        ctypes.byref(w), _ptr(h0), _ptr(t0), _ptr(k_cache), _ptr(v_cache), _ptr(ctx_len), B, K, H, nh, I, V, L,
+        _ptr(drafts), _ptr(h_out), _ptr(ws), ws.numel(), _stream(stream)))
+    return drafts
+
+
 def spec_k_policy(cond_accept, step_cost):
     """(k_best, tau [kmax+1], speedup [kmax+1]) from conditional acceptances and step costs."""
     import numpy as np

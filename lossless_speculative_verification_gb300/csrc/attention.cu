@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kAtThreads) attn_split_kernel(const __grid_con
         const int split = cur / per_split;
         const int bh = cur - split * per_split;
         const int b = bh / p.nh, h = bh - b * p.nh;
-        const int n = __ldg(p.ctx_len + b);
+        const int n = __ldcg(p.ctx_len + b);  // L2: the lengths may be rewritten between launches
         const int t_begin = split * kAtChunk;
         if (n < p.Q || n > p.L || t_begin >= n) continue;  // nothing to stream (the combine reports bad lengths)
         const int ntiles = (min(n, t_begin + kAtChunk) - t_begin + kAtTile - 1) / kAtTile;
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kAcThreads) attn_combine_kernel(const float* _
   pdl_trigger();
   const int h = blockIdx.x, b = blockIdx.y;
   if (h == 0 && b == 0 && threadIdx.x == 0) *dealer = 0;  // the split kernel is done with it
-  const int n = ctx_len[b];
+  const int n = __ldcg(ctx_len + b);
   const bool bad = n < Q || n > L;
   if (bad && h == 0 && threadIdx.x == 0) set_error(err, kErrDeviceIndex);
   const int nparts = bad ? 0 : (n + kAtChunk - 1) / kAtChunk;

@@ -170,6 +170,9 @@ size_t attention_ws_bytes(int B, int Q, int L, int nh, int d);
 cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, const int32_t* ctx_len, int B, int Q,
                              int L, int nh, int d, float scale, bf16* out, void* ws, const DeviceCtx& dc,
                              cudaStream_t s);
+// y[M, N] = bf16(x[M, K] w[N, K]^T) on tcgen05 (K % 64 == 0, N % 8 == 0).
+cudaError_t launch_dense_gemm(const bf16* x, const bf16* w, bf16* y, int M, int N, int K, const DeviceCtx& dc,
+                              cudaStream_t s);
 // Counts of the accepted lengths of a batch into hist [K+1].
 cudaError_t launch_accept_histogram(const int32_t* accept_len, int B, int K, int64_t* hist, int* err,
                                     cudaStream_t s);

@@ -369,9 +369,10 @@ def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=T
         u  = u + W_o attn
         f  = RMSNorm(u);  u = u + W_down (silu(W_gate f) * (W_up f))
         h_next = u;  draft = argmax_v (W_vocab RMSNorm(u))_v   (the first index of the maximum)
-    RMSNorm has unit weight.  With round_bf16 the values the kernels store (the normalised
-    input, u, a, q, k, v, the attention output, f, the activation, the final normalised state)
-    are rounded to bf16; every sum is exact in float64.
+    RMSNorm has unit weight.  With round_bf16 the values the kernels store are rounded to bf16:
+    the normalised input, u, a, q, k, v, the attention output, each projection added to the
+    residual (W_o attn and the FFN output, then their sum with u), f, the activation and the
+    final normalised state; every sum is exact in float64.
 
     h_prev [B, H] float64 or bf16 bits; tok_prev [B] int; w: dict of bf16-bit arrays emb [V, H],
     w_proj [H, 2H], w_q, w_k, w_v, w_o [H, H], w_gate_up [2I, H] (gate rows, then up rows),
@@ -405,10 +406,10 @@ def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=T
         p /= p.sum(axis=1, keepdims=True)
         attn[b] = np.einsum("ht,thd->hd", p, v_cache[b, :n + 1]).reshape(H)
     attn = R(attn)
-    u = R(u + attn @ Wo.T)
+    u = R(u + R(attn @ Wo.T))
     f = R(_rms64(u, eps))
     act = R(_silu64(f @ Wgu[:I].T) * (f @ Wgu[I:].T))
-    u = R(u + act @ Wd.T)
+    u = R(u + R(act @ Wd.T))
     hn = R(_rms64(u, eps))
     logits = hn @ Wv_out.T
     draft = np.argmax(logits, axis=1).astype(np.int32)
@@ -416,10 +417,11 @@ def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=T
     return u, draft, top2[:, 1] - top2[:, 0]
 
 
-def draft_loop(h0, t0, w, k_cache, v_cache, ctx_len, nh, K, round_bf16=True):
+def draft_loop(h0, t0, w, k_cache, v_cache, ctx_len, nh, K, round_bf16=True, return_state=False):
     """K recursive applications of the draft block: step i takes step i-1's output state and
     draft token (step 1: the verifier's last hidden state and the last committed token), and
-    appends to the block's cache at ctx_len + i - 1.  Returns (drafts [B, K], gaps [B, K])."""
+    appends to the block's cache at ctx_len + i - 1.  Returns (drafts [B, K], gaps [B, K]),
+    plus the last state [B, H] with return_state."""
     h = h0
     t = np.asarray(t0, np.int64)
     n = np.asarray(ctx_len, np.int64).copy()
@@ -431,4 +433,4 @@ def draft_loop(h0, t0, w, k_cache, v_cache, ctx_len, nh, K, round_bf16=True):
         drafts[:, i] = t
         gaps[:, i] = g
         n += 1
-    return drafts, gaps
+    return (drafts, gaps, h) if return_state else (drafts, gaps)

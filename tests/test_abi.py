@@ -104,6 +104,22 @@ def test_argument_errors_return_before_any_launch(lib):
     assert att(p_odd, 4, 4, 128, 0.1, need) == 3
     assert att(p16, 4, 4, 128, 0.1, need - 1) == 4
     assert lib.spec_verify_attention(None, None, None, None, 0, 4, 1024, 10, 128, 0.1, None, None, 0, None) == 0
+    # dense product: K % 64, N % 8; null, misaligned
+    assert lib.dense_matmul(p16, p16, p16, 4, 8, 100, None) == 2
+    assert lib.dense_matmul(p16, p16, p16, 4, 12, 128, None) == 2
+    assert lib.dense_matmul(None, p16, p16, 4, 8, 128, None) == 1
+    assert lib.dense_matmul(p_odd, p16, p16, 4, 8, 128, None) == 3
+    assert lib.dense_matmul(None, None, None, 0, 8, 128, None) == 0
+    # draft loop: unsupported head width, workspace sizes, small workspace
+    assert lib.spec_draft_workspace_size(4, 1280, 5, 7168, 1000, 2048) == 0       # d = 256
+    assert lib.spec_draft_workspace_size(4, 1280, 10, 7100, 1000, 2048) == 0      # I % 64
+    assert lib.spec_draft_workspace_size(4, 1280, 10, 7168, 1000, 2048) > 0
+    from lossless_speculative_verification_gb300 import _ffi
+    dw = _ffi.DraftWeights(*([p16] * 9))
+    assert lib.spec_draft_loop(ctypes.byref(dw), p16, p16, p16, p16, p16, 4, 3, 1280, 10, 7168, 1000, 2048, p16,
+                               None, p16, 16, None) == 4
+    assert lib.spec_draft_loop(ctypes.byref(dw), p16, p16, p16, p16, p16, 4, 0, 1280, 10, 7168, 1000, 2048, p16,
+                               None, p16, 1 << 30, None) == 1
     assert lib.lsv_set_wait_limit_ns(0) == 1
     assert lib.lsv_selftest_wait_timeout(0, None) == 1
     # empty work is a no-op that succeeds without a device

@@ -1,0 +1,99 @@
+"""The FastMTP draft block on the GPU (spec_draft_loop) and its dense product
+(dense_matmul) against the oracle.
+
+Drafts are integers decided by an argmax: they must match bit for bit.  The
+inputs are redrawn (hidden state and last token of a sequence) until every
+step's top two logits are at least 1e-2 apart in the oracle, far above the
+difference between the GPU's fp32 sums and the oracle's float64 ones; both
+sides round to bf16 at the same points.  The last state and the appended cache
+entries are compared with the layer tolerances; the rest of the caches must be
+untouched."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_speculative_verification_gb300 import api, synth
+
+from gpu_util import assert_layer_close, bf16_f64, from_dev_bf16, need_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+    yield
+    torch.cuda.synchronize()
+    assert api.get_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(32, 1280, 2560), (1, 8, 64), (130, 1288, 1280), (4, 7168, 1280), (300, 96, 192)])
+def test_dense_matmul(M, N, K):
+    rs = np.random.default_rng(M + N + K)
+    x = synth.bf16_bits(rs.standard_normal((M, K)).astype(np.float32))
+    w = synth.bf16_bits((rs.standard_normal((N, K)) * 0.02).astype(np.float32))
+    got = bf16_f64(from_dev_bf16(api.dense_matmul(to_dev(x), to_dev(w))))
+    torch.cuda.synchronize()
+    ref = bf16_f64(x) @ bf16_f64(w).T
+    # fp32 sums, one bf16 rounding
+    np.testing.assert_allclose(got, ref, rtol=2 ** -8, atol=1e-4 * np.sqrt((ref ** 2).mean()))
+
+
+def judged(B, K, H, nh, I, V, seed, min_gap=1e-2, rounds=60):
+    """The problem with every sequence's drafts decided by at least min_gap in the oracle, and
+    the oracle's drafts, last states and caches (sequences are independent: only the redrawn
+    ones are run again)."""
+    p = synth.draft_problem(B, K=K, H=H, nh=nh, I=I, V=V, seed=seed)
+    rng = np.random.default_rng(seed + 99)
+    kc0, vc0 = bf16_f64(p.k_cache), bf16_f64(p.v_cache)
+    kc, vc = kc0.copy(), vc0.copy()
+    drafts, gaps, h = oracle.draft_loop(p.h0, p.t0, p.weights, kc, vc, p.ctx_len, nh, K, return_state=True)
+    for _ in range(rounds):
+        bad = np.nonzero(gaps.min(axis=1) < min_gap)[0]
+        if bad.size == 0:
+            return p, drafts, h, kc, vc
+        p.h0[bad] = synth.hidden_rows(rng, bad.size, H, "sphere")
+        p.t0[bad] = rng.integers(0, V, size=bad.size).astype(np.int32)
+        kb, vb = kc0[bad].copy(), vc0[bad].copy()
+        d2, g2, h2 = oracle.draft_loop(p.h0[bad], p.t0[bad], p.weights, kb, vb, p.ctx_len[bad], nh, K,
+                                       return_state=True)
+        drafts[bad], gaps[bad], h[bad], kc[bad], vc[bad] = d2, g2, h2, kb, vb
+    raise RuntimeError("gap condition not met")
+
+
+def run(p, K):
+    w = {n: to_dev(p.weights[n]) for n in api.DRAFT_WEIGHTS}
+    kc, vc = to_dev(p.k_cache), to_dev(p.v_cache)
+    B, H = p.h0.shape
+    ws = api.spec_draft_workspace(B, H, p.nh, p.I, p.V, p.L)
+    h_out = torch.empty((B, H), dtype=torch.bfloat16, device="cuda")
+    drafts = api.spec_draft_loop(w, to_dev(p.h0), torch.from_numpy(p.t0).cuda(), kc, vc,
+                                 torch.from_numpy(p.ctx_len).cuda(), K, ws, h_out=h_out)
+    torch.cuda.synchronize()
+    return drafts.cpu().numpy(), from_dev_bf16(h_out), from_dev_bf16(kc), from_dev_bf16(vc)
+
+
+def check(B, K, H, nh, I, V, seed):
+    p, ref_drafts, ref_h, ref_kc, ref_vc = judged(B, K, H, nh, I, V, seed)
+    drafts, h, kc, vc = run(p, K)
+    np.testing.assert_array_equal(drafts, ref_drafts)
+    assert_layer_close(bf16_f64(h), ref_h, "last state")
+    for b in range(B):
+        n = int(p.ctx_len[b])
+        np.testing.assert_array_equal(kc[b, :n], p.k_cache[b, :n])       # earlier entries untouched
+        np.testing.assert_array_equal(kc[b, n + K:], p.k_cache[b, n + K:])
+        np.testing.assert_array_equal(vc[b, n + K:], p.v_cache[b, n + K:])
+        assert_layer_close(bf16_f64(kc[b, n:n + K]), ref_kc[b, n:n + K], "appended keys")
+        assert_layer_close(bf16_f64(vc[b, n:n + K]), ref_vc[b, n:n + K], "appended values")
+
+
+def test_draft_loop_small():
+    check(B=4, K=3, H=256, nh=2, I=512, V=3000, seed=1)
+
+
+def test_draft_loop_decoder_shape():
+    # 32 sequences, K = 3, hidden 1280 (10 heads x 128), FFN 7,168, vocabulary 129,280
+    check(B=32, K=3, H=1280, nh=10, I=synth.DRAFT_FFN, V=synth.VOCAB, seed=2)
