@@ -76,11 +76,22 @@ def run(p, K):
     return drafts.cpu().numpy(), from_dev_bf16(h_out), from_dev_bf16(kc), from_dev_bf16(vc)
 
 
+def assert_state_close(got, ref, what):
+    """The state is the block's residual stream (|u| reaches a few units) after K recursive
+    steps that each store bf16 at about ten points; a bf16 ulp at |u| in [2, 4) is 2^-6.  Bound:
+    rel-L2 1e-2 and at most two bf16 ulps at each element's magnitude (2^-6 max(|ref|, 1))."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+    excess = np.abs(got - ref) - 2.0 ** -6 * np.maximum(np.abs(ref), 1.0)
+    assert rel <= 1e-2 and excess.max() <= 0, "%s rel-L2 %.3e worst excess %.3e" % (what, rel, excess.max())
+
+
 def check(B, K, H, nh, I, V, seed):
     p, ref_drafts, ref_h, ref_kc, ref_vc = judged(B, K, H, nh, I, V, seed)
     drafts, h, kc, vc = run(p, K)
     np.testing.assert_array_equal(drafts, ref_drafts)
-    assert_layer_close(bf16_f64(h), ref_h, "last state")
+    assert_state_close(bf16_f64(h), ref_h, "last state")
     for b in range(B):
         n = int(p.ctx_len[b])
         np.testing.assert_array_equal(kc[b, :n], p.k_cache[b, :n])       # earlier entries untouched
