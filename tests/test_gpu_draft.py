@@ -77,13 +77,17 @@ def run(p, K):
 
 
 def assert_state_close(got, ref, what):
-    """The state is the block's residual stream (|u| reaches a few units) after K recursive
-    steps that each store bf16 at about ten points; a bf16 ulp at |u| in [2, 4) is 2^-6.  Bound:
-    rel-L2 1e-2 and at most two bf16 ulps at each element's magnitude (2^-6 max(|ref|, 1))."""
+    """The state is the block's residual stream after K recursive steps.  Two sources of
+    difference: the final bf16 rounding of each element (at most 2 ulps, <= 2^-6 |ref|), and the
+    differences of the projections added to the stream at every step (attention output, FFN),
+    which scale with the stream's size, not with the element's own value; they are about one
+    bf16 ulp RMS (rel-L2 ~4e-3 measured at the decoder shape), so 2^-5 rms(ref) bounds them at
+    about 8 standard deviations.  Plus the layers' rel-L2 bound of 1e-2."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
-    excess = np.abs(got - ref) - 2.0 ** -6 * np.maximum(np.abs(ref), 1.0)
+    rms = np.sqrt((ref ** 2).mean())
+    excess = np.abs(got - ref) - (2.0 ** -6 * np.abs(ref) + 2.0 ** -5 * rms)
     assert rel <= 1e-2 and excess.max() <= 0, "%s rel-L2 %.3e worst excess %.3e" % (what, rel, excess.max())
 
 
