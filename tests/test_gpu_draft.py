@@ -17,7 +17,7 @@ import torch
 import oracle
 from lossless_speculative_verification_gb300 import api, synth
 
-from gpu_util import assert_layer_close, bf16_f64, from_dev_bf16, need_gpu, to_dev
+from gpu_util import bf16_f64, from_dev_bf16, need_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -99,10 +99,15 @@ def check(B, K, H, nh, I, V, seed):
     for b in range(B):
         n = int(p.ctx_len[b])
         np.testing.assert_array_equal(kc[b, :n], p.k_cache[b, :n])       # earlier entries untouched
+        np.testing.assert_array_equal(vc[b, :n], p.v_cache[b, :n])
         np.testing.assert_array_equal(kc[b, n + K:], p.k_cache[b, n + K:])
         np.testing.assert_array_equal(vc[b, n + K:], p.v_cache[b, n + K:])
-        assert_layer_close(bf16_f64(kc[b, n:n + K]), ref_kc[b, n:n + K], "appended keys")
-        assert_layer_close(bf16_f64(vc[b, n:n + K]), ref_vc[b, n:n + K], "appended values")
+    # the appended keys and values are projections of the normalised state: the same two sources
+    # of difference, at their own scale
+    for name, got_c, ref_c in (("keys", kc, ref_kc), ("values", vc, ref_vc)):
+        app = np.concatenate([bf16_f64(got_c[b, int(p.ctx_len[b]):int(p.ctx_len[b]) + K]) for b in range(B)])
+        ref_app = np.concatenate([ref_c[b, int(p.ctx_len[b]):int(p.ctx_len[b]) + K] for b in range(B)])
+        assert_state_close(app, ref_app, "appended " + name)
 
 
 def test_draft_loop_small():
