@@ -6,7 +6,7 @@ grouped SwiGLU experts, shared experts, combine) followed by greedy
 acceptance over the verifier's [32, 4, 129280] bf16 logits.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|prefill|sweep|stack|lmhead|attention]
+                    [--workload decode|prefill|sweep|stack|lmhead|attention|draft]
 
 Prints one JSON line per measured configuration (rank 0; the default run
 prints exactly one).  `value` is tokens/s with all inputs resident in HBM;
@@ -25,6 +25,7 @@ Other workloads (not the default line):
   stack    11 layers (Zipf-skewed routing, residual + RMSNorm) at 64 x 4 tokens + acceptance
   lmhead   the verifier's output layer fused with greedy verification at 32 x 4 positions
   attention  causal attention of 32 x 4 verified positions over page-shaped caches
+  draft    3 recursive FastMTP draft-block steps for 32 sequences
 """
 from __future__ import annotations
 
@@ -54,7 +55,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack", "lmhead", "attention"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack", "lmhead", "attention", "draft"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed oracle sample (for profiler runs; the line then has no cpu_baseline)")
@@ -147,12 +148,15 @@ class ClockSampler:
 
 # per workload: the sources its kernels come from, and the first and last kernel of one step
 STEP_SOURCES = {
+    "draft": ("draft.cu", "attention.cu", "lmhead.cu", "accept.cu", "ffn.cu", "route.cu", "combine.cu", "ptx.cuh",
+              "api.cu"),
     "layer": ("ffn.cu", "ptx.cuh", "route.cu", "permute.cu", "combine.cu", "ffn_plan.cuh", "api.cu", "tmap.h"),
     "lmhead": ("lmhead.cu", "accept.cu", "ptx.cuh", "api.cu", "tmap.h"),
     "attention": ("attention.cu", "ptx.cuh", "api.cu"),
 }
 STEP_BOUNDS = {"layer": ("route", "combine_kernel"), "lmhead": ("lmhead_argmax_kernel", "accept_finalize_kernel"),
-               "attention": ("attn_split_kernel", "attn_combine_kernel")}
+               "attention": ("attn_split_kernel", "attn_combine_kernel"),
+               "draft": ("draft_norm_kernel", "accept_finalize_kernel")}   # one recursion step
 
 
 def step_kind(workload):
@@ -206,7 +210,7 @@ def record_traffic(args):
     for i in sorted(launches):
         e = launches[i]
         base = e["name"].split("<")[0]
-        if base.startswith(first):
+        if base.startswith(first) and cur is None:
             cur = []
         if cur is None:
             continue
@@ -557,8 +561,120 @@ def attention_oracle_sampler(step):
     return sample
 
 
+class DraftStep:
+    """K = 3 recursive applications of the FastMTP draft block to 32 sequences (spec_draft_loop):
+    hidden 1280 (10 heads x 128), FFN 7,168, vocabulary 129,280, block caches with the page
+    lengths.  The unit is a drafted token (B x K per step)."""
+
+    B, K, H, NH, I, V = 32, 3, 1280, 10, 7168, 129_280
+
+    def __init__(self, seed, dev):
+        import torch
+        from lossless_speculative_verification_gb300 import api, synth
+        self.name, self.dev, self.api = "draft", dev, api
+        self.w = None
+        self.layers = []
+        self.T = self.B * self.K
+        p = self.problem = synth.draft_problem(self.B, K=self.K, H=self.H, nh=self.NH, I=self.I, V=self.V, seed=seed)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        self.weights = {n: t(p.weights[n]) for n in api.DRAFT_WEIGHTS}
+        self.h0, self.k_cache, self.v_cache = t(p.h0), t(p.k_cache), t(p.v_cache)
+        self.t0 = torch.from_numpy(p.t0).to(dev)
+        self.ctx_len = torch.from_numpy(p.ctx_len).to(dev)
+        self.ws = api.spec_draft_workspace(self.B, self.H, self.NH, self.I, self.V, p.L, dev)
+        self.drafts = None
+        # per step: 2 norms + W_p + norm + 3 projections + append + attention (2) + W_o + norm + layer (3)
+        # + norm + output layer (2) = 17 kernels, plus the copy of the tokens
+        self.launches = 17 * self.K
+
+    @classmethod
+    def host_only(cls, seed):
+        from lossless_speculative_verification_gb300 import synth
+        step = cls.__new__(cls)
+        step.T = cls.B * cls.K
+        step.problem = synth.draft_problem(cls.B, K=cls.K, H=cls.H, nh=cls.NH, I=cls.I, V=cls.V, seed=seed)
+        return step
+
+    def describe(self):
+        p = self.problem
+        return ("%d recursive draft-block steps for %d sequences: hidden %d (%d heads), FFN %d, vocabulary %d, "
+                "block caches of %d..%d entries" % (self.K, self.B, self.H, self.NH, self.I, self.V,
+                                                    p.ctx_len.min(), p.ctx_len.max()))
+
+    def layer(self):
+        pass
+
+    def accept(self):
+        self.drafts = self.api.spec_draft_loop(self.weights, self.h0, self.t0, self.k_cache, self.v_cache,
+                                               self.ctx_len, self.K, self.ws)
+
+    def check(self):
+        """The drafts of sequences whose every step is decided by at least 1e-2 in the oracle."""
+        import oracle
+        from lossless_speculative_verification_gb300 import synth
+        p = self.problem
+        rows = np.arange(4)
+        kc = synth.bf16_value(p.k_cache[rows]).astype(np.float64)
+        vc = synth.bf16_value(p.v_cache[rows]).astype(np.float64)
+        d, g = oracle.draft_loop(p.h0[rows], p.t0[rows], p.weights, kc, vc, p.ctx_len[rows], self.NH, self.K)
+        got = self.drafts.cpu().numpy()[rows]
+        ok = g.min(axis=1) >= 1e-2
+        assert np.array_equal(got[ok], d[ok]), ("draft sample", got[ok], d[ok])
+
+    def bytes_and_flops(self):
+        p = self.problem
+        H, I, V = self.H, self.I, self.V
+        weights = (2 * H * H + 4 * H * H + 3 * H * I + V * H) * 2        # per step
+        cache = int((p.ctx_len.astype(np.int64) + 1).sum()) * H * 2 * 2   # keys and values read per step
+        byts = self.K * (weights + cache)
+        flops = 2.0 * self.B * self.K * (weights / 2)
+        return byts, flops, 0
+
+    def setup_e2e(self):
+        import torch
+        self.h_h0 = self.h0.cpu().pin_memory()
+        self.h_t0 = self.t0.cpu().pin_memory()
+        self.d_h0, self.d_t0 = torch.empty_like(self.h0), torch.empty_like(self.t0)
+        self.h_drafts = torch.empty((self.B, self.K), dtype=torch.int32).pin_memory()
+        return self.h_h0.numel() * 2 + self.h_t0.numel() * 4, self.h_drafts.numel() * 4
+
+    def e2e(self):
+        self.d_h0.copy_(self.h_h0, non_blocking=True)
+        self.d_t0.copy_(self.h_t0, non_blocking=True)
+        d = self.api.spec_draft_loop(self.weights, self.d_h0, self.d_t0, self.k_cache, self.v_cache, self.ctx_len,
+                                     self.K, self.ws)
+        self.h_drafts.copy_(d, non_blocking=True)
+
+
+def draft_oracle_sampler(step):
+    """The oracle's draft loop (numpy fp64) on one sequence at a time, cycling over the batch."""
+    import oracle
+    from lossless_speculative_verification_gb300 import synth
+    p = step.problem
+    state = {"n": 0}
+
+    def sample(seconds):
+        n0 = state["n"]
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            b = state["n"] % p.B
+            kc = synth.bf16_value(p.k_cache[b:b + 1]).astype(np.float64)
+            vc = synth.bf16_value(p.v_cache[b:b + 1]).astype(np.float64)
+            oracle.draft_loop(p.h0[b:b + 1], p.t0[b:b + 1], p.weights, kc, vc, p.ctx_len[b:b + 1], p.nh, p.K)
+            state["n"] += 1
+        dt = time.perf_counter() - t0
+        n = state["n"] - n0
+        return {"value": n * p.K / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                "kind": "oracle (numpy fp64; its BLAS may use every core)",
+                "sample": "%d sequences x %d drafted tokens (cycling over the %d) through the oracle's draft loop, "
+                          "%.1f s" % (n, p.K, p.B, dt)}
+
+    return sample
+
+
 # workloads outside the MoE layer: name -> (step class, oracle sampler)
-SIDE_STEPS = {"lmhead": (LmHeadStep, lmhead_oracle_sampler), "attention": (AttentionStep, attention_oracle_sampler)}
+SIDE_STEPS = {"lmhead": (LmHeadStep, lmhead_oracle_sampler), "attention": (AttentionStep, attention_oracle_sampler),
+              "draft": (DraftStep, draft_oracle_sampler)}
 
 
 def flush_l2(flush, i):
@@ -720,7 +836,10 @@ def result_line(args, step, m, world, cpu):
                   "to each row's (max, first index) per 128-token vocabulary tile) + accept_finalize_kernel"
                   if step.name == "lmhead" else
                   "attn_split_kernel (persistent: TMA key/value tiles, warp MMAs for scores and weighted values, "
-                  "online softmax in fp32, one state per 256-position split) + attn_combine_kernel")
+                  "online softmax in fp32, one state per 256-position split) + attn_combine_kernel"
+                  if step.name == "attention" else
+                  "spec_draft_loop: 17 launches per step (dense_gemm_kernel projections, attention, shared-expert "
+                  "FFN, norms, fused output-layer argmax)")
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts, "algorithmic_flops": flops, "kernel": kernel,
                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}
