@@ -820,6 +820,16 @@ def max_over_ranks(values, dist, device):
     return [float(v) for v in t.tolist()]
 
 
+def committed_tokens_per_s(accept_len, world, steps, total_ms):
+    """The secondary figure: tokens the step commits (each sequence's accepted drafts plus its
+    correction or bonus token, sum(accept_len + 1)) per second over the whole job; None when
+    the step has no acceptance."""
+    if accept_len is None:
+        return None
+    a = np.asarray(accept_len, dtype=np.int64)
+    return float((a + 1).sum()) * world * steps / (total_ms / 1e3)
+
+
 def job_tokens_per_s(tokens_per_step, world, steps, total_ms):
     """Whole-job throughput: every replica's verified positions over the slowest replica's time."""
     return tokens_per_step * world * steps / (total_ms / 1e3)
@@ -878,6 +888,9 @@ def result_line(args, step, m, world, cpu):
         "roofline": roof,
         "e2e": {"value": tokens / (m["e2e_total"] / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": m["h2d"],
                 "d2h_bytes_per_step": m["d2h"]},
+        "committed_tokens_per_s": committed_tokens_per_s(
+            step.alen.cpu().numpy() if getattr(step, "alen", None) is not None else None, world, args.steps,
+            m["total_ms"]),
         "gpu_launches": step.launches * args.steps,
         "clocks": m["clocks"],
     }
