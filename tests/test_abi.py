@@ -104,6 +104,19 @@ def test_argument_errors_return_before_any_launch(lib):
     assert att(p_odd, 4, 4, 128, 0.1, need) == 3
     assert att(p16, 4, 4, 128, 0.1, need - 1) == 4
     assert lib.spec_verify_attention(None, None, None, None, 0, 4, 1024, 10, 128, 0.1, None, None, 0, None) == 0
+    # attention limits: cache capacity, (sequence, head) pairs
+    assert lib.spec_verify_attention_workspace_size(4, 4, 65537, 10, 128) == 0
+    assert lib.spec_verify_attention_workspace_size(30000, 4, 1024, 10, 128) == 0
+    assert lib.spec_verify_attention_workspace_size(0, 4, 1024, 10, 128) > 0
+    # policy and histogram limits
+    cost = (ctypes.c_double * 65)(*([1.0] * 65))
+    kb = ctypes.c_int32(0)
+    assert lib.spec_k_policy(cost, 64, cost, ctypes.byref(kb), None, None) == 2
+    assert lib.spec_k_policy(None, 1, cost, ctypes.byref(kb), None, None) == 1
+    assert lib.spec_accept_histogram(p16, 4, 64, p16, None) == 2
+    assert lib.spec_accept_histogram(p16, -1, 3, p16, None) == 1
+    assert lib.spec_accept_histogram(None, 0, 3, None, None) == 0
+    assert lib.spec_cond_accept_from_histogram(None, 3, None) == 1
     # dense product: K % 64, N % 8; null, misaligned
     assert lib.dense_matmul(p16, p16, p16, 4, 8, 100, None) == 2
     assert lib.dense_matmul(p16, p16, p16, 4, 12, 128, None) == 2
