@@ -35,7 +35,9 @@ Pins (checked by tests marked "not gpu"):
                 scaled_dot_product_attention, silu, argmax); with attention
                 and FFN switched off it is the (pinned) output-layer oracle;
                 zero queries give the mean of the visible values; the K-step
-                loop is the chained block
+                loop is the chained block; its drafts, verified by the
+                acceptance rule against a toy verifier, commit exactly the
+                verifier's greedy sequence
 """
 from __future__ import annotations
 

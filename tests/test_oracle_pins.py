@@ -654,3 +654,31 @@ def test_draft_problem_shapes_and_oracle_run():
         np.testing.assert_array_equal(kc[b, :n], val64(p.k_cache[b, :n]))
         assert not np.array_equal(kc[b, n:n + 3], val64(p.k_cache[b, n:n + 3]))
         np.testing.assert_array_equal(kc[b, n + 3:], val64(p.k_cache[b, n + 3:]))
+
+
+def test_speculative_loop_with_the_draft_block_is_greedy():
+    # the drafts of the recursive block, checked by the acceptance rule against a verifier's greedy
+    # tokens, commit exactly the verifier's greedy sequence (lossless, whatever the drafter proposes)
+    V, H, nh, I = 50, 64, 4, 96
+    w = _draft_weights(H=H, I=I, V=V, seed=5)
+    verifier = lambda ctx: (7 * sum(ctx) + 3 * ctx[-1] + len(ctx)) % V     # a deterministic toy verifier
+    ref = [1, 2, 3]
+    while len(ref) < 40:
+        ref.append(verifier(ref))
+    out = [1, 2, 3]
+    L = 64
+    kc = np.zeros((1, L, nh, H // nh))
+    vc = np.zeros((1, L, nh, H // nh))
+    n, steps, accepted = 0, 0, 0
+    emb = val64(w["emb"])
+    while len(out) < len(ref):
+        K = 3
+        h0 = emb[[out[-1]]]
+        drafts, _ = oracle.draft_loop(h0, [out[-1]], w, kc, vc, [n], nh, K)
+        greedy = np.array([[verifier(out + list(drafts[0, :j])) for j in range(K + 1)]])
+        alen, comm = oracle.accept_from_greedy(greedy, drafts)
+        out += [int(c) for c in comm[0, :alen[0] + 1]]
+        accepted += int(alen[0])
+        n, steps = n + 1, steps + 1
+    assert len(out) >= len(ref) and out[:len(ref)] == ref
+    assert steps <= len(ref) - 3      # never fewer than one committed token per verify step
