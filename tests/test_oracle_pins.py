@@ -682,3 +682,24 @@ def test_speculative_loop_with_the_draft_block_is_greedy():
         n, steps = n + 1, steps + 1
     assert len(out) >= len(ref) and out[:len(ref)] == ref
     assert steps <= len(ref) - 3      # never fewer than one committed token per verify step
+
+
+def test_k_policy_reads_the_pages_speedups():
+    # S = tau / c with the pages' printed figures: eager K = 3 (83.1 vs 42.7 tok/s, tau 2.73) and
+    # graphs K = 1 (185.6 vs 158.3 tok/s) give the printed 1.95x and 1.17x; with the relative step
+    # cost c(1) they imply, the policy picks K = 1 under graphs whenever the dearer steps keep
+    # their speedups below 1.17x
+    page = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_numbers.json")))
+    a = page["conditional_accept_k3"]["value"]
+    greedy_e, spec_e = page["eager_tok_s"]["value"]
+    greedy_g, spec_g = page["graph_tok_s"]["value"]
+    assert round(spec_e / greedy_e, 2) == page["eager_speedup"]["value"]
+    assert round(spec_g / greedy_g, 2) == page["graph_speedup_best"]["value"]
+    _, tau, _ = oracle.k_policy(a, [1.0] * 4)
+    c3_eager = tau[3] / (spec_e / greedy_e)
+    c1_graph = tau[1] / (spec_g / greedy_g)
+    _, _, S = oracle.k_policy(a, [1.0, 1.0, 1.0, c3_eager])
+    assert abs(S[3] - spec_e / greedy_e) < 1e-9 and 1.35 < c3_eager < 1.45
+    # graphs: with c(1) from the pages and c(2), c(3) dear enough for S <= 1.17, K = 1 is chosen
+    k, _, S = oracle.k_policy(a, [1.0, c1_graph, tau[2] / 1.16, tau[3] / 1.16])
+    assert k == 1 and abs(S[1] - spec_g / greedy_g) < 1e-9
