@@ -703,3 +703,25 @@ def test_k_policy_reads_the_pages_speedups():
     # graphs: with c(1) from the pages and c(2), c(3) dear enough for S <= 1.17, K = 1 is chosen
     k, _, S = oracle.k_policy(a, [1.0, c1_graph, tau[2] / 1.16, tau[3] / 1.16])
     assert k == 1 and abs(S[1] - spec_g / greedy_g) < 1e-9
+
+
+def test_attention_single_query_is_plain_decode_attention():
+    # Q = 1: the one query sits at the last cache entry and sees all n of them (no mask at all)
+    q, k, v, n = _attn_problem(B=2, Q=1, L=20, nh=3, d=8, seed=6, lens=(20, 9))
+    out = oracle.verify_attention(q, k, v, n, 0.35)
+    for b in range(2):
+        m = int(n[b])
+        ref = F.scaled_dot_product_attention(torch.from_numpy(val64(q[b])).permute(1, 0, 2),
+                                             torch.from_numpy(val64(k[b, :m])).permute(1, 0, 2),
+                                             torch.from_numpy(val64(v[b, :m])).permute(1, 0, 2), scale=0.35)
+        np.testing.assert_allclose(out[b], ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_page_context_lengths_follow_the_recipe():
+    rs = synth.streams(3, 1)[0]
+    n = synth.page_context_lengths(rs, 20000, 4)
+    vis_txt = n - 4
+    assert vis_txt.min() >= 256 and vis_txt.max() <= 1156 + 1085
+    assert synth.page_cache_capacity(4) >= n.max() and synth.page_cache_capacity(4) % 64 == 0
+    # mean: 256 + 100 * 4.5 visual + 542.5 text
+    assert abs(vis_txt.mean() - (256 + 450 + 542.5)) < 15
