@@ -609,7 +609,9 @@ class DraftStep:
                                                self.ctx_len, self.K, self.ws)
 
     def check(self):
-        """The drafts of sequences whose every step is decided by at least 1e-2 in the oracle."""
+        """The drafts of sampled sequences whose every step the exact oracle decides by a clear
+        margin: 0.09 sigma_logit, above the bf16-storage error budget's 6-sigma gap (0.086 sigma_logit
+        at a state error of 1e-2; sigma_logit = rms(w_vocab) sqrt(H))."""
         import oracle
         from lossless_speculative_verification_gb300 import synth
         p = self.problem
@@ -618,7 +620,8 @@ class DraftStep:
         vc = synth.bf16_value(p.v_cache[rows]).astype(np.float64)
         d, g = oracle.draft_loop(p.h0[rows], p.t0[rows], p.weights, kc, vc, p.ctx_len[rows], self.NH, self.K)
         got = self.drafts.cpu().numpy()[rows]
-        ok = g.min(axis=1) >= 1e-2
+        wv = synth.bf16_value(p.weights["w_vocab"][:4096]).astype(np.float64)
+        ok = g.min(axis=1) >= 0.09 * np.sqrt((wv ** 2).mean() * self.H)
         assert np.array_equal(got[ok], d[ok]), ("draft sample", got[ok], d[ok])
 
     def bytes_and_flops(self):

@@ -37,7 +37,8 @@ Pins (checked by tests marked "not gpu"):
                 zero queries give the mean of the visible values; the K-step
                 loop is the chained block; its drafts, verified by the
                 acceptance rule against a toy verifier, commit exactly the
-                verifier's greedy sequence
+                verifier's greedy sequence.  It is the plain definition in
+                float64: no value is rounded to bf16 anywhere in it.
 """
 from __future__ import annotations
 
@@ -218,13 +219,14 @@ def lmhead_argmax(hidden, w_vocab, chunk=8192):
     logit[r, v] = sum_h hidden[r, h] * w_vocab[v, h], evaluated in fp64 from the exact bf16
     inputs (numpy's matmul is the only step taken from a library); g[r] = the first index
     attaining the row maximum; gap[r] = that maximum minus the largest logit of any other
-    index (0 when the maximum is attained twice).  hidden [R, H], w_vocab [V, H] as bf16 bits.
+    index (0 when the maximum is attained twice).  hidden [R, H] as bf16 bits (or float64
+    values), w_vocab [V, H] as bf16 bits.
     """
-    hs = _c(hidden, np.uint16)
+    hidden = np.asarray(hidden)
+    hf = hidden if hidden.dtype == np.float64 else _bf16_to_f64(_c(hidden, np.uint16))
     wv = _c(w_vocab, np.uint16)
-    R, H = hs.shape
+    R, H = hf.shape
     V = wv.shape[0]
-    hf = _bf16_to_f64(hs)
     best = np.full(R, -np.inf)
     second = np.full(R, -np.inf)
     g = np.zeros(R, np.int64)
@@ -347,18 +349,7 @@ def _silu64(z):
     return z / (1.0 + np.exp(-z))
 
 
-def _round_bf16(x, on):
-    """bf16 round-to-nearest-even of a float64 array through float32 (the storage points of the
-    draft block's kernels), or x unchanged."""
-    if not on:
-        return x
-    f = np.asarray(x, np.float64).astype(np.float32)
-    u = f.view(np.uint32)
-    u = ((u + (((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF))) >> np.uint32(16)) << np.uint32(16)
-    return u.view(np.float32).astype(np.float64)
-
-
-def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=True, eps=1e-6):
+def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, eps=1e-6):
     """One application of the shared FastMTP draft block to every sequence (kg.zhiyong.dev, "The
     speed comes from three layers working together": one dense draft block proposes the drafts;
     evolve.pub review, "Scope & Claims": one shared block applied recursively).
@@ -371,10 +362,8 @@ def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=T
         u  = u + W_o attn
         f  = RMSNorm(u);  u = u + W_down (silu(W_gate f) * (W_up f))
         h_next = u;  draft = argmax_v (W_vocab RMSNorm(u))_v   (the first index of the maximum)
-    RMSNorm has unit weight.  With round_bf16 the values the kernels store are rounded to bf16:
-    the normalised input, u, a, q, k, v, the attention output, each projection added to the
-    residual (W_o attn and the FFN output, then their sum with u), f, the activation and the
-    final normalised state; every sum is exact in float64.
+    RMSNorm has unit weight.  Everything is evaluated in float64 from the exact bf16 weights and
+    inputs; nothing is rounded on the way (the definition, not any storage format).
 
     h_prev [B, H] float64 or bf16 bits; tok_prev [B] int; w: dict of bf16-bit arrays emb [V, H],
     w_proj [H, 2H], w_q, w_k, w_v, w_o [H, H], w_gate_up [2I, H] (gate rows, then up rows),
@@ -382,7 +371,6 @@ def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=T
     position ctx_len[b]); ctx_len [B].
     Returns (h_next [B, H] float64, draft [B] int32, gap [B]: top-two logit difference).
     """
-    R = lambda x: _round_bf16(x, round_bf16)
     f64 = lambda u: _bf16_to_f64(w[u]) if w[u].dtype == np.uint16 else np.asarray(w[u], np.float64)
     h = np.asarray(h_prev, np.float64) if np.asarray(h_prev).dtype != np.uint16 else _bf16_to_f64(h_prev)
     B, H = h.shape
@@ -392,10 +380,10 @@ def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=T
     Wgu, Wd, Wv_out = f64("w_gate_up"), f64("w_down"), f64("w_vocab")
     I = Wd.shape[1]
     tok = np.asarray(tok_prev, np.int64)
-    inp = R(np.concatenate([_rms64(h, eps), _rms64(E[tok], eps)], axis=1))      # [B, 2H]
-    u = R(inp @ Wp.T)
-    a = R(_rms64(u, eps))
-    q, k, v = R(a @ Wq.T), R(a @ Wk.T), R(a @ Wv.T)
+    inp = np.concatenate([_rms64(h, eps), _rms64(E[tok], eps)], axis=1)         # [B, 2H]
+    u = inp @ Wp.T
+    a = _rms64(u, eps)
+    q, k, v = a @ Wq.T, a @ Wk.T, a @ Wv.T
     attn = np.zeros((B, H))
     for b in range(B):
         n = int(ctx_len[b])
@@ -407,19 +395,18 @@ def draft_block(h_prev, tok_prev, w, k_cache, v_cache, ctx_len, nh, round_bf16=T
         p = np.exp(s)
         p /= p.sum(axis=1, keepdims=True)
         attn[b] = np.einsum("ht,thd->hd", p, v_cache[b, :n + 1]).reshape(H)
-    attn = R(attn)
-    u = R(u + R(attn @ Wo.T))
-    f = R(_rms64(u, eps))
-    act = R(_silu64(f @ Wgu[:I].T) * (f @ Wgu[I:].T))
-    u = R(u + R(act @ Wd.T))
-    hn = R(_rms64(u, eps))
+    u = u + attn @ Wo.T
+    f = _rms64(u, eps)
+    act = _silu64(f @ Wgu[:I].T) * (f @ Wgu[I:].T)
+    u = u + act @ Wd.T
+    hn = _rms64(u, eps)
     logits = hn @ Wv_out.T
     draft = np.argmax(logits, axis=1).astype(np.int32)
     top2 = np.sort(logits, axis=1)[:, -2:] if logits.shape[1] > 1 else np.concatenate([logits, logits], 1)
     return u, draft, top2[:, 1] - top2[:, 0]
 
 
-def draft_loop(h0, t0, w, k_cache, v_cache, ctx_len, nh, K, round_bf16=True, return_state=False):
+def draft_loop(h0, t0, w, k_cache, v_cache, ctx_len, nh, K, return_state=False):
     """K recursive applications of the draft block: step i takes step i-1's output state and
     draft token (step 1: the verifier's last hidden state and the last committed token), and
     appends to the block's cache at ctx_len + i - 1.  Returns (drafts [B, K], gaps [B, K]),
@@ -431,7 +418,7 @@ def draft_loop(h0, t0, w, k_cache, v_cache, ctx_len, nh, K, round_bf16=True, ret
     drafts = np.zeros((B, K), np.int32)
     gaps = np.zeros((B, K))
     for i in range(K):
-        h, t, g = draft_block(h, t, w, k_cache, v_cache, n, nh, round_bf16=round_bf16)
+        h, t, g = draft_block(h, t, w, k_cache, v_cache, n, nh)
         drafts[:, i] = t
         gaps[:, i] = g
         n += 1
