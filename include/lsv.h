@@ -146,7 +146,8 @@ lsv_status moe_verify_layer(const void *x, const lsv_moe_weights *weights, const
                             int32_t *topk_idx_opt, int32_t *counts_opt, void *ws, size_t ws_bytes,
                             lsv_stream stream);
 
-/* Bytes of workspace spec_verify_accept needs (a multiple of 256). */
+/* Bytes of workspace spec_verify_accept needs (a multiple of 256).  Its
+ * contents need no initialisation: every call writes what it reads. */
 size_t spec_verify_workspace_size(int32_t B, int32_t K, int32_t V);
 
 /* Greedy verification (kg.zhiyong.dev, "Why FastMTP fits OCR particularly
@@ -155,7 +156,8 @@ size_t spec_verify_workspace_size(int32_t B, int32_t K, int32_t V);
  *   logits [B, K+1, V] bf16: row j is the verifier's prediction for the
  *          position after input j (input 0 = last committed token, input j = draft j)
  *   drafts [B, K] int32
- *   g[b,j]        = the smallest index attaining the row maximum (finite logits assumed)
+ *   g[b,j]        = the smallest index attaining the row maximum; logits are finite or
+ *                   -inf (a row of -inf gives 0); with a NaN in a row its g is unspecified
  *   accept_len[b] = largest L <= K with drafts[b,i] == g[b,i] for all i < L
  *   committed[b]  = drafts[b,0..L-1], g[b,L], then -1 (K+1 entries)
  *   argmax_opt [B, K+1] int32 or NULL: g
@@ -277,25 +279,25 @@ lsv_status spec_draft_loop(const lsv_draft_weights *weights, const void *h0, con
                            lsv_stream stream);
 
 /* spec_verify_accept without a workspace, for callers that cannot allocate
- * device memory when they verify: code that must not call cudaMalloc inside a
- * stream capture or a latency-critical decode loop, and plugin-style hosts
- * that give a kernel neither an allocator nor a workspace.  The paper has no
- * counterpart; this is a convenience of the library.
+ * device memory at the point where they verify: for example a host that runs
+ * this library as a plugin and hands it only the tensors of the call (no
+ * allocator and no workspace), or a decode loop whose memory is fixed before
+ * it starts and may not grow.  The paper has no counterpart; this is a
+ * convenience of the library.
  *   Same arguments, rule and outputs as spec_verify_accept, minus ws/ws_bytes.
  *   The argmax partials live in one fixed device array of 128 KiB (16,384
  *   (max, index) pairs), held by every device that loads the library until
- *   the process exits.  A problem needing more partials returns
- *   LSV_ERR_UNSUPPORTED before any launch; the count is B*(K+1) rows times
- *   the chunks per row (on a 152-SM GB300 3 chunks per row at 128 rows of
- *   129,280 logits, 1 chunk per row beyond 456 rows, so up to 16,384 rows).
+ *   the process exits.  A call needs B*(K+1) rows times the chunks per row
+ *   (on a 152-SM GB300: 3 chunks per row at 128 rows of 129,280 logits, 1
+ *   chunk per row from 456 rows on), so up to 16,384 rows; a larger problem
+ *   returns LSV_ERR_UNSUPPORTED before any launch.
  *   The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  *   routine.  The first call on each device looks up the array's device
- *   address (cudaGetSymbolAddress) and caches it; make that first call before
- *   any stream capture.  All calls on a device share the array and it keeps
- *   the previous call's contents; nothing in it needs to start at zero, since
- *   each call writes every partial it reads.  Calls that overlap on the GPU
- *   (different streams, no ordering between them) race on the array: order
- *   them on one stream or with events. */
+ *   address (cudaGetSymbolAddress) and caches it.  All calls on a device share
+ *   the array and it keeps the previous call's contents; nothing in it needs
+ *   to start at zero, since each call writes every partial it reads.  Calls
+ *   that overlap on the GPU (different streams, no ordering between them)
+ *   race on the array: order them on one stream or with events. */
 lsv_status spec_verify_accept_noalloc(const void *logits, const int32_t *drafts, int32_t B, int32_t K, int32_t V,
                                       int32_t *argmax_opt, int32_t *accept_len, int32_t *committed,
                                       lsv_stream stream);

@@ -36,6 +36,28 @@ def _need(t, dtype, name):
         raise ValueError("%s must be contiguous" % name)
 
 
+def _need_shape(t, shape, name):
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _verify_outputs(logits, drafts, argmax, accept_len, committed):
+    """Check the acceptance call's tensors against logits [B, K+1, V]; allocate missing outputs."""
+    _need(logits, torch.bfloat16, "logits"); _need(drafts, torch.int32, "drafts")
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B, K+1, V]")
+    B, K1, V = logits.shape
+    _need_shape(drafts, (B, K1 - 1), "drafts")
+    for name, t, shp in (("argmax", argmax, (B, K1)), ("accept_len", accept_len, (B,)),
+                         ("committed", committed, (B, K1))):
+        _need(t, torch.int32, name)
+        _need_shape(t, shp, name)
+    dev = logits.device
+    accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
+    committed = torch.empty((B, K1), dtype=torch.int32, device=dev) if committed is None else committed
+    return B, K1 - 1, V, accept_len, committed
+
+
 def shape(T, H, E, k, S, I) -> MoeShape:
     return MoeShape(T, H, E, k, S, I)
 
@@ -132,12 +154,7 @@ def spec_verify_workspace(B, K, V, device=None) -> torch.Tensor:
 
 
 def spec_verify_accept(logits, drafts, ws, argmax=None, accept_len=None, committed=None, stream=None):
-    _need(logits, torch.bfloat16, "logits"); _need(drafts, torch.int32, "drafts")
-    B, K1, V = logits.shape
-    K = K1 - 1
-    dev = logits.device
-    accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
-    committed = torch.empty((B, K1), dtype=torch.int32, device=dev) if committed is None else committed
+    B, K, V, accept_len, committed = _verify_outputs(logits, drafts, argmax, accept_len, committed)
     check("spec_verify_accept", _ffi.load().spec_verify_accept(
         _ptr(logits), _ptr(drafts), B, K, V, _ptr(argmax), _ptr(accept_len), _ptr(committed), _ptr(ws),
         ws.numel(), _stream(stream)))
@@ -282,14 +299,13 @@ def spec_verify_lmhead(hidden, w_vocab, drafts, ws, K, argmax=None, accept_len=N
 
 
 def spec_verify_accept_noalloc(logits, drafts, argmax=None, accept_len=None, committed=None, stream=None):
-    """spec_verify_accept without a workspace: its scratch is a fixed array inside the library."""
-    _need(logits, torch.bfloat16, "logits"); _need(drafts, torch.int32, "drafts")
-    B, K1, V = logits.shape
-    dev = logits.device
-    accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
-    committed = torch.empty((B, K1), dtype=torch.int32, device=dev) if committed is None else committed
+    """spec_verify_accept without a workspace, for callers that cannot allocate device memory
+    where they verify (a plugin host that passes only the call's tensors, a decode loop whose
+    memory is fixed in advance): its scratch is a fixed array inside the library.  The outputs
+    it is not given are allocated here, by torch, so a caller that may not allocate passes them."""
+    B, K, V, accept_len, committed = _verify_outputs(logits, drafts, argmax, accept_len, committed)
     check("spec_verify_accept_noalloc", _ffi.load().spec_verify_accept_noalloc(
-        _ptr(logits), _ptr(drafts), B, K1 - 1, V, _ptr(argmax), _ptr(accept_len), _ptr(committed),
+        _ptr(logits), _ptr(drafts), B, K, V, _ptr(argmax), _ptr(accept_len), _ptr(committed),
         _stream(stream)))
     return accept_len, committed
 

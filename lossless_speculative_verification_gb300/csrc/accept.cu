@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kAccThreads) argmax_partial_scalar_kernel(cons
   const int begin = c * chunk;
   const int end = min(V, begin + chunk);
   float bv = -INFINITY;
-  int bi = INT_MAX;
+  int bi = begin;  // a chunk of -inf gives its first index, so a row of -inf gives 0
   for (int e = begin + threadIdx.x; e < end; e += kAccThreads) {
     const float f = __bfloat162float(row[e]);
     if (f > bv) { bv = f; bi = e; }
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kAccThreads) argmax_partial_bulk_kernel(const 
     }
   }
   float bv = -INFINITY;
-  int bi = INT_MAX;
+  int bi = begin;  // a chunk of -inf gives its first index, so a row of -inf gives 0
   bool ok = true;
   for (int q = 0; q < npieces; ++q) {
     const int slot = q % kRingSlots;
@@ -261,12 +261,8 @@ cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int 
   cudaError_t e;
   if (aligned) {
     constexpr int kSmem = kRingSlots * kPiece + 128;
-    static int attr_done[64] = {0};
-    if (dc.device >= 0 && dc.device < 64 && !attr_done[dc.device]) {
-      e = cudaFuncSetAttribute(argmax_partial_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-      if (e != cudaSuccess) return e;
-      attr_done[dc.device] = 1;
-    }
+    e = ensure_smem_attr(reinterpret_cast<const void*>(argmax_partial_bulk_kernel), kSmem, dc.device);
+    if (e != cudaSuccess) return e;
     e = launch_pdl(argmax_partial_bulk_kernel, dim3(R, nchunk), dim3(kAccThreads), kSmem, s, logits, V, chunk, nchunk,
                    pv, pi, dc.err, wait_limit_ns());
   } else {
@@ -288,12 +284,11 @@ cudaError_t launch_accept_finalize(const float* pv, const int* pi, int nchunk, c
 
 // ----------------------------------------------------------------------------- no-allocation variant
 // Some callers cannot allocate device memory at the point where they verify
-// drafts: code that must not call cudaMalloc while a stream is being captured
-// or while a latency-critical decode loop runs, and plugin-style hosts that
-// hand a kernel neither an allocator nor a workspace.  For them the chunk
-// partials of the argmax live in this fixed array instead of a caller
-// workspace.  It exists once per device that loads the library and stays
-// allocated until the process exits.
+// drafts: a host that runs the library as a plugin and passes only the
+// tensors of the call, or a decode loop whose memory is fixed before it
+// starts.  For them the chunk partials of the argmax live in this fixed array
+// instead of a caller workspace.  It exists once per device that loads the
+// library and stays allocated until the process exits.
 namespace lsv {
 namespace {
 constexpr int kNoAllocPartials = 16384;  // (max, index) pairs: 128 KiB in total

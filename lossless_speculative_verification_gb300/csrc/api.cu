@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
 
 #include "internal.h"
@@ -57,6 +58,17 @@ cudaError_t device_ctx(DeviceCtx** out) {
   }
   *out = &c;
   return cudaSuccess;
+}
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes, int device) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  std::lock_guard<std::mutex> lk(mu);
+  int& have = done[std::make_pair(kernel, device)];
+  if (have >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
 }
 
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s) {

@@ -30,6 +30,8 @@
 // attn_combine_kernel (programmatic dependent launch): per (sequence, head),
 // the splits' states rescaled to their common maximum and summed;
 // out = sum / normaliser in bf16.  It also rewinds the dealer.
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -433,7 +435,9 @@ cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, co
                                int L, int nh, float scale, bf16* out, void* ws, const DeviceCtx& dc,
                                cudaStream_t s) {
   static int grid_per_sm[64] = {0};
+  static std::mutex mu;
   if (dc.device < 0 || dc.device >= 64) return cudaErrorInvalidDevice;
+  std::unique_lock<std::mutex> lk(mu);
   if (!grid_per_sm[dc.device]) {
     cudaError_t e =
         cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, AtSmem<D>::kTotal);
@@ -443,6 +447,8 @@ cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, co
     if (e != cudaSuccess) return e;
     grid_per_sm[dc.device] = per_sm > 0 ? per_sm : 1;
   }
+  const int per_sm_cached = grid_per_sm[dc.device];
+  lk.unlock();
   AtParams p;
   p.ctx_len = ctx_len;
   p.B = B;
@@ -466,7 +472,7 @@ cudaError_t launch_attention_d(const bf16* q, const bf16* kc, const bf16* vc, co
       !make_map(&vmap, vc, (uint64_t)B * L, (uint64_t)nh * D, kAtTile) ||
       !make_map(&qmap, q, (uint64_t)B * Q, (uint64_t)nh * D, kMaxAttnQ))
     return cudaErrorInvalidValue;
-  const long long cap = (long long)grid_per_sm[dc.device] * dc.num_sms;
+  const long long cap = (long long)per_sm_cached * dc.num_sms;
   const int grid = (int)(p.total < cap ? p.total : cap);
   cudaError_t e = launch_pdl(attn_split_kernel<D>, dim3(grid), dim3(kAtThreads), AtSmem<D>::kTotal, s, kmap, vmap,
                              qmap, p);

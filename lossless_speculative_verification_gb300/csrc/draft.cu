@@ -321,14 +321,8 @@ constexpr int kDraftRouterRows = 8;
 cudaError_t launch_dense_gemm(const bf16* x, const bf16* w, bf16* y, int M, int N, int K, const DeviceCtx& dc,
                               cudaStream_t s) {
   if (M == 0 || N == 0) return cudaSuccess;
-  static int attr_done[64] = {0};
-  if (dc.device < 0 || dc.device >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dc.device]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(dense_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DgSmem::kTotal);
-    if (e != cudaSuccess) return e;
-    attr_done[dc.device] = 1;
-  }
+  const cudaError_t ea = ensure_smem_attr(reinterpret_cast<const void*>(dense_gemm_kernel), DgSmem::kTotal, dc.device);
+  if (ea != cudaSuccess) return ea;
   DgParams p;
   p.M = M;
   p.N = N;

@@ -36,6 +36,8 @@
 // finished gate/up items; the wait always ends, because every gate/up item of
 // that group was dealt earlier to a running CTA whose progress on it depends
 // on nothing else.
+#include <mutex>
+
 #include "ffn_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -785,7 +787,9 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   auto kernel = ffn_kernel<BN, STAGES, KCH, PAIR>;
   static int attr_done[64] = {0};
   static int grid_for[64] = {0};  // PAIR: CTAs of the largest set of co-resident pairs
+  static std::mutex mu;
   if (dc.device < 0 || dc.device >= 64) return cudaErrorInvalidDevice;
+  std::unique_lock<std::mutex> lk(mu);
   if (!attr_done[dc.device]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
     if (e != cudaSuccess) return e;
@@ -810,6 +814,8 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
     }
     attr_done[dc.device] = 1;
   }
+  const int grid_cached = grid_for[dc.device];
+  lk.unlock();
   int32_t* table = reinterpret_cast<int32_t*>(ws + L.table);
   int32_t* counters = reinterpret_cast<int32_t*>(ws + L.counters);
   bf16* xperm = reinterpret_cast<bf16*>(ws + L.xperm);
@@ -868,7 +874,7 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
   p.deal_ahead = BN >= LSV_FFN_DEAL_AHEAD_BN ? 1 : 0;
   if (!PAIR) return launch_pdl(kernel, dim3(dc.num_sms), dim3(kFfnThreads), SM::kTotal, s, maps, p);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid_for[dc.device]);
+  cfg.gridDim = dim3(grid_cached);
   cfg.blockDim = dim3(kFfnThreads);
   cfg.dynamicSmemBytes = SM::kTotal;
   cfg.stream = s;

@@ -33,6 +33,9 @@ struct DeviceCtx {
 };
 cudaError_t device_ctx(DeviceCtx** out);
 uint64_t wait_limit_ns();
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on `device`, once per
+// (kernel, device) pair; safe to call from several host threads at once.
+cudaError_t ensure_smem_attr(const void* kernel, int bytes, int device);
 
 // ---------------------------------------------------------------- FFN tile table
 // int32 table in the workspace, written by the kernel that completes the

@@ -266,14 +266,9 @@ cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const 
                                  const DeviceCtx& dc, cudaStream_t s) {
   const int R = B * (K + 1);
   if (R == 0) return cudaSuccess;
-  static int attr_done[64] = {0};
-  if (dc.device < 0 || dc.device >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dc.device]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(lmhead_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, LhSmem::kTotal);
-    if (e != cudaSuccess) return e;
-    attr_done[dc.device] = 1;
-  }
+  const cudaError_t ea =
+      ensure_smem_attr(reinterpret_cast<const void*>(lmhead_argmax_kernel), LhSmem::kTotal, dc.device);
+  if (ea != cudaSuccess) return ea;
   LhParams p;
   p.R = R;
   p.H = H;

@@ -322,13 +322,8 @@ template <int NPAD>
 cudaError_t run_route_tc(const bf16* x, const bf16* wr, int T, int H, int E, int k, int32_t* idx, float* w,
                          float* logits, int* err, int device, cudaStream_t s) {
   using SM = RtSmem<NPAD>;
-  static int attr_done[64] = {0};
-  if (device >= 0 && device < 64 && !attr_done[device]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(route_tc_kernel<NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
-    if (e != cudaSuccess) return e;
-    attr_done[device] = 1;
-  }
+  const cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(route_tc_kernel<NPAD>), SM::kTotal, device);
+  if (e != cudaSuccess) return e;
   CUtensorMap xmap, wmap;
   if (!make_map(&xmap, x, T, H, 128) || !make_map(&wmap, wr, E, H, NPAD)) return cudaErrorInvalidValue;
   return launch_pdl(route_tc_kernel<NPAD>, dim3((T + 127) / 128), dim3(kRtThreads), SM::kTotal, s, xmap, wmap, T, H,

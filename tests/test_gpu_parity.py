@@ -157,6 +157,59 @@ def test_layer_pairs(T, H, E, k, S, I):
     assert_layer_close(bf16_f64(from_dev_bf16(out))[toks], ref, "pairs")
 
 
+# Token tiles of 64 and 128 rows: the tile follows the mean rows per expert (T k / E), 24 at
+# T = 256 (BN = 64, the router places the rows) and 60 at T = 640 (BN = 128, the fused
+# permutation + gather places them).
+TILE_SHAPES = [(256, 1280, 64, 6, 2, 896, 10**9), (640, 1280, 64, 6, 2, 896, 200)]
+
+
+@pytest.mark.parametrize("T,H,E,k,S,I,nsample", TILE_SHAPES)
+def test_grouped_ffn_token_tiles(T, H, E, k, S, I, nsample):
+    P = pair_problem(T, H, E, k, S, I)
+    d, prob = P.d, P.prob
+    r = P.oracle_route()
+    dev = lambda a: torch.from_numpy(a).cuda()
+    y_perm, y_sh = api.moe_grouped_ffn(P.x, dev(r["perm"]), dev(r["offsets"]), dev(r["counts"]), P.wts, P.sh, P.ws)
+    torch.cuda.synchronize()
+    rows = sample_rows(d.T * d.k, nsample, 21)
+    for e in (int(np.argmin(r["counts"])), int(np.argmax(r["counts"]))):
+        rows = np.union1d(rows, np.arange(r["offsets"][e], r["offsets"][e + 1]))
+    expert = np.searchsorted(r["offsets"], rows, side="right") - 1
+    token = r["perm"][rows] // d.k
+    ref = oracle.expert_rows(prob.x, prob.w_gate_up, prob.w_down, token, expert)
+    assert_layer_close(y_perm.cpu().numpy()[rows], ref, "routed T=%d" % T)
+    toks = sample_rows(d.T, min(nsample, d.T), 22)
+    ref_sh = oracle.shared_rows(prob.x, prob.ws_gate_up, prob.ws_down, d.S, toks)
+    assert_layer_close(y_sh.cpu().numpy()[toks], ref_sh, "shared T=%d" % T)
+
+
+@pytest.mark.parametrize("T,H,E,k,S,I,nsample", TILE_SHAPES)
+def test_layer_token_tiles(T, H, E, k, S, I, nsample):
+    P = pair_problem(T, H, E, k, S, I)
+    d, prob = P.d, P.prob
+    idx = torch.empty((d.T, d.k), dtype=torch.int32, device="cuda")
+    out = api.moe_verify_layer(P.x, P.wts, P.sh, P.ws, topk_idx=idx)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), P.oracle_route()["idx"])
+    toks = sample_rows(d.T, nsample, 23)
+    ref, _, _ = oracle.moe_layer(prob.x, prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up,
+                                 prob.ws_down, d.k, d.S, tokens=toks)
+    assert_layer_close(bf16_f64(from_dev_bf16(out))[toks], ref, "T=%d" % T)
+
+
+def test_weight_prefetch_leaves_the_layer_bit_identical():
+    # the L2 hint changes where the weights are read from, never the result
+    P = dev_problem("decode")
+    a = api.moe_verify_layer(P.x, P.wts, P.sh, P.ws)
+    torch.cuda.synchronize()
+    for budget in (0, 48 << 20, 1 << 40):
+        api.moe_prefetch_weights(P.wts, P.sh, budget)
+        b = api.moe_verify_layer(P.x, P.wts, P.sh, P.ws)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), budget
+    assert api.get_device_error() == 0
+
+
 # ----------------------------------------------------------------------------- combine
 def test_combine_parity():
     T, k, H = 128, 6, 1280
@@ -284,6 +337,29 @@ def test_accept_edge_shapes(B, K, V):
         drafts[-1, -1] = -3
     g, alen, comm = run_accept(logits, drafts)
     rg, ralen, rcomm = oracle.accept(logits, drafts)
+    np.testing.assert_array_equal(g, rg)
+    np.testing.assert_array_equal(alen, ralen)
+    np.testing.assert_array_equal(comm, rcomm)
+
+
+@pytest.mark.parametrize("V", [129_280, 1001])
+def test_accept_rows_of_minus_infinity(V):
+    # a row that is -inf everywhere (a fully masked vocabulary) has greedy token 0, the first index
+    # of its maximum; rows -inf except at one place, and rows with +inf, follow the same rule
+    B, K = 6, 3
+    logits, planted = synth.verify_logits(B, K, V, seed=21)
+    ninf, pinf = np.uint16(0xFF80), np.uint16(0x7F80)
+    logits[0, :, :] = ninf                       # every row of sequence 0
+    logits[1, 2, :] = ninf
+    logits[2, 1, :] = ninf
+    logits[2, 1, V - 1] = synth.bf16_bits(np.float32([-3.0]))[0]   # the only finite value: the last index
+    logits[3, 0, V // 2] = pinf
+    logits[3, 0, V // 3] = pinf                  # two +inf: the lower index wins
+    drafts = synth.draft_tokens(planted, V, [0.9] * K, seed=3)
+    drafts[0] = 0                                # drafts that equal the -inf rows' greedy token 0
+    g, alen, comm = run_accept(logits, drafts)
+    rg, ralen, rcomm = oracle.accept(logits, drafts)
+    assert rg[0].tolist() == [0] * (K + 1) and rg[2, 1] == V - 1 and rg[3, 0] == V // 3
     np.testing.assert_array_equal(g, rg)
     np.testing.assert_array_equal(alen, ralen)
     np.testing.assert_array_equal(comm, rcomm)
