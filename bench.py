@@ -583,9 +583,10 @@ class DraftStep:
         self.ctx_len = torch.from_numpy(p.ctx_len).to(dev)
         self.ws = api.spec_draft_workspace(self.B, self.H, self.NH, self.I, self.V, p.L, dev)
         self.drafts = None
-        # per step: 2 norms + W_p + norm + 3 projections + append + attention (2) + W_o + norm + layer (3)
-        # + norm + output layer (2) = 17 kernels, plus the copy of the tokens
-        self.launches = 17 * self.K
+        # per step: input norms + W_p + norm + q/k/v + append + attention (2) + W_o + residual norm
+        # + gate/up (SwiGLU) + down + residual norm + output layer (2) = 14 kernels, plus the copy of
+        # the tokens
+        self.launches = 14 * self.K
 
     @classmethod
     def host_only(cls, seed):
@@ -851,8 +852,8 @@ def result_line(args, step, m, world, cpu):
                   "attn_split_kernel (persistent: TMA key/value tiles, warp MMAs for scores and weighted values, "
                   "online softmax in fp32, one state per 256-position split) + attn_combine_kernel"
                   if step.name == "attention" else
-                  "spec_draft_loop: 17 launches per step (dense_gemm_kernel projections, attention, shared-expert "
-                  "FFN, norms, fused output-layer argmax)")
+                  "spec_draft_loop: 14 launches per step (skinny_gemm_kernel split-K projections with q/k/v in "
+                  "one launch and the SwiGLU FFN in two, attention, norms, fused output-layer argmax)")
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts, "algorithmic_flops": flops, "kernel": kernel,
                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}

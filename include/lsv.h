@@ -236,8 +236,22 @@ lsv_status spec_cond_accept_from_histogram(const int64_t *hist, int32_t K, doubl
 
 /* Dense product y [M, N] = bf16(x [M, K] w [N, K]^T), bf16 inputs, fp32 accumulation
  * (tcgen05).  Device pointers, 16-byte aligned; K % 64 == 0, K <= 16384,
- * N % 8 == 0.  No workspace.  One launch. */
+ * N % 8 == 0.  No workspace.  One launch.  Up to 256 rows of x (the decode
+ * shapes), the weight rows take the MMA's M side and each 128-row weight tile's
+ * K range is split over a thread-block cluster of up to 8 CTAs whose partial
+ * sums are added in shared memory in a fixed order (deterministic); w (not x)
+ * may then be read before the work that precedes the call on the stream has
+ * finished, so that work must not write w. */
 lsv_status dense_matmul(const void *x, const void *w, void *y, int32_t M, int32_t N, int32_t K, lsv_stream stream);
+
+/* The FFN form of the same product for few rows of x:
+ *   y [M, F] = bf16(silu(x [M, K] w_gate^T) * (x w_up^T)),  silu(z) = z / (1 + e^-z),
+ *   w_gate_up [2F, K]: rows 0..F-1 w_gate, F..2F-1 w_up.
+ * bf16 inputs, fp32 sums, deterministic.  1 <= M <= 256 (M = 0: no-op),
+ * K % 64 == 0, K <= 16384, F % 8 == 0, F <= 32768.  Device pointers, 16-byte
+ * aligned.  No workspace.  One launch. */
+lsv_status dense_swiglu(const void *x, const void *w_gate_up, void *y, int32_t M, int32_t F, int32_t K,
+                        lsv_stream stream);
 
 /* Weights of the FastMTP draft block (bf16, device, 16-byte aligned):
  *   emb [V, H] (token embedding), w_proj [H, 2H], w_q, w_k, w_v, w_o [H, H],
@@ -268,8 +282,11 @@ typedef struct {
  * RMSNorm: unit weight, eps 1e-6.  Every value between kernels is bf16.
  * drafts [B, K] int32 (device) receives t of every step; h_out [B, H] bf16
  * (optional) the last u.  ctx_len [B] int32 (device) is read, not written;
- * ctx_len[b] + K <= L.  Supported: H % 64 == 0, H <= 16384, H/nh in {64, 128},
- * I % 64 == 0, I <= 16384, 1 <= K <= 63.
+ * ctx_len[b] + K <= L.  Supported: 0 <= B <= 256, H % 64 == 0, H <= 16384,
+ * H/nh in {64, 128}, I % 64 == 0, I <= 16384, 1 <= K <= 63.  Per step: the
+ * projections as the few-row products of dense_matmul / dense_swiglu (q, k and
+ * v in one launch), the attention of spec_verify_attention at one query, and
+ * the output layer fused with the greedy search of spec_verify_lmhead.
  * ws: spec_draft_workspace_size(B, H, nh, I, V, L) bytes, zero before the first
  * use; calls that raise no device error leave it fit for the next call. */
 size_t spec_draft_workspace_size(int32_t B, int32_t H, int32_t nh, int32_t I, int32_t V, int32_t L);

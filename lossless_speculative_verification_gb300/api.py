@@ -205,6 +205,21 @@ def dense_matmul(x, w, out=None, stream=None):
     return out
 
 
+def dense_swiglu(x, w_gate_up, out=None, stream=None):
+    """out [M, F] = bf16(silu(x w_gate^T) * (x w_up^T)) with w_gate_up = [w_gate; w_up] [2F, K],
+    for few rows of x (M <= 256)."""
+    _need(x, torch.bfloat16, "x"); _need(w_gate_up, torch.bfloat16, "w_gate_up")
+    M, K = x.shape
+    if w_gate_up.shape[1] != K or w_gate_up.shape[0] % 2:
+        raise ValueError("x [M, K] and w_gate_up [2F, K] must have the same K")
+    F = w_gate_up.shape[0] // 2
+    out = torch.empty((M, F), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need(out, torch.bfloat16, "out")
+    _need_shape(out, (M, F), "out")
+    check("dense_swiglu", _ffi.load().dense_swiglu(_ptr(x), _ptr(w_gate_up), _ptr(out), M, F, K, _stream(stream)))
+    return out
+
+
 DRAFT_WEIGHTS = ("emb", "w_proj", "w_q", "w_k", "w_v", "w_o", "w_gate_up", "w_down", "w_vocab")
 
 

@@ -246,25 +246,28 @@ __global__ void __launch_bounds__(kDgThreads, 1) dense_gemm_kernel(const __grid_
 // ----------------------------------------------------------------------------- small kernels
 constexpr int kDnThreads = 256;
 
-// y[b, :] = bf16(RMSNorm(x[src, :])) with src = b, or src = rows[b] (an embedding row);
-// a row index outside [0, nsrc) writes zeros and raises LSV_ERR_DEVICE_INDEX.
-__global__ void __launch_bounds__(kDnThreads) draft_norm_kernel(const bf16* __restrict__ x, const int32_t* rows,
+// Row b of blockIdx.y == 0: y[b, 0:H] = bf16(RMSNorm(a[b, :])).  Of blockIdx.y == 1 (the block's
+// input): y[b, H:2H] = bf16(RMSNorm(e[rows[b], :])), an embedding row; a row index outside
+// [0, nsrc) writes zeros and raises LSV_ERR_DEVICE_INDEX.
+__global__ void __launch_bounds__(kDnThreads) draft_norm_kernel(const bf16* __restrict__ a,
+                                                                const bf16* __restrict__ e, const int32_t* rows,
                                                                 int nsrc, bf16* __restrict__ y, int ldy, int H,
                                                                 float eps, int* err) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
-  int src = b;
+  const bf16* xr = a + (size_t)b * H;
   bf16* yr = y + (size_t)b * ldy;
-  if (rows) {
-    src = __ldcg(rows + b);
+  if (blockIdx.y == 1) {
+    yr += H;
+    const int src = __ldcg(rows + b);
     if (src < 0 || src >= nsrc) {
       if (threadIdx.x == 0) set_error(err, kErrDeviceIndex);
       for (int c = threadIdx.x; c < H; c += kDnThreads) yr[c] = __float2bfloat16_rn(0.f);
       return;
     }
+    xr = e + (size_t)src * H;
   }
-  const bf16* xr = x + (size_t)src * H;
   float ss = 0.f;
   for (int c = threadIdx.x; c < H; c += kDnThreads) {
     const float f = __bfloat162float(xr[c]);
@@ -312,9 +315,6 @@ __global__ void __launch_bounds__(128) draft_append_kernel(const bf16* __restric
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Router rows of the shared-expert-only layer that runs the block's FFN (the routing shape the
-// layer's tests cover with k = 0).
-constexpr int kDraftRouterRows = 8;
 
 }  // namespace
 
@@ -340,11 +340,10 @@ cudaError_t launch_dense_gemm(const bf16* x, const bf16* w, bf16* y, int M, int 
 }
 
 // Workspace of the draft loop: activations, the lengths, and the sub-workspaces of the
-// kernels it reuses (each of which needs zero on first use and leaves its counters zero).
+// kernels it uses (each of which needs zero on first use and leaves its counters zero).
 struct DraftWs {
-  size_t inp, u, a, q, k, v, attn, y, f, hn, ffn, tok, alen, comm, len0, len1, router, layer_ws, attn_ws, lm_ws,
-      total;
-  size_t layer_bytes, attn_bytes, lm_bytes;
+  size_t inp, u, a, q, k, v, attn, y, f, hn, act, z, tok, alen, comm, len0, len1, attn_ws, lm_ws, total;
+  size_t attn_bytes, lm_bytes;
 };
 
 DraftWs draft_ws_layout(int B, int H, int nh, int I, int V, int L) {
@@ -366,21 +365,18 @@ DraftWs draft_ws_layout(int B, int H, int nh, int I, int V, int L) {
   w.y = take(act);
   w.f = take(act);
   w.hn = take(act);
-  w.ffn = take(act);
+  w.act = take((size_t)B * I * 2);
+  w.z = take(act);
   w.tok = take((size_t)B * 4);
   w.alen = take((size_t)B * 4);
   w.comm = take((size_t)B * 4);
   w.len0 = take((size_t)B * 4);
   w.len1 = take((size_t)B * 4);
-  w.router = take((size_t)kDraftRouterRows * H * 2);  // all-zero router rows: the FFN is the layer's shared expert
-  lsv_moe_shape sh = {B, H, kDraftRouterRows, 0, 1, I};
-  w.layer_bytes = lsv_workspace_size(&sh);
   w.attn_bytes = spec_verify_attention_workspace_size(B, 1, L, nh, H / nh);
   w.lm_bytes = spec_verify_lmhead_workspace_size(B, 0, V, H);
-  w.layer_ws = take(w.layer_bytes);
   w.attn_ws = take(w.attn_bytes);
   w.lm_ws = take(w.lm_bytes);
-  w.total = (w.layer_bytes && w.attn_bytes && w.lm_bytes) ? o : 0;
+  w.total = (w.attn_bytes && w.lm_bytes) ? o : 0;
   return w;
 }
 
@@ -399,18 +395,22 @@ lsv_status dense_matmul(const void* x, const void* w, void* y, int32_t M, int32_
   if (!al(x) || !al(w) || !al(y)) return LSV_ERR_MISALIGNED;
   DeviceCtx* dc = nullptr;
   if (device_ctx(&dc) != cudaSuccess) return LSV_ERR_CUDA;
-  return launch_dense_gemm(static_cast<const bf16*>(x), static_cast<const bf16*>(w), static_cast<bf16*>(y), M, N, K,
-                           *dc, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? LSV_OK
-             : LSV_ERR_CUDA;
+  const bf16* xb = static_cast<const bf16*>(x);
+  const bf16* wb = static_cast<const bf16*>(w);
+  bf16* yb = static_cast<bf16*>(y);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // few rows of x: the weights on the MMA's M side, K split over clusters (skinny.cu)
+  const cudaError_t e = M <= kSkMaxRows ? launch_skinny(xb, M, K, &wb, &N, &yb, &N, 1, false, *dc, s)
+                                        : launch_dense_gemm(xb, wb, yb, M, N, K, *dc, s);
+  return e == cudaSuccess ? LSV_OK : LSV_ERR_CUDA;
 }
 
 size_t spec_draft_workspace_size(int32_t B, int32_t H, int32_t nh, int32_t I, int32_t V, int32_t L) {
   if (B < 0 || H <= 0 || nh <= 0 || H % nh || I <= 0 || V <= 0 || L <= 0) return 0;
   const int d = H / nh;
   if (H % 64 || H > kMaxHidden || (d != 64 && d != 128) || I % 64 || I > kMaxHidden) return 0;
-  const DraftWs w = draft_ws_layout(B, H, nh, I, V, L);
-  return w.total;
+  if (B > kSkMaxRows) return 0;
+  return draft_ws_layout(B < 1 ? 1 : B, H, nh, I, V, L).total;
 }
 
 lsv_status spec_draft_loop(const lsv_draft_weights* wt, const void* h0, const int32_t* t0, void* k_cache,
@@ -437,51 +437,48 @@ lsv_status spec_draft_loop(const lsv_draft_weights* wt, const void* h0, const in
   uint8_t* w = static_cast<uint8_t*>(ws);
   auto act = [&](size_t off) { return reinterpret_cast<bf16*>(w + off); };
   auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(w + off); };
-  const bf16* emb = static_cast<const bf16*>(wt->emb);
+  auto wgt = [](const void* p) { return static_cast<const bf16*>(p); };
+  const bf16* emb = wgt(wt->emb);
   bf16* kc = static_cast<bf16*>(k_cache);
   bf16* vc = static_cast<bf16*>(v_cache);
   const float eps = 1e-6f;
   const int d = H / nh;
-  // the dense FFN runs as the layer's one shared expert: top-0 routing over all-zero router rows, so
-  // no routed expert is ever read (the routed-weight pointers only have to be valid)
-  lsv_moe_weights lw = {w + L8.router, wt->w_gate_up, wt->w_down, wt->w_gate_up, wt->w_down};
-  lsv_moe_shape lsh = {B, H, kDraftRouterRows, 0, 1, I};
+  const int nH = H, n2I = 2 * I, ldH = H, ldI = I;
+  const int nqkv[3] = {H, H, H}, ldqkv[3] = {H, H, H};
+  const bf16* wqkv[3] = {wgt(wt->w_q), wgt(wt->w_k), wgt(wt->w_v)};
+  bf16* yqkv[3] = {act(L8.q), act(L8.k), act(L8.v)};
   cudaError_t e = cudaSuccess;
   const int32_t* len_cur = ctx_len;
   for (int i = 0; i < K && e == cudaSuccess; ++i) {
     int32_t* len_next = i32((i & 1) ? L8.len1 : L8.len0);
     const bf16* h_prev = i == 0 ? static_cast<const bf16*>(h0) : act(L8.u);
     const int32_t* t_prev = i == 0 ? t0 : i32(L8.tok);
-    e = launch_pdl(draft_norm_kernel, dim3(B), dim3(kDnThreads), 0, s, h_prev, (const int32_t*)nullptr, B, act(L8.inp),
-                   2 * H, H, eps, dc->err);
+    // the block's input [RMSNorm(h); RMSNorm(E[t])], one launch for both halves
+    e = launch_pdl(draft_norm_kernel, dim3(B, 2), dim3(kDnThreads), 0, s, h_prev, emb, t_prev, V, act(L8.inp), 2 * H,
+                   H, eps, dc->err);
+    auto sk1 = [&](const bf16* x, int K_, const bf16* wm, int n, bf16* y, int ldy, bool swiglu) {
+      return launch_skinny(x, B, K_, &wm, &n, &y, &ldy, 1, swiglu, *dc, s);
+    };
+    if (e == cudaSuccess) e = sk1(act(L8.inp), 2 * H, wgt(wt->w_proj), nH, act(L8.u), ldH, false);
     if (e == cudaSuccess)
-      e = launch_pdl(draft_norm_kernel, dim3(B), dim3(kDnThreads), 0, s, emb, t_prev, V, act(L8.inp) + H, 2 * H, H,
-                     eps, dc->err);
-    if (e == cudaSuccess)
-      e = launch_dense_gemm(act(L8.inp), static_cast<const bf16*>(wt->w_proj), act(L8.u), B, H, 2 * H, *dc, s);
-    if (e == cudaSuccess)
-      e = launch_pdl(draft_norm_kernel, dim3(B), dim3(kDnThreads), 0, s, (const bf16*)act(L8.u),
-                     (const int32_t*)nullptr, B, act(L8.a), H, H, eps, dc->err);
-    if (e == cudaSuccess) e = launch_dense_gemm(act(L8.a), static_cast<const bf16*>(wt->w_q), act(L8.q), B, H, H, *dc, s);
-    if (e == cudaSuccess) e = launch_dense_gemm(act(L8.a), static_cast<const bf16*>(wt->w_k), act(L8.k), B, H, H, *dc, s);
-    if (e == cudaSuccess) e = launch_dense_gemm(act(L8.a), static_cast<const bf16*>(wt->w_v), act(L8.v), B, H, H, *dc, s);
+      e = launch_pdl(draft_norm_kernel, dim3(B, 1), dim3(kDnThreads), 0, s, (const bf16*)act(L8.u), emb,
+                     (const int32_t*)nullptr, V, act(L8.a), H, H, eps, dc->err);
+    if (e == cudaSuccess) e = launch_skinny(act(L8.a), B, H, wqkv, nqkv, yqkv, ldqkv, 3, false, *dc, s);
     if (e == cudaSuccess)
       e = launch_pdl(draft_append_kernel, dim3(B), dim3(128), 0, s, (const bf16*)act(L8.k), (const bf16*)act(L8.v), kc,
                      vc, len_cur, len_next, L, H, dc->err);
     if (e == cudaSuccess)
       e = launch_attention(act(L8.q), kc, vc, len_next, B, 1, L, nh, d, 1.0f / sqrtf((float)d), act(L8.attn),
                            w + L8.attn_ws, *dc, s);
-    if (e == cudaSuccess) e = launch_dense_gemm(act(L8.attn), static_cast<const bf16*>(wt->w_o), act(L8.y), B, H, H, *dc, s);
+    if (e == cudaSuccess) e = sk1(act(L8.attn), H, wgt(wt->w_o), nH, act(L8.y), ldH, false);
     if (e == cudaSuccess) e = launch_rmsnorm_residual(act(L8.u), act(L8.y), act(L8.f), B, H, eps, s);
-    if (e == cudaSuccess) {
-      const lsv_status st =
-          moe_verify_layer(act(L8.f), &lw, &lsh, act(L8.ffn), nullptr, nullptr, w + L8.layer_ws, L8.layer_bytes, stream);
-      if (st != LSV_OK) return st;
-    }
-    if (e == cudaSuccess) e = launch_rmsnorm_residual(act(L8.u), act(L8.ffn), act(L8.hn), B, H, eps, s);
+    // the dense SwiGLU FFN: gate/up pair with the activation in the epilogue, then the down projection
+    if (e == cudaSuccess) e = sk1(act(L8.f), H, wgt(wt->w_gate_up), n2I, act(L8.act), ldI, true);
+    if (e == cudaSuccess) e = sk1(act(L8.act), I, wgt(wt->w_down), nH, act(L8.z), ldH, false);
+    if (e == cudaSuccess) e = launch_rmsnorm_residual(act(L8.u), act(L8.z), act(L8.hn), B, H, eps, s);
     if (e == cudaSuccess)
-      e = launch_lmhead_accept(act(L8.hn), static_cast<const bf16*>(wt->w_vocab), nullptr, B, 0, V, H, i32(L8.tok),
-                               i32(L8.alen), i32(L8.comm), w + L8.lm_ws, *dc, s);
+      e = launch_lmhead_accept(act(L8.hn), wgt(wt->w_vocab), nullptr, B, 0, V, H, i32(L8.tok), i32(L8.alen),
+                               i32(L8.comm), w + L8.lm_ws, *dc, s);
     if (e == cudaSuccess)
       e = cudaMemcpy2DAsync(drafts + i, (size_t)K * 4, i32(L8.tok), 4, 4, B, cudaMemcpyDeviceToDevice, s);
     len_cur = len_next;

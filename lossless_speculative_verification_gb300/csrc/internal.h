@@ -173,6 +173,13 @@ size_t attention_ws_bytes(int B, int Q, int L, int nh, int d);
 cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, const int32_t* ctx_len, int B, int Q,
                              int L, int nh, int d, float scale, bf16* out, void* ws, const DeviceCtx& dc,
                              cudaStream_t s);
+// Dense products for few rows of x (skinny.cu): y_j = x W_j^T for up to kSkMaxJobs weight matrices
+// W_j [n_rows[j], K] sharing x [M, K] (M <= kSkMaxRows), or in the SwiGLU form y = silu(x W_g^T) * (x W_u^T)
+// with W = [W_g; W_u] of n_rows = 2F rows.  K split over the CTAs of a cluster, reduced in shared memory.
+constexpr int kSkMaxRows = 256;
+constexpr int kSkMaxJobs = 3;
+cudaError_t launch_skinny(const bf16* x, int M, int K, const bf16* const* w, const int* n_rows, bf16* const* y,
+                          const int* ldy, int njobs, bool swiglu, const DeviceCtx& dc, cudaStream_t s);
 // y[M, N] = bf16(x[M, K] w[N, K]^T) on tcgen05 (K % 64 == 0, N % 8 == 0).
 cudaError_t launch_dense_gemm(const bf16* x, const bf16* w, bf16* y, int M, int N, int K, const DeviceCtx& dc,
                               cudaStream_t s);

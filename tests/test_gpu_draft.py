@@ -8,6 +8,8 @@ rel-L2 1e-2 and every element within 6 times that of the RMS; drafts, integers d
 argmax, bit for bit wherever the exact top-two logits are at least 6 standard deviations of the
 budget's logit error apart at every step (the inputs of sequences that fall short are redrawn).
 The rest of the caches must be untouched."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -40,6 +42,53 @@ def test_dense_matmul(M, N, K):
     ref = bf16_f64(x) @ bf16_f64(w).T
     # fp32 sums, one bf16 rounding
     np.testing.assert_allclose(got, ref, rtol=2 ** -8, atol=1e-4 * np.sqrt((ref ** 2).mean()))
+
+
+# Few rows of x (the cluster split-K path): the draft block's projections at decode sizes (W_p, the
+# FFN's down projection, W_o at 64 rows), ragged shapes (rows past a tile, a partial last weight
+# tile, one chunk of K) and the longest K
+SKINNY = [(32, 1280, 2560), (32, 1280, 7168), (1, 8, 64), (7, 96, 192), (256, 136, 16384), (64, 1280, 1280),
+          (17, 392, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", SKINNY)
+def test_dense_matmul_few_rows(M, N, K):
+    rs = np.random.default_rng(M * 7 + N + K)
+    x = synth.bf16_bits(rs.standard_normal((M, K)).astype(np.float32))
+    w = synth.bf16_bits((rs.standard_normal((N, K)) * 0.02).astype(np.float32))
+    a = api.dense_matmul(to_dev(x), to_dev(w))
+    b = api.dense_matmul(to_dev(x), to_dev(w))
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))   # the splits add in a fixed order
+    got = bf16_f64(from_dev_bf16(a))
+    ref = bf16_f64(x) @ bf16_f64(w).T
+    # fp32 sums, one bf16 rounding
+    np.testing.assert_allclose(got, ref, rtol=2 ** -8, atol=1e-4 * np.sqrt((ref ** 2).mean()))
+
+
+@pytest.mark.parametrize("M,F,K", [(32, 7168, 1280), (4, 512, 256), (19, 136, 640), (256, 64, 128), (1, 8, 4096)])
+def test_dense_swiglu(M, F, K):
+    rs = np.random.default_rng(M + F + K)
+    x = synth.bf16_bits(rs.standard_normal((M, K)).astype(np.float32))
+    w = synth.bf16_bits((rs.standard_normal((2 * F, K)) * 0.02).astype(np.float32))
+    a = api.dense_swiglu(to_dev(x), to_dev(w))
+    b = api.dense_swiglu(to_dev(x), to_dev(w))
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    got = bf16_f64(from_dev_bf16(a))
+    g = bf16_f64(x) @ bf16_f64(w[:F]).T
+    u = bf16_f64(x) @ bf16_f64(w[F:]).T
+    ref = g / (1.0 + np.exp(-g)) * u
+    np.testing.assert_allclose(got, ref, rtol=2 ** -8, atol=1e-4 * np.sqrt((ref ** 2).mean()))
+
+
+def test_dense_swiglu_rejects_bad_shapes():
+    lib = api._ffi.load()
+    x = torch.zeros((300, 64), dtype=torch.bfloat16, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    assert lib.dense_swiglu(p(x), p(x), p(x), 300, 8, 64, None) == api._ffi.ERR_UNSUPPORTED    # > 256 rows
+    assert lib.dense_swiglu(p(x), p(x), p(x), 4, 8, 96, None) == api._ffi.ERR_UNSUPPORTED      # K % 64
+    assert lib.dense_swiglu(p(x), p(x), p(x), 4, 12, 64, None) == api._ffi.ERR_UNSUPPORTED     # F % 8
 
 
 def judged(B, K, H, nh, I, V, seed, rounds=80):
