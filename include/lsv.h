@@ -195,6 +195,29 @@ lsv_status spec_verify_attention(const void *q, const void *k_cache, const void 
                                  int32_t B, int32_t Q, int32_t L, int32_t nh, int32_t d, float scale, void *out,
                                  void *ws, size_t ws_bytes, lsv_stream stream);
 
+/* The data movements of a verify pass around its kernels (one launch each).
+ *
+ * lsv_gather_rows: out[i, :] = table[idx[i], :] for i < n, rows of row_elems
+ *   bf16 (for example the embedding rows of the verified tokens).
+ *   table [n_table, row_elems], idx [n] int32 (device), out [n, row_elems].
+ *   row_elems % 8 == 0.  An index outside [0, n_table) writes a zero row and
+ *   raises LSV_ERR_DEVICE_INDEX.
+ *
+ * spec_cache_append: the keys and values of the Q verified positions of every
+ *   sequence go to its cache before the verify attention reads it:
+ *   k_cache[b, ctx_len[b] - Q + j, :] = k_new[b*Q + j, :] (the same for v),
+ *   k_new, v_new [B*Q, row_elems] bf16 (row_elems = heads * head width),
+ *   k_cache, v_cache [B, L, row_elems] bf16, ctx_len [B] int32 (device): the
+ *   lengths after the append, as spec_verify_attention takes them.
+ *   row_elems % 8 == 0, 1 <= Q <= L.  A length outside [Q, L] raises
+ *   LSV_ERR_DEVICE_INDEX and leaves that sequence's cache alone.
+ * Device pointers, 16-byte aligned. */
+lsv_status lsv_gather_rows(const void *table, const int32_t *idx, int32_t n, int32_t n_table, int32_t row_elems,
+                           void *out, lsv_stream stream);
+lsv_status spec_cache_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int32_t *ctx_len, int32_t B, int32_t Q, int32_t L, int32_t row_elems,
+                             lsv_stream stream);
+
 /* Greedy verification with the verify logits produced by the verifier's output
  * layer, inside the call (the logits are never written to memory):
  *   hidden  [B*(K+1), H] bf16: the verifier's last hidden state of every verified

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "liblsv.so")
-SOURCES = ["api.cu", "route.cu", "permute.cu", "ffn.cu", "combine.cu", "accept.cu", "prefetch.cu", "lmhead.cu", "attention.cu", "policy.cu", "draft.cu", "skinny.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "ffn.cu", "combine.cu", "accept.cu", "prefetch.cu", "lmhead.cu", "attention.cu", "policy.cu", "draft.cu", "skinny.cu", "cache.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -59,6 +59,8 @@ SIGNATURES = {
     "dense_matmul": (I32, [P, P, P, I32, I32, I32, P]),
     "spec_draft_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32]),
     "dense_swiglu": (I32, [P, P, P, I32, I32, I32, P]),
+    "lsv_gather_rows": (I32, [P, P, I32, I32, I32, P, P]),
+    "spec_cache_append": (I32, [P, P, P, P, P, I32, I32, I32, I32, P]),
     "spec_draft_loop": (I32, [DRAFT_P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, P, P, P, SZ, P]),
     "spec_accept_histogram": (I32, [P, I32, I32, P, P]),
     "spec_cond_accept_from_histogram": (I32, [P, I32, P]),

@@ -205,6 +205,35 @@ def dense_matmul(x, w, out=None, stream=None):
     return out
 
 
+def gather_rows(table, idx, out=None, stream=None):
+    """out[i] = table[idx[i]] (bf16 rows; e.g. the embedding rows of the verified tokens)."""
+    _need(table, torch.bfloat16, "table"); _need(idx, torch.int32, "idx")
+    n_table, row = table.shape
+    n = idx.numel()
+    out = torch.empty((n, row), dtype=torch.bfloat16, device=table.device) if out is None else out
+    _need(out, torch.bfloat16, "out")
+    _need_shape(out, (n, row), "out")
+    check("lsv_gather_rows", _ffi.load().lsv_gather_rows(_ptr(table), _ptr(idx), n, n_table, row, _ptr(out),
+                                                         _stream(stream)))
+    return out
+
+
+def spec_cache_append(k_new, v_new, k_cache, v_cache, ctx_len, stream=None):
+    """Keys and values of the Q verified positions [B, Q, ...] into the caches [B, L, ...] at
+    ctx_len[b] - Q + j (ctx_len: the lengths after the append)."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, torch.bfloat16, n)
+    _need(ctx_len, torch.int32, "ctx_len")
+    B, Q = k_new.shape[:2]
+    L = k_cache.shape[1]
+    row = k_new[0, 0].numel()
+    if k_cache.shape[0] != B or k_cache[0, 0].numel() != row or v_new.shape != k_new.shape or \
+            v_cache.shape != k_cache.shape:
+        raise ValueError("k_new/v_new [B, Q, ...] and caches [B, L, ...] with the same row width")
+    check("spec_cache_append", _ffi.load().spec_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                                             _ptr(ctx_len), B, Q, L, row, _stream(stream)))
+
+
 def dense_swiglu(x, w_gate_up, out=None, stream=None):
     """out [M, F] = bf16(silu(x w_gate^T) * (x w_up^T)) with w_gate_up = [w_gate; w_up] [2F, K],
     for few rows of x (M <= 256)."""
@@ -231,7 +260,7 @@ def spec_draft_workspace(B, H, nh, I, V, L, device=None) -> torch.Tensor:
     return torch.zeros(int(n), dtype=torch.uint8, device=device or "cuda")
 
 
-def spec_draft_loop(weights, h0, t0, k_cache, v_cache, ctx_len, K, ws, h_out=None, stream=None):
+def spec_draft_loop(weights, h0, t0, k_cache, v_cache, ctx_len, K, ws, h_out=None, out=None, stream=None):
     """K recursive draft-block steps; returns drafts [B, K] int32 (the caches get the K new entries)."""
     for n in DRAFT_WEIGHTS:
         _need(weights[n], torch.bfloat16, n)
@@ -244,7 +273,9 @@ def spec_draft_loop(weights, h0, t0, k_cache, v_cache, ctx_len, K, ws, h_out=Non
     if tuple(v_cache.shape) != tuple(k_cache.shape) or nh * d != H or k_cache.shape[0] != B:
         raise ValueError("caches must be [B, L, nh, H/nh]")
     w = _ffi.DraftWeights(*[_ptr(weights[n]) for n in DRAFT_WEIGHTS])
-    drafts = torch.empty((B, K), dtype=torch.int32, device=h0.device)
+    drafts = torch.empty((B, K), dtype=torch.int32, device=h0.device) if out is None else out
+    _need(drafts, torch.int32, "out")
+    _need_shape(drafts, (B, K), "out")
     check("spec_draft_loop", _ffi.load().spec_draft_loop(
         ctypes.byref(w), _ptr(h0), _ptr(t0), _ptr(k_cache), _ptr(v_cache), _ptr(ctx_len), B, K, H, nh, I, V, L,
         _ptr(drafts), _ptr(h_out), _ptr(ws), ws.numel(), _stream(stream)))

@@ -456,3 +456,57 @@ def draft_problem(B: int, K: int = 3, H: int = 1280, nh: int = ATTN_HEADS, I: in
     kc = _normal_bf16(rs[12], (B, L, nh, d), 1.0)
     vc = _normal_bf16(rs[13], (B, L, nh, d), 1.0)
     return DraftProblem(B, K, H, nh, I, V, L, wts, h0, t0, kc, vc, lens)
+
+
+# --------------------------------------------------------------------------- a decoder around the verify step
+@dataclass
+class DecoderProblem:
+    layers: list         # per layer: dict of bf16 bits w_q, w_k, w_v, w_o [H, H] and the MoE weights
+    emb: np.ndarray      # [V, H] token embedding (shared with the draft block)
+    w_vocab: np.ndarray  # [V, H] output layer (shared with the draft block)
+    draft: dict          # the draft block's weights (emb and w_vocab included)
+    dims: MoeDims        # the MoE layer's H, E, k, S, I (T unused)
+    nh: int
+    V: int
+    I_draft: int
+
+
+def decoder_problem(n_layers: int, dims: MoeDims, V: int, nh: int = ATTN_HEADS, I_draft: int = DRAFT_FFN,
+                    seed: int = 0, out_scale: float = 1.0, mimic_draft: bool = False,
+                    std: float = 0.02) -> DecoderProblem:
+    """Synthetic weights of an n_layers decoder (attention block + MoE FFN per layer) and its draft
+    block, all N(0, std) in bf16 except the embedding N(0, 1).
+
+    out_scale multiplies the two projections that write into the residual stream (W_o and the
+    experts' down projections), so that at out_scale < 1 the stream stays close to the token
+    embedding.  mimic_draft sets the draft block to pass the embedding of its input token
+    through (W_p = [0 | I], W_o = 0, W_down = 0): it then proposes the greedy token of the
+    embedding alone, which the verifier agrees with more often the smaller out_scale is."""
+    H = dims.H
+    rs = streams(seed, 4 + n_layers * 9 + 8)
+    emb = _normal_bf16(rs[0], (V, H), 1.0)
+    w_vocab = _normal_bf16(rs[1], (V, H), std)
+    layers = []
+    for l in range(n_layers):
+        r = rs[4 + 9 * l: 13 + 9 * l]
+        w_router, w_gate_up, w_down, ws_gate_up, ws_down = moe_weights(dims, r[4:9], std)
+        if out_scale != 1.0:
+            w_down = bf16_bits(bf16_value(w_down) * np.float32(out_scale))
+            ws_down = bf16_bits(bf16_value(ws_down) * np.float32(out_scale))
+        layers.append(dict(w_q=_normal_bf16(r[0], (H, H), std), w_k=_normal_bf16(r[1], (H, H), std),
+                           w_v=_normal_bf16(r[2], (H, H), std), w_o=_normal_bf16(r[3], (H, H), std * out_scale),
+                           w_router=w_router, w_gate_up=w_gate_up, w_down=w_down, ws_gate_up=ws_gate_up,
+                           ws_down=ws_down))
+    rd = rs[4 + 9 * n_layers:]
+    if mimic_draft:
+        w_proj = bf16_bits(np.concatenate([np.zeros((H, H), np.float32), np.eye(H, dtype=np.float32)], axis=1))
+        w_o_d = np.zeros((H, H), np.uint16)
+        w_down_d = np.zeros((H, I_draft), np.uint16)
+    else:
+        w_proj = _normal_bf16(rd[0], (H, 2 * H), std)
+        w_o_d = _normal_bf16(rd[1], (H, H), std)
+        w_down_d = _normal_bf16(rd[2], (H, I_draft), std)
+    draft = dict(emb=emb, w_proj=w_proj, w_q=_normal_bf16(rd[3], (H, H), std), w_k=_normal_bf16(rd[4], (H, H), std),
+                 w_v=_normal_bf16(rd[5], (H, H), std), w_o=w_o_d, w_gate_up=_normal_bf16(rd[6], (2 * I_draft, H), std),
+                 w_down=w_down_d, w_vocab=w_vocab)
+    return DecoderProblem(layers, emb, w_vocab, draft, dims, nh, V, I_draft)
