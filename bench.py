@@ -26,6 +26,10 @@ Other workloads (not the default line):
   lmhead   the verifier's output layer fused with greedy verification at 32 x 4 positions
   attention  causal attention of 32 x 4 verified positions over page-shaped caches
   draft    3 recursive FastMTP draft-block steps for 32 sequences
+  spec     one speculative step per batch size B in {1,4,8,16,32,64} and K in {0,1,2,3}: K draft-block
+           steps, then the verify pass of an 11-layer decoder (attention over page-shaped caches + the
+           MoE layer per layer, the output layer fused with the acceptance rule) over K+1 positions;
+           one line each, then the "k_policy" line from these step costs
 """
 from __future__ import annotations
 
@@ -55,7 +59,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "sweep", "stack", "lmhead", "attention", "draft"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "sweep", "stack", "lmhead", "attention", "draft", "spec"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed oracle sample (for profiler runs; the line then has no cpu_baseline)")
@@ -978,8 +983,117 @@ def k_policy_line(step_ms):
             "block, no attention); acceptances 0.830/0.663/0.636 from the pages", "per_batch": out}
 
 
+def run_spec(args, rank, world, local, dev, flush):
+    """Speculative step costs t(B, K) (drafting + verify pass) and the K policy on them."""
+    import torch
+    from lossless_speculative_verification_gb300 import api, synth
+    from lossless_speculative_verification_gb300.decoder import Decoder
+    n_layers = 11
+    dims = synth._verify_dims(1, 0)
+    prob = synth.decoder_problem(n_layers, dims, V=synth.VOCAB, seed=args.seed + 1000 * rank)
+    Bmax, Qmax = max(synth.SWEEP_B), max(synth.SWEEP_K) + 1
+    L = synth.page_cache_capacity(Qmax)
+    dec = Decoder(prob, Bmax, L, dev)
+    dec.fill_caches(args.seed + 5)
+    rs = synth.streams(args.seed + 77, 4)
+    ctx0 = synth.page_context_lengths(rs[0], Bmax, 0)                 # the prefix before the verified positions
+    g = torch.Generator(device=dev).manual_seed(args.seed + 9)
+    dk = torch.randn((Bmax, L, dec.nh, dec.hd), generator=g, device=dev).to(torch.bfloat16)
+    dv = torch.randn_like(dk)
+    h_all = torch.from_numpy(synth.hidden_rows(rs[1], Bmax, dec.H, "sphere").view(np.int16)).view(torch.bfloat16).to(dev)
+    tok_all = torch.from_numpy(rs[2].integers(0, dec.V, size=(Bmax, Qmax)).astype(np.int32)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    step_ms, draft_ms = {}, {}
+    for B in synth.SWEEP_B:
+        dws = api.spec_draft_workspace(B, dec.H, dec.nh, prob.I_draft, dec.V, L, dev)
+        dctx = torch.from_numpy(ctx0[:B].astype(np.int32)).to(dev)
+        for K in synth.SWEEP_K:
+            Q = K + 1
+            tokens = tok_all[:B, :Q].contiguous()                   # the verify pass's inputs (their values
+            ctx_after = dctx + Q                                      # do not change the work)
+            dr = torch.zeros((B, K), dtype=torch.int32, device=dev)
+            h0, t0 = h_all[:B].contiguous(), tokens[:, 0].contiguous()
+
+            def draft():
+                if K:
+                    api.spec_draft_loop(dec.draft_w, h0, t0, dk[:B], dv[:B], dctx, K, dws, out=dr)
+
+            def step():
+                draft()
+                dec.verify(tokens, ctx_after, dr)
+
+            for _ in range(max(args.warmup, 1)):
+                step()
+            torch.cuda.synchronize()
+            graphs = []
+            for fn in (step, draft):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    fn()
+                graphs.append(gr)
+            for gr in graphs:
+                gr.replay()
+            torch.cuda.synchronize()
+            assert api.get_device_error() == 0
+            times = {0: [], 1: []}
+            with ClockSampler(local) as clk:
+                clk.wait_first_sample()
+                for which in (0, 1):
+                    if which == 1 and K == 0:
+                        continue
+                    for i in range(args.steps):
+                        flush_l2(flush, i)
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        graphs[which].replay()
+                        b.record(stream)
+                        b.synchronize()
+                        times[which].append(a.elapsed_time(b))
+            assert api.get_device_error() == 0
+            t_step = statistics.median(times[0])
+            t_draft = statistics.median(times[1]) if K else 0.0
+            step_ms[(B, K)], draft_ms[(B, K)] = t_step, t_draft
+            tau = float(api.spec_k_policy(list(synth.PAGE_ACCEPT[:K]) or [0.0], [1.0] * (K + 1) if K else [1.0, 1.0])[1][K])
+            launches = dec.launches_per_verify(B, Q) + 14 * K
+            if rank == 0:
+                print(json.dumps({
+                    "metric": "speculative step: %d-layer verify pass over B x (K+1) positions after K draft-block "
+                              "steps" % n_layers,
+                    "value": B * Q / (t_step / 1e3), "unit": "verified tokens/s", "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
+                    "dtype": "bf16", "data": "synthetic",
+                    "config": {"workload": "spec: B=%d, K=%d; %d layers (attention 10x128 over page-shaped caches "
+                                           "+ MoE H=1280, E=64 top-6, S=2, I=896), output layer [129280,1280] fused "
+                                           "with acceptance; draft block FFN 7168" % (B, K, n_layers),
+                               "l2": "flushed before every timed step",
+                               "timing": "median of CUDA-graph replays, CUDA events"},
+                    "draft_ms": t_draft, "verify_ms": t_step - t_draft,
+                    "expected_committed_tokens_per_s": B * tau / (t_step / 1e3),
+                    "gpu_launches": launches * args.steps, "clocks": clk.summary()}), flush=True)
+            del graphs
+        del dws
+        torch.cuda.empty_cache()
+    if rank == 0:
+        out = {}
+        for B in synth.SWEEP_B:
+            cost = [step_ms[(B, k)] for k in synth.SWEEP_K]
+            k_best, tau, sp = api.spec_k_policy(list(synth.PAGE_ACCEPT), cost)
+            out[str(B)] = {"step_ms": [round(c, 4) for c in cost], "draft_ms": [round(draft_ms[(B, k)], 4)
+                                                                              for k in synth.SWEEP_K],
+                           "tau": [round(x, 4) for x in tau], "speedup": [round(x, 4) for x in sp], "k_best": k_best}
+        print(json.dumps({"metric": "k_policy", "note": "cost = one speculative step: K draft-block steps + the "
+                          "verify pass of an 11-layer decoder (attention + MoE per layer, output layer fused with "
+                          "acceptance) over K+1 positions; acceptances 0.830/0.663/0.636 from the pages",
+                          "per_batch": out}), flush=True)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
+        return
+    if args.workload == "spec":
+        print(json.dumps({"impl": "reference", "workload": "spec",
+                          "unavailable": "no bounded oracle sample of the 11-layer speculative step (the oracle takes "
+                                         "minutes per step); the component workloads carry the oracle baselines"}))
         return
     for name, w, seed in workloads(args.workload):
         per_step = 2.0 if name != "sweep" else 0.5       # seconds of oracle work per timed step
@@ -1021,6 +1135,12 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.barrier()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if args.workload == "spec":
+        run_spec(args, rank, world, local, dev, flush)
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
     step_ms = {}
     for name, w, seed in workloads(args.workload):
         if name in SIDE_STEPS:
