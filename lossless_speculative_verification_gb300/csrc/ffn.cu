@@ -99,15 +99,20 @@ struct FfnParams {
   int deal_ahead;          // take each next item index one item early
 };
 
+// Token-row boxes of 16, 32, 64 and 128 rows: an item loads the smallest that holds its rows (at
+// most the token tile a CTA stages), so an expert with few rows moves few bytes.
+constexpr int kBoxN = 4;
+__host__ __device__ constexpr int box_rows(int b) { return 16 << b; }
+
 struct FfnMaps {
-  CUtensorMap wgu;     // [E*2I, H]   as {H, 2, E*2I}, box 64 x 2 x 64 (gate/up interleaved)
-  CUtensorMap wsgu;    // [2SI, H]    as {H, 2, SI},   box 64 x 2 x 64
-  CUtensorMap wd;      // [E*H, I]    box 64 x 128
-  CUtensorMap wsd;     // [H, SI]     box 64 x 128
-  CUtensorMap xperm;   // [T*k, H]    box 64 x BN
-  CUtensorMap x;       // [T, H]      box 64 x BN
-  CUtensorMap act;     // [T*k, I]    box 64 x BN
-  CUtensorMap act_sh;  // [T, SI]     box 64 x BN
+  CUtensorMap wgu;             // [E*2I, H]   as {H, 2, E*2I}, box 64 x 2 x 64 (gate/up interleaved)
+  CUtensorMap wsgu;            // [2SI, H]    as {H, 2, SI},   box 64 x 2 x 64
+  CUtensorMap wd;              // [E*H, I]    box 64 x 128
+  CUtensorMap wsd;             // [H, SI]     box 64 x 128
+  CUtensorMap xperm[kBoxN];    // [T*k, H]    box 64 x box_rows(b)
+  CUtensorMap x[kBoxN];        // [T, H]
+  CUtensorMap act[kBoxN];      // [T*k, I]
+  CUtensorMap act_sh[kBoxN];   // [T, SI]
 };
 
 struct Item {
@@ -411,7 +416,6 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           fence_proxy_async_global();
         }
         const CUtensorMap* amap = m.gu ? (routed ? &maps.wgu : &maps.wsgu) : (routed ? &maps.wd : &maps.wsd);
-        const CUtensorMap* bmap = m.gu ? (routed ? &maps.xperm : &maps.x) : (routed ? &maps.act : &maps.act_sh);
         // this CTA's feature tile; past the group's last tile (odd count, PAIR) it stages the last
         // one again and its epilogue discards the result
         const int ft = min(m.ft + (int)rank, m.nft - 1);
@@ -421,6 +425,13 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         // PAIR: the MMA takes n/2 token rows from each CTA
         const int n_mma = max(16, (m.cnt + 15) & ~15);
         const int brow0 = m.row0 + (PAIR ? (int)rank * (n_mma / 2) : 0);
+        // the smallest token-row box that holds this CTA's rows of the item
+        const int rows_cta = PAIR ? n_mma / 2 : n_mma;
+        int bx = 0;
+        while (bx + 1 < kBoxN && box_rows(bx) < rows_cta && box_rows(bx + 1) <= (PAIR ? BN / 2 : BN)) ++bx;
+        const int b_bytes = box_rows(bx) * 128;
+        const CUtensorMap* bmap = m.gu ? (routed ? &maps.xperm[bx] : &maps.x[bx])
+                                       : (routed ? &maps.act[bx] : &maps.act_sh[bx]);
         for (int kc0 = 0; kc0 < m.nk; kc0 += KCH) {
           const int nch = min(KCH, m.nk - kc0);
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
@@ -432,7 +443,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
           uint8_t* b_s = a_s + KCH * SM::kChunkA;
           if constexpr (PAIR) {
             // both CTAs' bytes complete the leader's stage barrier
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * nch * (SM::kChunkA + SM::kChunkB));
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * nch * (SM::kChunkA + b_bytes));
             const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
             for (int c = 0; c < nch; ++c) {
               if (m.gu)
@@ -443,7 +454,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
             for (int c = 0; c < nch; ++c)
               tma_load_2d_pair(b_s + c * SM::kChunkB, bmap, fb, (kc0 + c) * 64, brow0, pol_x);
           } else {
-            mbar_arrive_expect_tx(&full[stage], nch * (SM::kChunkA + SM::kChunkB));
+            mbar_arrive_expect_tx(&full[stage], nch * (SM::kChunkA + b_bytes));
             // all K chunks of one weight row block back to back: neighbouring 128-byte pieces of
             // every row reach the memory system together
             for (int c = 0; c < nch; ++c) {
@@ -839,12 +850,15 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
                   make_map_gu(&maps.wsgu, S > 0 ? ws_gate_up : w_gate_up, S > 0 ? (uint64_t)S * I : 1,
                               S > 0 ? (uint64_t)S * I : 1, H) &&
                   make_map(&maps.wd, w_down, (uint64_t)E * H, I, 128) &&
-                  make_map(&maps.wsd, S > 0 ? ws_down : w_down, S > 0 ? (uint64_t)H : 1, S > 0 ? SI : I, 128) &&
-                  make_map(&maps.xperm, xperm, rows_routed, H, BROWS) && make_map(&maps.x, x, T, H, BROWS) &&
-                  make_map(&maps.act, act, rows_routed, I, BROWS) &&
-                  make_map(&maps.act_sh, S > 0 ? (const void*)act_sh : (const void*)act, S > 0 ? T : 1,
-                           S > 0 ? SI : I, BROWS);
+                  make_map(&maps.wsd, S > 0 ? ws_down : w_down, S > 0 ? (uint64_t)H : 1, S > 0 ? SI : I, 128);
   if (!ok) return cudaErrorInvalidValue;
+  for (int b = 0; b < kBoxN; ++b) {
+    const uint32_t h = box_rows(b) <= BROWS ? box_rows(b) : BROWS;  // heights past the tile: never chosen
+    if (!make_map(&maps.xperm[b], xperm, rows_routed, H, h) || !make_map(&maps.x[b], x, T, H, h) ||
+        !make_map(&maps.act[b], act, rows_routed, I, h) ||
+        !make_map(&maps.act_sh[b], S > 0 ? (const void*)act_sh : (const void*)act, S > 0 ? T : 1, S > 0 ? SI : I, h))
+      return cudaErrorInvalidValue;
+  }
 
   FfnParams p;
   p.T = T; p.H = H; p.E = E; p.k = k; p.S = S; p.I = I; p.G = G;
@@ -897,11 +911,20 @@ cudaError_t run_ffn(const bf16* x, const int32_t* perm, const int32_t* offsets, 
 #ifndef LSV_FFN_MAX_BN
 #define LSV_FFN_MAX_BN 256
 #endif
+#ifndef LSV_FFN_BN32_MAX_MEAN
+#define LSV_FFN_BN32_MAX_MEAN 20.0
+#endif
+#ifndef LSV_FFN_BN64_MAX_MEAN
+#define LSV_FFN_BN64_MAX_MEAN 44.0
+#endif
+#ifndef LSV_FFN_BN128_MAX_MEAN
+#define LSV_FFN_BN128_MAX_MEAN 96.0
+#endif
 int ffn_token_tile(int T, int k, int E) {
   const double mean = E > 0 ? (double)T * k / E : 0.0;
-  if (mean <= 20.0) return 32;
-  if (mean <= 44.0 || LSV_FFN_MAX_BN <= 64) return 64;
-  if (mean <= 96.0 || LSV_FFN_MAX_BN <= 128) return 128;
+  if (mean <= LSV_FFN_BN32_MAX_MEAN) return 32;
+  if (mean <= LSV_FFN_BN64_MAX_MEAN || LSV_FFN_MAX_BN <= 64) return 64;
+  if (mean <= LSV_FFN_BN128_MAX_MEAN || LSV_FFN_MAX_BN <= 128) return 128;
   return 256;
 }
 
