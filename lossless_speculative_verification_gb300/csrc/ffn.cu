@@ -580,12 +580,11 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     int* seg_first = tab + 10 + 2 * G;
     int* seg_rows = seg_first + p.E;
     if (p.seg_cap > 0) {
-      build_item_table(nullptr, p.seg_counts, p.T, p.H, p.E, p.k, p.S, p.I, p.BN, tab, p.err);
+      build_item_table(nullptr, p.seg_counts, p.T, p.H, p.E, p.k, p.S, p.I, p.BN, tab, p.err, seg_rows);
+      __syncwarp();
       for (int e = lane; e < p.E; e += 32) {
-        const int c = p.seg_counts[e];
         seg_first[e] = e * p.seg_cap;
-        seg_rows[e] = c;
-        if (p.counts_out && blockIdx.x == 0) p.counts_out[e] = c;
+        if (p.counts_out && blockIdx.x == 0) p.counts_out[e] = seg_rows[e];
       }
     } else {
       if (lane < 2) tab[lane] = p.table[lane];
