@@ -153,8 +153,8 @@ class ClockSampler:
 
 # per workload: the sources its kernels come from, and the first and last kernel of one step
 STEP_SOURCES = {
-    "draft": ("draft.cu", "attention.cu", "lmhead.cu", "accept.cu", "ffn.cu", "route.cu", "combine.cu", "ptx.cuh",
-              "api.cu"),
+    "draft": ("draft.cu", "skinny.cu", "attention.cu", "lmhead.cu", "accept.cu", "combine.cu", "ptx.cuh", "api.cu",
+              "tmap.h"),
     "layer": ("ffn.cu", "ptx.cuh", "route.cu", "permute.cu", "combine.cu", "ffn_plan.cuh", "api.cu", "tmap.h"),
     "lmhead": ("lmhead.cu", "accept.cu", "ptx.cuh", "api.cu", "tmap.h"),
     "attention": ("attention.cu", "ptx.cuh", "api.cu"),
@@ -862,6 +862,9 @@ def result_line(args, step, m, world, cpu):
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts, "algorithmic_flops": flops, "kernel": kernel,
                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}
+        if step.name == "draft" and roof["traffic"] is not None:
+            roof["traffic"] *= step.K   # the capture sums one recursion step; a launch of the loop runs K
+
     elif step.name == "prefill":
         achieved = flops / (m["layer_ms"] / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s", "frac": achieved / tflops,
