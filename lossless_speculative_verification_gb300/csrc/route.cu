@@ -2,19 +2,21 @@
 //
 // logits[t,e] = sum_h x[t,h] * W_r[e,h] with fp32 accumulation; p = softmax
 // over all E in fp32 (not renormalised over the selection); the k largest
-// logits in descending order with ties to the lower expert index.
-// (jina-ocr-v1: "64 routed experts ... Top-6 routing", kg.zhiyong.dev, section
-// "The speed comes from three layers working together".)
+// logits in descending order with ties to the lower expert index.  (The
+// jina-ocr-v1 decoder sends each token to 6 of its 64 routed experts;
+// kg.zhiyong.dev, section "The speed comes from three layers working together".)
 //
-// Up to 256 tokens (decode sizes) the router runs on CUDA cores, latency-first:
-// one CTA takes TT tokens.  Warp w computes experts 4w..4w+3 (then 4w+64..)
-// for all TT tokens; inside a warp each lane owns a contiguous 8-element slice
-// of every 256-element block of h (16-byte loads of x and W), and the 32
-// partial sums are combined by a fixed butterfly.  The summation order is fixed, so
-// results are run-to-run identical; it differs from a sequential sum only by
-// fp32 rounding (far below the router gaps the selection depends on).  The
-// E logits of each token then go through shared memory to one warp per token
-// for the softmax and the k selection rounds.
+// Up to 256 tokens (decode sizes) the router runs on CUDA cores, latency-first.
+// Up to 128 tokens: one cluster of eight CTAs per one or two tokens, each CTA
+// computing an eighth of the tokens' logits, which meet in the leader CTA's
+// shared memory; from 129 to 256 tokens: one CTA per token.  In both, each lane
+// owns a contiguous 8-element slice of every 256-element block of h (16-byte
+// loads of x and W) and the 32 partial sums are combined by a fixed butterfly;
+// the summation order is fixed, so results are run-to-run identical and equal
+// between the two forms; it differs from a sequential sum only by fp32 rounding
+// (far below the router gaps the selection depends on).  One warp per token
+// takes the softmax and the k selection rounds.  Above 256 tokens the product
+// is a dense contraction on tcgen05 (below).
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -22,9 +24,15 @@
 namespace lsv {
 namespace {
 
-constexpr int kRouteWarps = 16;
 constexpr int kRouteTcMinTokens = 256;  // above this many tokens the router runs on tensor cores
-constexpr int kExpPerWarp = 4;
+// Router form by token count (measured at 1..256 tokens): clusters of one token up to
+// LSV_ROUTE_TT1_MAX, clusters of two tokens up to LSV_ROUTE_CLUSTER_MAX, then one CTA per token.
+#ifndef LSV_ROUTE_TT1_MAX
+#define LSV_ROUTE_TT1_MAX 64
+#endif
+#ifndef LSV_ROUTE_CLUSTER_MAX
+#define LSV_ROUTE_CLUSTER_MAX 128
+#endif
 constexpr int kLoadAhead = 5;  // 16-byte pieces per row and lane in flight together (H = 1280: a whole row)
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
@@ -36,12 +44,190 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
+// One cluster of kRcCluster CTAs per TT tokens.  CTA r computes the logits of
+// experts [r*per, r*per + per) for the cluster's tokens (one warp per expert in
+// turn: each lane owns a contiguous 8-element slice of every 256-element block
+// of h, kLoadAhead 16-byte pieces of the weight row in flight together, a fixed
+// butterfly over the lanes) and stores them into the leader CTA's shared
+// memory.  After the cluster barrier the leader's warp i takes token i's
+// softmax and top-k, and all its warps place the tokens' rows.  Splitting the
+// experts over eight SMs cuts the router weight bytes each SM reads per token
+// eightfold; several tokens per cluster cut the weight bytes read in all.
+constexpr int kRcCluster = 8;
+constexpr int kRcWarps = 8;
+
+// Softmax over the E logits in lg (fp32) and the k largest, descending, ties to the lower
+// expert: k rounds of a warp-wide maximum over the experts not yet taken.  Lane r returns
+// the r-th choice (expert, probability) in (*e_out, *p_out); lanes >= k return -1.
+__device__ __forceinline__ void softmax_topk_warp(const float* lg, int E, int k, int* e_out, float* p_out) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPerLane = kMaxExperts / 32;
+  float v[kPerLane];
+  int taken = 0;  // bit j: expert lane + 32j is absent or already chosen
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kPerLane; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? lg[e] : -INFINITY;
+    if (e < E)
+      m = fmaxf(m, v[j]);
+    else
+      taken |= 1 << j;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float z = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kPerLane; ++j)
+    if (lane + 32 * j < E) z += expf(v[j] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  int my_e = -1;
+  float my_v = 0.0f;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int be = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+      const int e = lane + 32 * j;
+      if (!((taken >> j) & 1) && (v[j] > bv || (v[j] == bv && e < be))) {
+        bv = v[j];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be < E && (be & 31) == lane) taken |= 1 << (be >> 5);
+    if (lane == r) {
+      my_e = be < E ? be : -1;
+      my_v = bv;
+    }
+  }
+  *e_out = my_e;
+  *p_out = my_e >= 0 ? expf(my_v - m) / z : 0.0f;
+}
+
 template <int TT>
-__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __restrict__ x,
-                                                                 const bf16* __restrict__ wr, int T, int H,
-                                                                 int E, int k, int32_t* __restrict__ idx,
-                                                                 float* __restrict__ w,
-                                                                 float* __restrict__ logits, const RouteSlots sl) {
+__global__ void __launch_bounds__(kRcWarps * 32) route_cluster_kernel(const bf16* __restrict__ x,
+                                                                      const bf16* __restrict__ wr, int T, int H,
+                                                                      int E, int k, int32_t* __restrict__ idx,
+                                                                      float* __restrict__ w,
+                                                                      float* __restrict__ logits,
+                                                                      const RouteSlots sl) {
+  __shared__ float lg[TT][kMaxExperts];  // the leader's copy receives every CTA's logits
+  __shared__ int sel_row[TT][kMaxTopK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int t0 = blockIdx.y * TT;
+  const int nt = min(TT, T - t0);
+  const int n8 = H / 8;  // 16-byte groups per row
+  const int per = (E + kRcCluster - 1) / kRcCluster;
+  const int e_lo = (int)rank * per, e_hi = min(E, e_lo + per);
+  cluster_arrive_relaxed();  // the matching wait below: every CTA of the cluster is running
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t lg_leader = mapa_shared(smem_u32(&lg[0][0]), 0);
+  bool waited = false;
+  for (int e = e_lo + warp; e < e_hi; e += kRcWarps) {
+    float acc[TT];
+#pragma unroll
+    for (int i = 0; i < TT; ++i) acc[i] = 0.0f;
+    for (int c0 = lane; c0 < n8; c0 += 32 * kLoadAhead) {
+      uint4 wv[kLoadAhead];
+#pragma unroll
+      for (int u = 0; u < kLoadAhead; ++u) {
+        const int c = c0 + 32 * u;
+        wv[u] = c < n8 ? __ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < TT; ++i) {
+        uint4 xv[kLoadAhead];
+#pragma unroll
+        for (int u = 0; u < kLoadAhead; ++u) {
+          const int c = c0 + 32 * u;
+          xv[u] = (c < n8 && i < nt) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H) + c)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadAhead; ++u) {
+          float xf[8], wf[8];
+          bf16x8_to_f32(xv[u], xf);
+          bf16x8_to_f32(wv[u], wf);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i] = fmaf(xf[j], wf[j], acc[i]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < TT; ++i)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+    if (!waited) {
+      cluster_wait();
+      waited = true;
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+        st_shared_cluster_f32(lg_leader + 4u * (uint32_t)(i * kMaxExperts + e), acc[i]);
+  }
+  if (!waited) cluster_wait();
+  cluster_sync();  // the leader's lg holds all E logits (release by the writers, acquire here)
+  if (rank != 0) return;
+
+  const bool slots = sl.xperm != nullptr;
+  for (int i = warp; i < nt; i += kRcWarps) {
+    const int t = t0 + i;
+    if (logits)
+      for (int e = lane; e < E; e += 32) logits[(size_t)t * E + e] = lg[i][e];
+    int my_e;
+    float my_p;
+    softmax_topk_warp(lg[i], E, k, &my_e, &my_p);
+    if (lane < k && my_e >= 0) {
+      idx[(size_t)t * k + lane] = my_e;
+      w[(size_t)t * k + lane] = my_p;
+      if (slots) {
+        // the next free row of expert my_e's region
+        const int row = my_e * T + atomicAdd(&sl.slots[my_e], 1);
+        sl.inv[(size_t)t * k + lane] = row;
+        sel_row[i][lane] = row;
+      }
+    }
+  }
+  if (!slots) return;
+
+  // place the tokens' rows at their k rows of the routed row space
+  __syncthreads();
+  for (int q = warp; q < nt * k; q += kRcWarps) {
+    const int i = q / k, r = q - (q / k) * k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t0 + i) * H);
+    uint4* dst = reinterpret_cast<uint4*>(sl.xperm + (size_t)sel_row[i][r] * H);
+    for (int c = lane; c < n8; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+// From 129 to 256 tokens: one CTA of 16 warps per token.  Warp w computes experts
+// 4w..4w+3 (then 4w+64..) over the whole row, with the same lane layout and
+// summation order as the cluster kernel, so both give the same logits bit for
+// bit.  Measured faster than the clusters at 192 and 256 tokens (the clusters'
+// CTAs outnumber the SMs' slots there).
+constexpr int kRouteWarps = 16;
+constexpr int kExpPerWarp = 4;
+
+__global__ void __launch_bounds__(kRouteWarps * 32) route_token_kernel(const bf16* __restrict__ x,
+                                                                       const bf16* __restrict__ wr, int T, int H,
+                                                                       int E, int k, int32_t* __restrict__ idx,
+                                                                       float* __restrict__ w,
+                                                                       float* __restrict__ logits,
+                                                                       const RouteSlots sl) {
+  constexpr int TT = 1;
   __shared__ float lg[TT][kMaxExperts];
   __shared__ int sel_row[kMaxTopK];
   pdl_wait();
@@ -50,7 +236,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
   const int t0 = blockIdx.x * TT;
   const int nt = min(TT, T - t0);
   const int n8 = H / 8;  // 16-byte groups per row
-  const bool slots = TT == 1 && sl.xperm != nullptr;
+  const bool slots = sl.xperm != nullptr;
 
   // warp w owns experts [4w, 4w+4), [4w+64, 4w+68), ...; each lane loads kLoadAhead 16-byte pieces
   // of each of the four rows (and of x) before it uses any, so that one memory round trip
@@ -103,37 +289,22 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const bf16* __r
   }
   __syncthreads();
 
-  // softmax + top-k: one warp per token.  The selection is by rank: an expert's
-  // rank is the number of experts with a larger logit, or an equal logit and a
-  // lower index, so ranks are distinct and ties go to the lower index.
-  for (int i = warp; i < nt; i += kRouteWarps) {
-    const int t = t0 + i;
-    float m = -INFINITY;
-    for (int e = lane; e < E; e += 32) m = fmaxf(m, lg[i][e]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float z = 0.0f;
-    for (int e = lane; e < E; e += 32) z += expf(lg[i][e] - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  // softmax + top-k of the token by warp 0; lane r < k takes the r-th choice's row
+  if (warp == 0) {
+    const int t = t0;
     if (logits)
-      for (int e = lane; e < E; e += 32) logits[(size_t)t * E + e] = lg[i][e];
-    for (int e = lane; e < E; e += 32) {
-      const float v = lg[i][e];
-      int r = 0;
-      for (int e2 = 0; e2 < E; ++e2) {
-        const float v2 = lg[i][e2];
-        r += (v2 > v || (v2 == v && e2 < e)) ? 1 : 0;
-      }
-      if (r < k) {
-        idx[(size_t)t * k + r] = e;
-        w[(size_t)t * k + r] = expf(v - m) / z;
-        if (slots) {
-          // the next free row of expert e's region
-          const int row = e * T + atomicAdd(&sl.slots[e], 1);
-          sl.inv[(size_t)t * k + r] = row;
-          sel_row[r] = row;
-        }
+      for (int e = lane; e < E; e += 32) logits[(size_t)t * E + e] = lg[0][e];
+    int my_e;
+    float my_p;
+    softmax_topk_warp(lg[0], E, k, &my_e, &my_p);
+    if (lane < k && my_e >= 0) {
+      idx[(size_t)t * k + lane] = my_e;
+      w[(size_t)t * k + lane] = my_p;
+      if (slots) {
+        // the next free row of expert my_e's region
+        const int row = my_e * T + atomicAdd(&sl.slots[my_e], 1);
+        sl.inv[(size_t)t * k + lane] = row;
+        sel_row[lane] = row;
       }
     }
   }
@@ -347,10 +518,27 @@ cudaError_t launch_route(const bf16* x, const bf16* wr, int T, int H, int E, int
     if (E <= 128) return run_route_tc<128>(x, wr, T, H, E, k, idx, w, logits, dc->err, dc->device, s);
     return run_route_tc<256>(x, wr, T, H, E, k, idx, w, logits, dc->err, dc->device, s);
   }
-  const dim3 block(kRouteWarps * 32);
-  // about one CTA per SM at decode sizes; more tokens per CTA once T is large
-  // one CTA per token (at most 256 tokens here; more go to the tensor-core router above)
-  return launch_pdl(route_kernel<1>, dim3(T), block, 0, s, x, wr, T, H, E, k, idx, w, logits, sl);
+  if (T > LSV_ROUTE_CLUSTER_MAX)
+    return launch_pdl(route_token_kernel, dim3(T), dim3(kRouteWarps * 32), 0, s, x, wr, T, H, E, k, idx, w, logits,
+                      sl);
+  // one cluster per TT tokens
+  const int TT = T <= LSV_ROUTE_TT1_MAX ? 1 : 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kRcCluster, (T + TT - 1) / TT);
+  cfg.blockDim = dim3(kRcWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kRcCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (TT == 1) return cudaLaunchKernelEx(&cfg, route_cluster_kernel<1>, x, wr, T, H, E, k, idx, w, logits, sl);
+  return cudaLaunchKernelEx(&cfg, route_cluster_kernel<2>, x, wr, T, H, E, k, idx, w, logits, sl);
 }
 
 }  // namespace lsv

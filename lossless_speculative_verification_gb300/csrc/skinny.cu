@@ -5,11 +5,13 @@
 // many SMs as possible: the weight rows sit on the MMA's M side (128 per
 // tile), the rows of x on its N side (M rounded up to 16), and the K range of
 // a tile is split over the CTAs of a thread-block cluster (1, 2, 4 or 8,
-// chosen so that the launch fits one wave).  Each CTA of the cluster leaves
-// its fp32 partial tile in its own shared memory; after a cluster barrier
-// every CTA sums a slice of the tile's rows over distributed shared memory,
-// in cluster-rank order (so the result is deterministic), and stores bf16.
-// No workspace and no atomics.
+// chosen so that the launch fits one wave).  Cluster rank r owns a slice of
+// 128/ns accumulator rows: every CTA sends each slice of its fp32 partial tile
+// straight from TMEM to the slice's owner with asynchronous stores into
+// distributed shared memory (counted on the owner's mbarrier), and each owner
+// sums its slice over the ranks in rank order (so the result is
+// deterministic) and stores bf16.  No workspace, no atomics, and no CTA waits
+// for another to finish reading.
 //
 // One launch can carry up to three weight matrices that share x (the block's
 // q, k and v projections).  In the SwiGLU form the weight is a gate/up pair
@@ -58,9 +60,6 @@ struct SkMaps {
 
 __device__ __forceinline__ float sk_silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-// First accumulator row of cluster rank r's slice (even, so that a SwiGLU pair stays together).
-__device__ __forceinline__ int sk_slice_row(int r, int ns) { return ((r * 128) / ns) & ~1; }
-
 // Grid (nsplit, tiles): blockIdx.y is the weight tile, blockIdx.x its K split and cluster rank.
 template <bool kSwiglu>
 __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_constant__ SkMaps maps,
@@ -68,7 +67,7 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stage_bytes = kSkATile + p.n_mma * 128;
-  __shared__ uint64_t full[kSkMaxStages], empty[kSkMaxStages], tfull, final_bar;
+  __shared__ uint64_t full[kSkMaxStages], empty[kSkMaxStages], tfull, final_bar, recv_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -82,6 +81,10 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
   const int c0 = split * p.nk / ns, c1 = (split + 1) * p.nk / ns;  // at least one chunk (ns <= nk)
   uint32_t tcols = 32;
   while (tcols < (uint32_t)p.n_mma) tcols <<= 1;
+  // rank r sums accumulator rows [r * slot_rows, (r + 1) * slot_rows) (ns is 1, 2, 4 or 8, so a
+  // slice is even and SwiGLU pairs stay together); recv[src] receives rank src's partial of them
+  const int slot_rows = 128 / ns;
+  float* recv = reinterpret_cast<float*>(smem + p.stages * stage_bytes);  // [ns][slot_rows][n_mma]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -90,8 +93,11 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
     }
     mbar_init(&tfull, 1);
     mbar_init(&final_bar, 1);
+    mbar_init(&recv_bar, 1);
     abort_flag = 0;
     fence_barrier_init();
+    // the other ranks' partials of this CTA's rows
+    if (ns > 1) mbar_arrive_expect_tx(&recv_bar, (uint32_t)((ns - 1) * slot_rows * p.n_mma * 4));
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, tcols);
@@ -107,6 +113,7 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
   tc_fence_after_sync();
   const uint32_t tmem_base = tmem_slot;
   pdl_trigger();
+  cluster_arrive_relaxed();  // matched by one cluster_wait per thread before any store into a peer
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -151,6 +158,8 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
         mbar_arrive(&full[q % p.stages]);  // wake the MMA issuer so that it sees the abort
       }
     }
+    __syncwarp();
+    cluster_wait();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -187,16 +196,22 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
       if (!mbar_wait(&final_bar, 0, p.wait_ns)) set_error(p.err, kErrTimeout);
     }
     __syncwarp();
+    cluster_wait();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
-    // Warp w reads TMEM lanes 32*(w%4)..+31 (one weight row per thread) into the partial tile
-    // [128][n_mma] fp32 at the start of the ring, which no copy or MMA touches any more.
+    // Warp w reads TMEM lanes 32*(w%4)..+31 (one weight row per thread) and sends each row to
+    // the rank that sums it: into that rank's recv[split] (its own rows: plain shared stores).
     const bool got = mbar_wait(&tfull, 0, p.wait_ns);
     if (!got) set_error(p.err, kErrTimeout);
     tc_fence_after_sync();
     const int qd = warp & 3;
     const int row = 32 * qd + lane;
-    float* red = reinterpret_cast<float*>(smem) + row * p.n_mma;
+    const int dst_rank = row / slot_rows;
+    const int off = ((split * slot_rows) + row - dst_rank * slot_rows) * p.n_mma;
+    float* mine = recv + off;
+    cluster_wait();  // every CTA of the cluster runs, with its receive barrier armed
+    const uint32_t dst = mapa_shared(smem_u32(recv + off), (uint32_t)dst_rank);
+    const uint32_t dst_bar = mapa_shared(smem_u32(&recv_bar), (uint32_t)dst_rank);
     const uint32_t t_row = tmem_base + ((uint32_t)(32 * qd) << 16);
     const bool live = got && !abort_flag;
     for (int cc = 0; cc < p.n_mma; cc += 16) {
@@ -206,41 +221,46 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
         tmem_ld_wait();
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] = 0u;
+        for (int j = 0; j < 16; ++j) r[j] = 0u;  // the owner still counts these bytes
       }
 #pragma unroll
-      for (int j = 0; j < 16; j += 4)
-        *reinterpret_cast<float4*>(red + cc + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                               __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+      for (int j = 0; j < 16; j += 4) {
+        const float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                     __uint_as_float(r[j + 3]));
+        if (dst_rank == split)
+          *reinterpret_cast<float4*>(mine + cc + j) = v;
+        else
+          st_async_f4(dst + (uint32_t)((cc + j) * 4), v, dst_bar);
+      }
     }
     tc_fence_before_sync();
   }
   __syncwarp();
-  __syncthreads();
-  cluster_sync();  // every CTA's partial tile is complete and visible to the cluster
+  __syncthreads();  // this CTA's own rows are in recv[split]
+  if (ns > 1 && !mbar_wait(&recv_bar, 0, p.wait_ns)) set_error(p.err, kErrTimeout);  // and the others'
 
-  // ------------------------------------------------------------ reduction over the cluster
-  // This rank's slice of rows, summed over the ranks in rank order; 4 columns per unit.
+  // ------------------------------------------------------------ reduction of this rank's rows
+  // Summed over the ranks in rank order; 4 columns per unit.
   {
     const SkJob& jb = p.job[job];
-    const int r0 = sk_slice_row(split, ns), r1 = split + 1 == ns ? 128 : sk_slice_row(split + 1, ns);
+    const int r0 = split * slot_rows;
     const int q4 = p.n_mma / 4;
-    const uint32_t red_s = smem_u32(smem);
+    const int src_stride = slot_rows * p.n_mma;  // floats between two ranks' partials
     if (kSwiglu) {
       // units: (feature pair, 4 columns)
-      const int units = (r1 - r0) / 2 * q4;
+      const int units = slot_rows / 2 * q4;
       for (int u = threadIdx.x; u < units; u += kSkThreads) {
-        const int pr = r0 / 2 + u / q4, c4 = u % q4;
-        const uint32_t off_g = (uint32_t)(((2 * pr) * p.n_mma + 4 * c4) * 4);
-        const uint32_t off_u = off_g + (uint32_t)(p.n_mma * 4);
-        // every rank's values first (independent remote loads in flight together), then the sums
+        const int pl = u / q4, c4 = u % q4;  // pair within the slice
+        const float* pg = recv + (2 * pl) * p.n_mma + 4 * c4;
+        const float* pu = pg + p.n_mma;
         float4 a[8], b[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r)
           if (r < ns) {
-            a[r] = ld_shared_cluster_f4(mapa_shared(red_s + off_g, (uint32_t)r));
-            b[r] = ld_shared_cluster_f4(mapa_shared(red_s + off_u, (uint32_t)r));
+            a[r] = *reinterpret_cast<const float4*>(pg + r * src_stride);
+            b[r] = *reinterpret_cast<const float4*>(pu + r * src_stride);
           }
+        const int pr = r0 / 2 + pl;
         float4 g = make_float4(0.f, 0.f, 0.f, 0.f), v = g;
 #pragma unroll
         for (int r = 0; r < 8; ++r)
@@ -260,15 +280,16 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
       }
     } else {
       // units: (row, 4 columns), consecutive threads on consecutive rows (coalesced stores)
-      const int rows = r1 - r0;
+      const int rows = slot_rows;
       const int units = rows * q4;
       for (int u = threadIdx.x; u < units; u += kSkThreads) {
-        const int rr = r0 + u % rows, c4 = u / rows;
-        const uint32_t off = (uint32_t)((rr * p.n_mma + 4 * c4) * 4);
+        const int rl = u % rows, c4 = u / rows;
+        const int rr = r0 + rl;
+        const float* pa = recv + rl * p.n_mma + 4 * c4;
         float4 a[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r)
-          if (r < ns) a[r] = ld_shared_cluster_f4(mapa_shared(red_s + off, (uint32_t)r));
+          if (r < ns) a[r] = *reinterpret_cast<const float4*>(pa + r * src_stride);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int r = 0; r < 8; ++r)
@@ -287,7 +308,6 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
       }
     }
   }
-  cluster_sync();  // no CTA leaves while another still reads its shared memory
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, tcols);
@@ -295,16 +315,16 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
 }
 
 // Ring stages: `base` (four keep two CTAs per SM up to 64 rows of x; eight give a lone CTA per SM
-// more bytes in flight), within 200 KB, and enough to hold the fp32 partial tile.
+// more bytes in flight), within 200 KB together with the receive slots (at least two).
 int sk_stages(int n_mma, int base) {
   const int stage = kSkATile + n_mma * 128;
-  int st = base;
-  while (st > 2 && st * stage > 200 * 1024) --st;
-  while (st * stage < 128 * n_mma * 4) ++st;
-  return st > kSkMaxStages ? kSkMaxStages : st;
+  int st = base > kSkMaxStages ? kSkMaxStages : base;
+  while (st > 2 && st * stage + 512 * n_mma > 200 * 1024) --st;
+  return st;
 }
 
-int sk_smem(int n_mma, int stages) { return 1024 + stages * (kSkATile + n_mma * 128); }
+// The ring, then the receive slots: ns ranks x 128/ns rows x n_mma fp32 = 512 n_mma bytes.
+int sk_smem(int n_mma, int stages) { return 1024 + stages * (kSkATile + n_mma * 128) + 512 * n_mma; }
 
 // CTAs of clusters of `ns` that the device holds at once for this shared-memory size (cached).
 int sk_capacity(bool swiglu, int ns, int smem, const DeviceCtx& dc) {

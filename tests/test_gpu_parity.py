@@ -57,6 +57,24 @@ def test_route_parity_tensor_core_path(T, H, E, k):
     np.testing.assert_allclose(w.cpu().numpy(), rp, rtol=1e-5, atol=1e-9)
 
 
+@pytest.mark.parametrize("T,H,E,k", [(1, 1280, 64, 6), (37, 2048, 128, 4), (97, 1280, 64, 6), (128, 512, 256, 8),
+                                     (129, 1280, 64, 6), (193, 512, 256, 8), (256, 256, 8, 2), (255, 1280, 64, 1)])
+def test_route_parity_cuda_core_paths(T, H, E, k):
+    """Up to 128 tokens the router runs as clusters of eight CTAs over one or two tokens (ragged last
+    cluster included), each CTA an eighth of the experts; from 129 to 256 tokens as one CTA per token.
+    H past one 1,280-wide pass of the lanes."""
+    d = synth.MoeDims(T, H, E, k, 0, 64)
+    prob = synth.moe_problem(d, seed=3 * T + E, hidden="sphere", row_ok=oracle.gap_ok(k))
+    x, wr = to_dev(prob.x), to_dev(prob.w_router)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    idx, w = api.moe_route(x, wr, k, logits=logits)
+    torch.cuda.synchronize()
+    ridx, rp, rlog = oracle.route(prob.x, prob.w_router, k, return_logits=True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(logits.cpu().numpy(), rlog, rtol=0, atol=2e-5 * np.sqrt(H / 256))
+    np.testing.assert_allclose(w.cpu().numpy(), rp, rtol=1e-5, atol=1e-9)
+
+
 # ----------------------------------------------------------------------------- permutation
 def random_routing(T, k, E, seed):
     rs = np.random.default_rng(seed)
