@@ -9,8 +9,8 @@
 // particularly well"; evolve.pub review, Section 3.1 / Eq. 2).
 //
 // Phase 1 streams the logits once: each CTA owns a chunk of one row, streams it
-// through a ring of shared-memory buffers filled by 1-D bulk copies (64 KB in
-// flight per CTA from a single issuing thread), scans it and writes the
+// through a ring of shared-memory buffers filled by 1-D bulk copies (48 KB in
+// flight per CTA from a single issuing thread, four CTAs per SM), scans it and writes the
 // chunk's (max, first index).  Phase 2 (one CTA per sequence, one warp per
 // row) reduces the chunk partials and applies the rule.
 // No atomics decide anything, so the result is deterministic.
@@ -27,13 +27,13 @@ namespace {
 
 constexpr int kAccThreads = 256;
 #ifndef LSV_ACC_CTAS_PER_SM
-#define LSV_ACC_CTAS_PER_SM 3
+#define LSV_ACC_CTAS_PER_SM 4
 #endif
 #ifndef LSV_ACC_PIECE
 #define LSV_ACC_PIECE 16384
 #endif
 #ifndef LSV_ACC_RING
-#define LSV_ACC_RING 4
+#define LSV_ACC_RING 3
 #endif
 constexpr int kAccCtasPerSm = LSV_ACC_CTAS_PER_SM;  // resident CTAs per SM the chunking plans for (one wave)
 constexpr int kPiece = LSV_ACC_PIECE;                // bytes per bulk copy

@@ -21,10 +21,6 @@ struct PrefetchPlan {
 
 constexpr uint64_t kPrefetchChunk = 32768;
 
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __global__ void __launch_bounds__(128) l2_prefetch_kernel(const PrefetchPlan plan) {
   // the weights are never written by the preceding kernels: start at once, and
   // only wait for the predecessor at the end, so that this kernel's completion
@@ -44,7 +40,7 @@ __global__ void __launch_bounds__(128) l2_prefetch_kernel(const PrefetchPlan pla
     const uint64_t left = plan.budget - j * kPrefetchChunk;
     if (len > left) len = left;
     len &= ~uint64_t(15);
-    if (len) prefetch_l2(plan.base[r] + off, (uint32_t)len);
+    if (len) prefetch_l2_bulk(plan.base[r] + off, (uint32_t)len);
   }
   pdl_wait();
 }
