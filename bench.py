@@ -879,8 +879,13 @@ def result_line(args, step, m, world, cpu):
                      "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "layer_ms": m["layer_ms"],
                      "kernel_source_hash": khash})
     if acc_bytes:
+        # "ms": the acceptance launches between two events (the event costs them their early launch);
+        # "in_step_ms": what they add to the step, the step time less the layer's
+        in_step = m["total_ms"] / args.steps - m["layer_ms"]
         roof["accept"] = {"ms": m["accept_ms"], "algorithmic_bytes": acc_bytes,
-                          "achieved_gbs": acc_bytes / (m["accept_ms"] / 1e3) / 1e9}
+                          "achieved_gbs": acc_bytes / (m["accept_ms"] / 1e3) / 1e9,
+                          "in_step_ms": in_step,
+                          "in_step_gbs": acc_bytes / (in_step / 1e3) / 1e9 if in_step > 0 else None}
     tokens = step.T * world * args.steps
     line = {
         "metric": METRIC, "value": job_tokens_per_s(step.T, world, args.steps, m["total_ms"]), "unit": "tokens/s",

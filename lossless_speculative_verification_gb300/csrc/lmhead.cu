@@ -26,6 +26,9 @@
 namespace lsv {
 namespace {
 
+#ifndef LSV_LH_FIT_ROWS
+#define LSV_LH_FIT_ROWS 1
+#endif
 constexpr int kLhThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kLhEpiThreads = 128;
 constexpr int kLhStages = 6;
@@ -44,6 +47,7 @@ struct LhParams {
   int ntv;     // vocabulary tiles
   int nitems;  // row tiles x vocabulary tiles
   int nslot;   // partials per row: min(ntv, grid); vocabulary tile tv goes to slot tv % nslot
+  int hbytes;  // bytes of one hidden-row chunk the producer stages (rows of the box x 128)
   float* pv;   // [R, nslot] maxima over a CTA's vocabulary tiles of the row
   int* pi;     // [R, nslot] their first indices
   int* err;
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
           }
           uint8_t* a_s = smem + stage * LhSmem::kStage;
           uint8_t* b_s = a_s + kLhChunk;
-          mbar_arrive_expect_tx(&full[stage], 2 * kLhChunk);
+          mbar_arrive_expect_tx(&full[stage], p.hbytes + kLhChunk);
           tma_load_2d(a_s, &hmap, &full[stage], kc * 64, tr * kLhTile, pol_x);
           tma_load_2d(b_s, &wmap, &full[stage], kc * 64, tv * kLhTile, pol_w);
           if (++stage == kLhStages) {
@@ -280,8 +284,14 @@ cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const 
   p.pi = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + one);
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();
+  // Fewer than 128 positions (one row tile): stage only their rows, rounded up to 16.  The MMA
+  // still reads 128 rows of the A tile; the rows past them hold whatever an earlier stage left,
+  // and their results are never written (rows >= R are skipped).  This cuts the bytes each
+  // stage moves into shared memory from 32 KB to 18-24 KB at draft and small-batch sizes.
+  const int hrows = (LSV_LH_FIT_ROWS && R < kLhTile) ? (R + 15) / 16 * 16 : kLhTile;
+  p.hbytes = hrows * 128;
   CUtensorMap hmap, wmap;
-  if (!make_map(&hmap, hidden, R, H, kLhTile) || !make_map(&wmap, w_vocab, V, H, kLhTile))
+  if (!make_map(&hmap, hidden, R, H, (uint32_t)hrows) || !make_map(&wmap, w_vocab, V, H, kLhTile))
     return cudaErrorInvalidValue;
   const int grid = p.nitems < dc.num_sms ? p.nitems : dc.num_sms;
   // a CTA's vocabulary tiles of one row tile are congruent modulo the grid: one slot per CTA
