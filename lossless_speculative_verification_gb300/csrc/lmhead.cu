@@ -31,12 +31,26 @@ namespace {
 #endif
 constexpr int kLhThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kLhEpiThreads = 128;
-constexpr int kLhStages = 6;
-constexpr int kLhTile = 128;             // rows of either operand per item
-constexpr int kLhChunk = kLhTile * 128;  // bytes of one 64-wide K chunk of either operand
+// Vocabulary rows per tile.  Each stage moves the 128 hidden rows' chunk and the weight rows'
+// chunk into shared memory, and the hidden part is re-read for every tile; that fill, not HBM,
+// bounds the kernel at 128 rows per tile.  176 rows make the weights 58 % of the fill instead of
+// 50 %, and 129,280 rows give 735 tiles, 4.8 per SM (5 on most SMs), a smaller tail than 1,010
+// tiles of 128 (6.6 per SM).
+#ifndef LSV_LH_N
+#define LSV_LH_N 176
+#endif
+constexpr int kLhTile = 128;              // hidden rows per row tile (the MMA's M)
+constexpr int kLhN = LSV_LH_N;            // vocabulary rows per tile (the MMA's N: a multiple of 16, <= 256)
+constexpr int kLhChunk = kLhTile * 128;   // bytes of one 64-wide K chunk of the hidden rows
+constexpr int kLhWChunk = kLhN * 128;     // the same for the weight rows
+constexpr int kLhStages = (192 * 1024) / (kLhChunk + kLhWChunk);
+constexpr int kLhAccCols = kLhN <= 128 ? 128 : 256;  // TMEM columns between the two accumulators
+constexpr int kLhTmemCols = 2 * kLhAccCols;
+static_assert(kLhN % 16 == 0 && kLhN >= 16 && kLhN <= 256, "MMA N");
+static_assert(kLhWChunk % 1024 == 0, "128-byte swizzle atoms");
 
 struct LhSmem {
-  static constexpr int kStage = 2 * kLhChunk;
+  static constexpr int kStage = kLhChunk + kLhWChunk;
   static constexpr int kRing = kLhStages * kStage;
   static constexpr int kBars = (2 * kLhStages + 5) * 8;
   static constexpr int kTotal = 1024 /*alignment slack*/ + kRing + kBars + 16;
@@ -47,7 +61,9 @@ struct LhParams {
   int ntv;     // vocabulary tiles
   int nitems;  // row tiles x vocabulary tiles
   int nslot;   // partials per row: min(ntv, grid); vocabulary tile tv goes to slot tv % nslot
-  int hbytes;  // bytes of one hidden-row chunk the producer stages (rows of the box x 128)
+  int hbytes;       // bytes of one hidden-row chunk of a full row tile (rows of the box x 128)
+  int hbytes_last;  // the same for the last row tile
+  int wbytes_last;  // bytes of one weight-row chunk of the last vocabulary tile
   float* pv;   // [R, nslot] maxima over a CTA's vocabulary tiles of the row
   int* pi;     // [R, nslot] their first indices
   int* err;
@@ -55,7 +71,9 @@ struct LhParams {
 };
 
 __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __grid_constant__ CUtensorMap hmap,
+                                                                      const __grid_constant__ CUtensorMap hmap_last,
                                                                       const __grid_constant__ CUtensorMap wmap,
+                                                                      const __grid_constant__ CUtensorMap wmap_last,
                                                                       const LhParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -83,12 +101,14 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 2 * kLhTile);
+    tmem_alloc(tmem_slot, kLhTmemCols);
     tmem_relinquish();
   }
   if (threadIdx.x == 32) {
     tma_prefetch_desc(&hmap);
+    tma_prefetch_desc(&hmap_last);
     tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&wmap_last);
   }
   __syncwarp();
   tc_fence_before_sync();
@@ -107,8 +127,14 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const int ntr = p.nitems / p.ntv;
       for (int it = blockIdx.x; it < p.nitems && ok; it += gridDim.x) {
         const int tr = it / p.ntv, tv = it - tr * p.ntv;
+        const bool last = tr == ntr - 1, last_v = tv == p.ntv - 1;
+        const CUtensorMap* hm = last ? &hmap_last : &hmap;
+        const CUtensorMap* wm = last_v ? &wmap_last : &wmap;
+        const int hb = last ? p.hbytes_last : p.hbytes;
+        const int wb = last_v ? p.wbytes_last : kLhWChunk;
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns)) {
             set_error(p.err, kErrTimeout);
@@ -117,9 +143,9 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
           }
           uint8_t* a_s = smem + stage * LhSmem::kStage;
           uint8_t* b_s = a_s + kLhChunk;
-          mbar_arrive_expect_tx(&full[stage], p.hbytes + kLhChunk);
-          tma_load_2d(a_s, &hmap, &full[stage], kc * 64, tr * kLhTile, pol_x);
-          tma_load_2d(b_s, &wmap, &full[stage], kc * 64, tv * kLhTile, pol_w);
+          mbar_arrive_expect_tx(&full[stage], hb + wb);
+          tma_load_2d(a_s, hm, &full[stage], kc * 64, tr * kLhTile, pol_x);
+          tma_load_2d(b_s, wm, &full[stage], kc * 64, tv * kLhN, pol_w);
           if (++stage == kLhStages) {
             stage = 0;
             phase ^= 1u;
@@ -140,7 +166,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      const uint32_t idesc = idesc_bf16_f32(kLhTile, kLhTile);
+      const uint32_t idesc = idesc_bf16_f32(kLhTile, kLhN);
       for (int it = blockIdx.x; it < p.nitems && ok; it += gridDim.x) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.wait_ns)) {
           set_error(p.err, kErrTimeout);
@@ -148,7 +174,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kLhTile);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kLhAccCols);
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait(&full[stage], phase, p.wait_ns)) {
             set_error(p.err, kErrTimeout);
@@ -223,10 +249,10 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
       }
       cur_tv = tv;
       tc_fence_after_sync();
-      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kLhTile);
-      const int v0 = tv * kLhTile;
-      const int vn = min(kLhTile, p.V - v0);  // columns past the vocabulary hold zero-filled rows
-      for (int c0 = 0; c0 < kLhTile; c0 += 16) {
+      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kLhAccCols);
+      const int v0 = tv * kLhN;
+      const int vn = min(kLhN, p.V - v0);  // columns past the vocabulary hold zero-filled rows
+      for (int c0 = 0; c0 < kLhN; c0 += 16) {
         uint32_t r[16];
         tmem_ld_32x32b_x16(t_row + c0, r);
         tmem_ld_wait();
@@ -252,7 +278,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, 2 * kLhTile);
+    tmem_dealloc(tmem_base, kLhTmemCols);
   }
 }
 
@@ -260,7 +286,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
 
 size_t lmhead_ws_bytes(int B, int K, int V) {
   const size_t R = (size_t)B * (K + 1);
-  const size_t ntv = ((size_t)V + kLhTile - 1) / kLhTile;
+  const size_t ntv = ((size_t)V + kLhN - 1) / kLhN;
   const size_t one = (R * ntv * 4 + 255) / 256 * 256;
   return R == 0 ? 256 : 2 * one;
 }
@@ -277,26 +303,35 @@ cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const 
   p.R = R;
   p.H = H;
   p.V = V;
-  p.ntv = (V + kLhTile - 1) / kLhTile;
+  p.ntv = (V + kLhN - 1) / kLhN;
   p.nitems = ((R + kLhTile - 1) / kLhTile) * p.ntv;
   const size_t one = ((size_t)R * p.ntv * 4 + 255) / 256 * 256;
   p.pv = reinterpret_cast<float*>(ws);
   p.pi = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + one);
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();
-  // Fewer than 128 positions (one row tile): stage only their rows, rounded up to 16.  The MMA
-  // still reads 128 rows of the A tile; the rows past them hold whatever an earlier stage left,
-  // and their results are never written (rows >= R are skipped).  This cuts the bytes each
-  // stage moves into shared memory from 32 KB to 18-24 KB at draft and small-batch sizes.
-  const int hrows = (LSV_LH_FIT_ROWS && R < kLhTile) ? (R + 15) / 16 * 16 : kLhTile;
-  p.hbytes = hrows * 128;
-  CUtensorMap hmap, wmap;
-  if (!make_map(&hmap, hidden, R, H, (uint32_t)hrows) || !make_map(&wmap, w_vocab, V, H, kLhTile))
+  // The last row tile stages only the rows it has, rounded up to 16 (a TMA box reaching far past
+  // the tensor's end makes every load of it slow: 92 vs 62 us for the whole call at 32 positions).
+  // The MMA still reads 128 rows of the A tile; the rows past them hold whatever an earlier stage
+  // left, and their results are never written (rows >= R are skipped).
+  const int tail = R - (R - 1) / kLhTile * kLhTile;  // rows of the last row tile, 1..128
+  const int hrows_last = LSV_LH_FIT_ROWS ? (tail + 15) / 16 * 16 : kLhTile;
+  p.hbytes = kLhTile * 128;
+  p.hbytes_last = hrows_last * 128;
+  // the same for the last vocabulary tile's weight rows
+  const int vtail = V - (p.ntv - 1) * kLhN;
+  const int wrows_last = LSV_LH_FIT_ROWS ? (vtail + 15) / 16 * 16 : kLhN;
+  p.wbytes_last = wrows_last * 128;
+  CUtensorMap hmap, hmap_last, wmap, wmap_last;
+  if (!make_map(&hmap, hidden, R, H, kLhTile) || !make_map(&hmap_last, hidden, R, H, (uint32_t)hrows_last) ||
+      !make_map(&wmap, w_vocab, V, H, kLhN) || !make_map(&wmap_last, w_vocab, V, H, (uint32_t)wrows_last))
     return cudaErrorInvalidValue;
   const int grid = p.nitems < dc.num_sms ? p.nitems : dc.num_sms;
   // a CTA's vocabulary tiles of one row tile are congruent modulo the grid: one slot per CTA
   p.nslot = p.ntv < grid ? p.ntv : grid;
-  cudaError_t e = launch_pdl(lmhead_argmax_kernel, dim3(grid), dim3(kLhThreads), LhSmem::kTotal, s, hmap, wmap, p);
+  cudaError_t e =
+      launch_pdl(lmhead_argmax_kernel, dim3(grid), dim3(kLhThreads), LhSmem::kTotal, s, hmap, hmap_last, wmap,
+                 wmap_last, p);
   if (e != cudaSuccess) return e;
   return launch_accept_finalize(p.pv, p.pi, p.nslot, drafts, B, K, argmax, accept_len, committed, s);
 }

@@ -58,9 +58,11 @@ def test_lmhead_decode_shape():
 
 
 @pytest.mark.parametrize("B,K,V,H", [(1, 1, 129_280, 1280), (40, 3, 5000, 256), (3, 0, 1000, 128),
-                                     (64, 7, 4099, 192)])
+                                     (64, 7, 4099, 192), (32, 0, 129_280, 1280), (17, 7, 3001, 256),
+                                     (9, 7, 2000, 128)])
 def test_lmhead_shapes(B, K, V, H):
-    # one sequence; two row tiles (160 rows); K = 0; ragged vocabulary tiles (V % 128 != 0)
+    # one sequence; two row tiles (160 rows); K = 0; ragged vocabulary tiles (V % 128 != 0); the draft
+    # block's 32 rows; a last row tile of 8 rows (box of 16); 72 rows in one tile (box of 80)
     check(problem(B, K, V, H, 1000 * B + K))
 
 
