@@ -852,7 +852,7 @@ def result_line(args, step, m, world, cpu):
     if step.name in SIDE_STEPS:
         achieved = byts / (m["total_ms"] / args.steps / 1e3) / 1e9
         kernel = ("lmhead_argmax_kernel (tcgen05 product of the output layer and the hidden rows, reduced "
-                  "to each row's (max, first index) per 128-token vocabulary tile) + accept_finalize_kernel"
+                  "to each row's (max, first index) per 176-row vocabulary tile) + accept_finalize_kernel"
                   if step.name == "lmhead" else
                   "attn_split_kernel (persistent: TMA key/value tiles, warp MMAs for scores and weighted values, "
                   "online softmax in fp32, one state per 256-position split) + attn_combine_kernel"
