@@ -352,11 +352,20 @@ class DeviceStep:
         return h2d, d2h
 
     def e2e(self):
+        import torch
+        cur = torch.cuda.current_stream(self.dev)
+        if self.logits is not None:
+            # the acceptance's inputs travel on a second stream while the layer runs
+            if not hasattr(self, "copy_stream"):
+                self.copy_stream = torch.cuda.Stream(self.dev)
+            self.copy_stream.wait_stream(cur)
+            with torch.cuda.stream(self.copy_stream):
+                self.dl.copy_(self.hl, non_blocking=True)
+                self.dd.copy_(self.hd, non_blocking=True)
         self.dx.copy_(self.hx, non_blocking=True)
         self._layers(self.dx)
         if self.logits is not None:
-            self.dl.copy_(self.hl, non_blocking=True)
-            self.dd.copy_(self.hd, non_blocking=True)
+            cur.wait_stream(self.copy_stream)
             self.api.spec_verify_accept(self.dl, self.dd, self.aws, accept_len=self.alen, committed=self.comm)
             self.h_len.copy_(self.alen, non_blocking=True)
             self.h_comm.copy_(self.comm, non_blocking=True)
