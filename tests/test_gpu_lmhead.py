@@ -49,7 +49,7 @@ def check(p):
 
 @functools.lru_cache(maxsize=None)
 def problem(B, K, V, H, seed):
-    return synth.lmhead_problem(B, K, V=V, H=H, seed=seed, judge=oracle.lmhead_judge())
+    return synth.lmhead_problem(B, K, V=V, H=H, seed=seed, row_check=oracle.lmhead_row_check())
 
 
 def test_lmhead_decode_shape():
