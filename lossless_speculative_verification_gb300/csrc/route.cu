@@ -58,10 +58,12 @@ constexpr int kRcWarps = 8;
 
 // Softmax over the E logits in lg (fp32) and the k largest, descending, ties to the lower
 // expert: k rounds of a warp-wide maximum over the experts not yet taken.  Lane r returns
-// the r-th choice (expert, probability) in (*e_out, *p_out); lanes >= k return -1.
-__device__ __forceinline__ void softmax_topk_warp(const float* lg, int E, int k, int* e_out, float* p_out) {
+// the r-th choice (expert, probability) in (*e_out, *p_out); lanes >= k return -1.  kPerLane
+// experts per lane (E <= 32 kPerLane): one warp's dependent chain, so it is instantiated for
+// the smallest count that holds E.
+template <int kPerLane>
+__device__ __forceinline__ void softmax_topk_warp_n(const float* lg, int E, int k, int* e_out, float* p_out) {
   const int lane = threadIdx.x & 31;
-  constexpr int kPerLane = kMaxExperts / 32;
   float v[kPerLane];
   int taken = 0;  // bit j: expert lane + 32j is absent or already chosen
   float m = -INFINITY;
@@ -112,6 +114,15 @@ __device__ __forceinline__ void softmax_topk_warp(const float* lg, int E, int k,
   }
   *e_out = my_e;
   *p_out = my_e >= 0 ? expf(my_v - m) / z : 0.0f;
+}
+
+__device__ __forceinline__ void softmax_topk_warp(const float* lg, int E, int k, int* e_out, float* p_out) {
+  if (E <= 64)
+    softmax_topk_warp_n<2>(lg, E, k, e_out, p_out);
+  else if (E <= 128)
+    softmax_topk_warp_n<4>(lg, E, k, e_out, p_out);
+  else
+    softmax_topk_warp_n<kMaxExperts / 32>(lg, E, k, e_out, p_out);
 }
 
 template <int TT>
