@@ -603,7 +603,7 @@ class DraftStep:
         # per step: input norms + W_p + norm + q/k/v + append + attention (2) + W_o + residual norm
         # + gate/up (SwiGLU) + down + residual norm + output layer (2) = 14 kernels, plus the copy of
         # the tokens
-        self.launches = 14 * self.K
+        self.launches = 11 * self.K
 
     @classmethod
     def host_only(cls, seed):
@@ -853,8 +853,9 @@ def result_line(args, step, m, world, cpu):
                   "attn_split_kernel (persistent: TMA key/value tiles, warp MMAs for scores and weighted values, "
                   "online softmax in fp32, one state per 256-position split) + attn_combine_kernel"
                   if step.name == "attention" else
-                  "spec_draft_loop: 14 launches per step (skinny_gemm_kernel split-K projections with q/k/v in "
-                  "one launch and the SwiGLU FFN in two, attention, norms, fused output-layer argmax)")
+                  "spec_draft_loop: 11 launches per step (skinny_gemm_kernel split-K projections with q/k/v in "
+                  "one launch and the SwiGLU FFN in two, the RMSNorms and residual adds folded into them, "
+                  "attention, fused output-layer argmax)")
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "algorithmic_bytes": byts, "algorithmic_flops": flops, "kernel": kernel,
                 "peak_source": peak_src, "traffic": ncu_traffic(step.name, khash), "kernel_source_hash": khash}
@@ -1058,7 +1059,7 @@ def run_spec(args, rank, world, local, dev, flush):
             t_draft = statistics.median(times[1]) if K else 0.0
             step_ms[(B, K)], draft_ms[(B, K)] = t_step, t_draft
             tau = float(api.spec_k_policy(list(synth.PAGE_ACCEPT[:K]) or [0.0], [1.0] * (K + 1) if K else [1.0, 1.0])[1][K])
-            launches = dec.launches_per_verify(B, Q) + 14 * K
+            launches = dec.launches_per_verify(B, Q) + 11 * K
             if rank == 0:
                 print(json.dumps({
                     "metric": "speculative step: %d-layer verify pass over B x (K+1) positions after K draft-block "

@@ -302,14 +302,20 @@ typedef struct {
  *     q attends to positions 0..ctx_len[b] + i - 1 (scale 1/sqrt(H/nh))
  *   u = u + W_o attn;  f = RMSNorm(u);  u = u + W_down (silu(W_gate f) * W_up f)
  *   t = argmax_v (W_vocab RMSNorm(u))_v (the smallest index of the maximum), h = u
- * RMSNorm: unit weight, eps 1e-6.  Every value between kernels is bf16.
+ * RMSNorm: unit weight, eps 1e-6.  Every value stored between kernels is bf16:
+ * the block input, u, q, k, v, the attention output, the activation; the
+ * RMSNorms of u are folded into the products that read them (each output row
+ * scaled by its input row's 1/rms in fp32) and never stored, the residual adds
+ * happen in the products' epilogues, and t is taken from W_vocab u (the same
+ * greedy token: the norm scales a row's logits by one positive factor).
  * drafts [B, K] int32 (device) receives t of every step; h_out [B, H] bf16
  * (optional) the last u.  ctx_len [B] int32 (device) is read, not written;
  * ctx_len[b] + K <= L.  Supported: 0 <= B <= 256, H % 64 == 0, H <= 16384,
- * H/nh in {64, 128}, I % 64 == 0, I <= 16384, 1 <= K <= 63.  Per step: the
- * projections as the few-row products of dense_matmul / dense_swiglu (q, k and
- * v in one launch), the attention of spec_verify_attention at one query, and
- * the output layer fused with the greedy search of spec_verify_lmhead.
+ * H/nh in {64, 128}, I % 64 == 0, I <= 16384, 1 <= K <= 63.  Per step, 11
+ * launches: the block input's norms, the projections as the few-row products of
+ * dense_matmul / dense_swiglu (q, k and v in one launch), the cache append, the
+ * attention of spec_verify_attention at one query, and the output layer fused
+ * with the greedy search of spec_verify_lmhead.
  * ws: spec_draft_workspace_size(B, H, nh, I, V, L) bytes, zero before the first
  * use; calls that raise no device error leave it fit for the next call. */
 size_t spec_draft_workspace_size(int32_t B, int32_t H, int32_t nh, int32_t I, int32_t V, int32_t L);

@@ -460,24 +460,37 @@ lsv_status spec_draft_loop(const lsv_draft_weights* wt, const void* h0, const in
       return launch_skinny(x, B, K_, &wm, &n, &y, &ldy, 1, swiglu, *dc, s);
     };
     if (e == cudaSuccess) e = sk1(act(L8.inp), 2 * H, wgt(wt->w_proj), nH, act(L8.u), ldH, false);
-    if (e == cudaSuccess)
-      e = launch_pdl(draft_norm_kernel, dim3(B, 1), dim3(kDnThreads), 0, s, (const bf16*)act(L8.u), emb,
-                     (const int32_t*)nullptr, V, act(L8.a), H, H, eps, dc->err);
-    if (e == cudaSuccess) e = launch_skinny(act(L8.a), B, H, wqkv, nqkv, yqkv, ldqkv, 3, false, *dc, s);
+    // q, k, v of RMSNorm(u): the norm is folded into the products (each output row scaled by its
+    // input row's 1/rms), so the normalised rows are never stored
+    if (e == cudaSuccess) e = launch_skinny(act(L8.u), B, H, wqkv, nqkv, yqkv, ldqkv, 3, false, *dc, s, eps);
     if (e == cudaSuccess)
       e = launch_pdl(draft_append_kernel, dim3(B), dim3(128), 0, s, (const bf16*)act(L8.k), (const bf16*)act(L8.v), kc,
                      vc, len_cur, len_next, L, H, dc->err);
     if (e == cudaSuccess)
       e = launch_attention(act(L8.q), kc, vc, len_next, B, 1, L, nh, d, 1.0f / sqrtf((float)d), act(L8.attn),
                            w + L8.attn_ws, *dc, s);
-    if (e == cudaSuccess) e = sk1(act(L8.attn), H, wgt(wt->w_o), nH, act(L8.y), ldH, false);
-    if (e == cudaSuccess) e = launch_rmsnorm_residual(act(L8.u), act(L8.y), act(L8.f), B, H, eps, s);
-    // the dense SwiGLU FFN: gate/up pair with the activation in the epilogue, then the down projection
-    if (e == cudaSuccess) e = sk1(act(L8.f), H, wgt(wt->w_gate_up), n2I, act(L8.act), ldI, true);
-    if (e == cudaSuccess) e = sk1(act(L8.act), I, wgt(wt->w_down), nH, act(L8.z), ldH, false);
-    if (e == cudaSuccess) e = launch_rmsnorm_residual(act(L8.u), act(L8.z), act(L8.hn), B, H, eps, s);
+    // u += attn W_o^T, the residual added in the product's epilogue (one rounding)
+    const bf16* res_u = act(L8.u);
+    if (e == cudaSuccess) {
+      const bf16* wo = wgt(wt->w_o);
+      bf16* yu = act(L8.u);
+      e = launch_skinny(act(L8.attn), B, H, &wo, &nH, &yu, &ldH, 1, false, *dc, s, 0.0f, &res_u);
+    }
+    // the dense SwiGLU FFN of RMSNorm(u) (the norm folded in), then u += act W_down^T
+    if (e == cudaSuccess) {
+      const bf16* wgu = wgt(wt->w_gate_up);
+      bf16* ya = act(L8.act);
+      e = launch_skinny(act(L8.u), B, H, &wgu, &n2I, &ya, &ldI, 1, true, *dc, s, eps);
+    }
+    if (e == cudaSuccess) {
+      const bf16* wd = wgt(wt->w_down);
+      bf16* yu = act(L8.u);
+      e = launch_skinny(act(L8.act), B, I, &wd, &nH, &yu, &ldH, 1, false, *dc, s, 0.0f, &res_u);
+    }
+    // the draft token: the greedy token of W_vocab RMSNorm(u), which is the greedy token of W_vocab u
+    // (the norm scales a row's logits by one positive factor)
     if (e == cudaSuccess)
-      e = launch_lmhead_accept(act(L8.hn), wgt(wt->w_vocab), nullptr, B, 0, V, H, i32(L8.tok), i32(L8.alen),
+      e = launch_lmhead_accept(act(L8.u), wgt(wt->w_vocab), nullptr, B, 0, V, H, i32(L8.tok), i32(L8.alen),
                                i32(L8.comm), w + L8.lm_ws, *dc, s);
     if (e == cudaSuccess)
       e = cudaMemcpy2DAsync(drafts + i, (size_t)K * 4, i32(L8.tok), 4, 4, B, cudaMemcpyDeviceToDevice, s);

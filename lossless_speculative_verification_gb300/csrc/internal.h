@@ -176,10 +176,13 @@ cudaError_t launch_attention(const bf16* q, const bf16* kc, const bf16* vc, cons
 // Dense products for few rows of x (skinny.cu): y_j = x W_j^T for up to kSkMaxJobs weight matrices
 // W_j [n_rows[j], K] sharing x [M, K] (M <= kSkMaxRows), or in the SwiGLU form y = silu(x W_g^T) * (x W_u^T)
 // with W = [W_g; W_u] of n_rows = 2F rows.  K split over the CTAs of a cluster, reduced in shared memory.
+// norm_eps > 0 folds RMSNorm of x's rows in (output row m scaled by 1/sqrt(mean_k x[m,k]^2 + eps));
+// res[j] (optional, [M, ldy[j]], may equal y[j]) is added before the bf16 store.
 constexpr int kSkMaxRows = 256;
 constexpr int kSkMaxJobs = 3;
 cudaError_t launch_skinny(const bf16* x, int M, int K, const bf16* const* w, const int* n_rows, bf16* const* y,
-                          const int* ldy, int njobs, bool swiglu, const DeviceCtx& dc, cudaStream_t s);
+                          const int* ldy, int njobs, bool swiglu, const DeviceCtx& dc, cudaStream_t s,
+                          float norm_eps = 0.0f, const bf16* const* res = nullptr);
 // y[M, N] = bf16(x[M, K] w[N, K]^T) on tcgen05 (K % 64 == 0, N % 8 == 0).
 cudaError_t launch_dense_gemm(const bf16* x, const bf16* w, bf16* y, int M, int N, int K, const DeviceCtx& dc,
                               cudaStream_t s);

@@ -40,15 +40,18 @@ constexpr int kSkMaxStages = 8;
 constexpr int kSkATile = 128 * 128;  // one 64-wide K chunk of 128 weight rows
 
 struct SkJob {
-  bf16* y;    // output [M, ldy]
+  bf16* y;         // output [M, ldy]
+  const bf16* r;   // optional residual [M, ldy] added before the bf16 store (may be y itself)
   int ldy;
-  int n_out;  // output columns of this job
-  int tile0;  // first tile of this job
+  int n_out;       // output columns of this job
+  int tile0;       // first tile of this job
 };
 
 struct SkParams {
   int M, nk, n_mma, nsplit, njobs, stages;
   SkJob job[kSkMaxJobs];
+  const bf16* x;   // the rows of x (for their mean squares)
+  float norm_eps;  // > 0: scale output column m by 1/sqrt(mean_k x[m,k]^2 + eps) (RMSNorm of x folded in)
   int* err;
   uint64_t wait_ns;
 };
@@ -59,6 +62,18 @@ struct SkMaps {
 };
 
 __device__ __forceinline__ float sk_silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// 1/sqrt(mean square + eps) of x rows 4c4..4c4+3, from every rank's share in rank order.
+__device__ __forceinline__ float4 row_scales(const float* recv_ss, int ns, int n_mma, int c4, int K, float eps) {
+  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = 0; r < ns; ++r) {
+    const float4 v = *reinterpret_cast<const float4*>(recv_ss + r * n_mma + 4 * c4);
+    t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+  }
+  const float inv_k = 1.0f / (float)K;
+  return make_float4(rsqrtf(t.x * inv_k + eps), rsqrtf(t.y * inv_k + eps), rsqrtf(t.z * inv_k + eps),
+                     rsqrtf(t.w * inv_k + eps));
+}
 
 // Grid (nsplit, tiles): blockIdx.y is the weight tile, blockIdx.x its K split and cluster rank.
 template <bool kSwiglu>
@@ -85,6 +100,8 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
   // slice is even and SwiGLU pairs stay together); recv[src] receives rank src's partial of them
   const int slot_rows = 128 / ns;
   float* recv = reinterpret_cast<float*>(smem + p.stages * stage_bytes);  // [ns][slot_rows][n_mma]
+  float* recv_ss = recv + ns * slot_rows * p.n_mma;                       // [ns][n_mma] (norm_eps > 0)
+  const bool norm = p.norm_eps > 0.0f;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -96,8 +113,9 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
     mbar_init(&recv_bar, 1);
     abort_flag = 0;
     fence_barrier_init();
-    // the other ranks' partials of this CTA's rows
-    if (ns > 1) mbar_arrive_expect_tx(&recv_bar, (uint32_t)((ns - 1) * slot_rows * p.n_mma * 4));
+    // the other ranks' partials of this CTA's rows (and of the rows' mean squares)
+    if (ns > 1)
+      mbar_arrive_expect_tx(&recv_bar, (uint32_t)((ns - 1) * (slot_rows + (p.norm_eps > 0.0f ? 1 : 0)) * p.n_mma * 4));
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, tcols);
@@ -199,6 +217,36 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
     cluster_wait();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
+    if (norm) {
+      // While the MMAs run: this split's share of each x row's sum of squares (its K chunks),
+      // one warp per row in turn, sent to every rank (its own: a plain shared store).
+      pdl_wait();  // x comes from the preceding kernel
+      const int we = warp - 2;
+      const int q0 = c0 * 8, q1 = c1 * 8;  // 16-byte pieces of the row in this split
+      float* ss_own = recv_ss + split * p.n_mma;
+      for (int m = we; m < p.n_mma; m += 4) {
+        float a = 0.0f;
+        if (m < p.M) {
+          const uint4* row = reinterpret_cast<const uint4*>(p.x + (size_t)m * p.nk * 64);
+          for (int q = q0 + lane; q < q1; q += 32) {
+            float f[8];
+            const uint4 v = __ldg(row + q);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              f[2 * i] = __uint_as_float(wv[i] << 16);
+              f[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a = fmaf(f[i], f[i], a);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) ss_own[m] = a;
+      }
+      named_bar_sync(1, 128);  // the epilogue warps' shares are in ss_own
+    }
     // Warp w reads TMEM lanes 32*(w%4)..+31 (one weight row per thread) and sends each row to
     // the rank that sums it: into that rank's recv[split] (its own rows: plain shared stores).
     const bool got = mbar_wait(&tfull, 0, p.wait_ns);
@@ -210,6 +258,17 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
     const int off = ((split * slot_rows) + row - dst_rank * slot_rows) * p.n_mma;
     float* mine = recv + off;
     cluster_wait();  // every CTA of the cluster runs, with its receive barrier armed
+    if (norm) {
+      // this split's sums of squares to every other rank's recv_ss[split]
+      const int tid = threadIdx.x - 64, q4 = p.n_mma / 4;
+      const float* ss_own = recv_ss + split * p.n_mma;
+      for (int u = tid; u < (ns - 1) * q4; u += 128) {
+        const int d = u / q4 + (u / q4 >= split ? 1 : 0), c = u % q4;
+        const float4 v = *reinterpret_cast<const float4*>(ss_own + 4 * c);
+        st_async_f4(mapa_shared(smem_u32(ss_own + 4 * c), (uint32_t)d), v,
+                    mapa_shared(smem_u32(&recv_bar), (uint32_t)d));
+      }
+    }
     const uint32_t dst = mapa_shared(smem_u32(recv + off), (uint32_t)dst_rank);
     const uint32_t dst_bar = mapa_shared(smem_u32(&recv_bar), (uint32_t)dst_rank);
     const uint32_t t_row = tmem_base + ((uint32_t)(32 * qd) << 16);
@@ -268,6 +327,11 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
             g.x += a[r].x; g.y += a[r].y; g.z += a[r].z; g.w += a[r].w;
             v.x += b[r].x; v.y += b[r].y; v.z += b[r].z; v.w += b[r].w;
           }
+        if (norm) {
+          const float4 sc = row_scales(recv_ss, ns, p.n_mma, c4, p.nk * 64, p.norm_eps);
+          g.x *= sc.x; g.y *= sc.y; g.z *= sc.z; g.w *= sc.w;
+          v.x *= sc.x; v.y *= sc.y; v.z *= sc.z; v.w *= sc.w;
+        }
         const int f = tile * 64 + pr;
         if (f < jb.n_out) {
           bf16* yc = jb.y + (size_t)(4 * c4) * jb.ldy + f;
@@ -296,10 +360,23 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
           if (r < ns) {
             acc.x += a[r].x; acc.y += a[r].y; acc.z += a[r].z; acc.w += a[r].w;
           }
+        if (norm) {
+          const float4 sc = row_scales(recv_ss, ns, p.n_mma, c4, p.nk * 64, p.norm_eps);
+          acc.x *= sc.x; acc.y *= sc.y; acc.z *= sc.z; acc.w *= sc.w;
+        }
         const int f = tile * 128 + rr;
         if (f < jb.n_out) {
-          bf16* yc = jb.y + (size_t)(4 * c4) * jb.ldy + f;
+          const size_t at = (size_t)(4 * c4) * jb.ldy + f;
+          bf16* yc = jb.y + at;
           const int m = p.M - 4 * c4;
+          if (jb.r) {
+            // the residual stream plus this product, rounded once
+            const bf16* rc = jb.r + at;
+            if (m > 0) acc.x += __bfloat162float(rc[0]);
+            if (m > 1) acc.y += __bfloat162float(rc[jb.ldy]);
+            if (m > 2) acc.z += __bfloat162float(rc[2 * jb.ldy]);
+            if (m > 3) acc.w += __bfloat162float(rc[3 * jb.ldy]);
+          }
           if (m > 0) yc[0] = __float2bfloat16_rn(acc.x);
           if (m > 1) yc[jb.ldy] = __float2bfloat16_rn(acc.y);
           if (m > 2) yc[2 * jb.ldy] = __float2bfloat16_rn(acc.z);
@@ -316,15 +393,23 @@ __global__ void __launch_bounds__(kSkThreads) skinny_gemm_kernel(const __grid_co
 
 // Ring stages: `base` (four keep two CTAs per SM up to 64 rows of x; eight give a lone CTA per SM
 // more bytes in flight), within 200 KB together with the receive slots (at least two).
-int sk_stages(int n_mma, int base) {
+// Bytes per accumulator column of the receive slots: ns ranks x 128/ns rows x fp32 = 512, plus, with
+// the norm folded in, up to 8 ranks' mean-square shares (32).
+int sk_recv_per_col(bool norm) { return norm ? 544 : 512; }
+
+int sk_stages(int n_mma, int base, bool norm) {
   const int stage = kSkATile + n_mma * 128;
   int st = base > kSkMaxStages ? kSkMaxStages : base;
-  while (st > 2 && st * stage + 512 * n_mma > 200 * 1024) --st;
+  while (st > 2 && st * stage + sk_recv_per_col(norm) * n_mma > 200 * 1024) --st;
   return st;
 }
 
-// The ring, then the receive slots: ns ranks x 128/ns rows x n_mma fp32 = 512 n_mma bytes.
-int sk_smem(int n_mma, int stages) { return 1024 + stages * (kSkATile + n_mma * 128) + 512 * n_mma; }
+// The ring, then the receive slots.  At n_mma = 256, two stages and the norm's shares that would be
+// 233 KB, past the 227 KB a CTA may have, so products with the norm folded in take at most 128 rows
+// of x per launch.
+int sk_smem(int n_mma, int stages, bool norm) {
+  return 1024 + stages * (kSkATile + n_mma * 128) + sk_recv_per_col(norm) * n_mma;
+}
 
 // CTAs of clusters of `ns` that the device holds at once for this shared-memory size (cached).
 int sk_capacity(bool swiglu, int ns, int smem, const DeviceCtx& dc) {
@@ -363,8 +448,22 @@ int sk_capacity(bool swiglu, int ns, int smem, const DeviceCtx& dc) {
 }  // namespace
 
 cudaError_t launch_skinny(const bf16* x, int M, int K, const bf16* const* w, const int* n_rows, bf16* const* y,
-                          const int* ldy, int njobs, bool swiglu, const DeviceCtx& dc, cudaStream_t s) {
+                          const int* ldy, int njobs, bool swiglu, const DeviceCtx& dc, cudaStream_t s,
+                          float norm_eps, const bf16* const* res) {
   if (M <= 0 || M > kSkMaxRows || njobs < 1 || njobs > kSkMaxJobs || K <= 0 || K % 64) return cudaErrorInvalidValue;
+  if (norm_eps > 0.0f && M > 128) {
+    // two launches of at most 128 rows each (the norm is per row, so this is exact)
+    bf16* y2[kSkMaxJobs];
+    const bf16* r2[kSkMaxJobs];
+    for (int j = 0; j < njobs; ++j) {
+      y2[j] = y[j] + (size_t)128 * ldy[j];
+      r2[j] = res && res[j] ? res[j] + (size_t)128 * ldy[j] : nullptr;
+    }
+    const cudaError_t e = launch_skinny(x, 128, K, w, n_rows, y, ldy, njobs, swiglu, dc, s, norm_eps, res);
+    if (e != cudaSuccess) return e;
+    return launch_skinny(x + (size_t)128 * K, M - 128, K, w, n_rows, y2, ldy, njobs, swiglu, dc, s, norm_eps,
+                         res ? r2 : nullptr);
+  }
   SkParams p = {};
   SkMaps maps;
   p.M = M;
@@ -375,6 +474,7 @@ cudaError_t launch_skinny(const bf16* x, int M, int K, const bf16* const* w, con
   for (int j = 0; j < njobs; ++j) {
     SkJob& jb = p.job[j];
     jb.y = y[j];
+    jb.r = res ? res[j] : nullptr;
     jb.ldy = ldy[j];
     jb.n_out = swiglu ? n_rows[j] / 2 : n_rows[j];
     jb.tile0 = tiles;
@@ -386,8 +486,9 @@ cudaError_t launch_skinny(const bf16* x, int M, int K, const bf16* const* w, con
   for (int j = njobs; j < kSkMaxJobs; ++j) maps.w[j] = maps.w[0];
   if (!make_map(&maps.x, x, M, K, p.n_mma)) return cudaErrorInvalidValue;
   if (tiles > 65535) return cudaErrorInvalidValue;
-  p.stages = sk_stages(p.n_mma, 4);
-  int smem = sk_smem(p.n_mma, p.stages);
+  const bool norm = norm_eps > 0.0f;
+  p.stages = sk_stages(p.n_mma, 4, norm);
+  int smem = sk_smem(p.n_mma, p.stages, norm);
   // splits per tile: the one of 1, 2, 4, 8 (at most the K chunks) whose launch fits one wave and
   // gives the SMs the smallest share of the weights (the fewer splits on equal shares)
   int ns = 1;
@@ -403,14 +504,16 @@ cudaError_t launch_skinny(const bf16* x, int M, int K, const bf16* const* w, con
   }
   // at most one CTA per SM: a deeper ring, if the clusters still fit at once
   if ((long long)tiles * ns <= dc.num_sms) {
-    const int st = sk_stages(p.n_mma, kSkMaxStages);
-    const int sm2 = sk_smem(p.n_mma, st);
+    const int st = sk_stages(p.n_mma, kSkMaxStages, norm);
+    const int sm2 = sk_smem(p.n_mma, st, norm);
     if (st > p.stages && (long long)tiles * ns <= sk_capacity(swiglu, ns, sm2, dc)) {
       p.stages = st;
       smem = sm2;
     }
   }
   p.nsplit = ns;
+  p.x = x;
+  p.norm_eps = norm_eps;
   p.err = dc.err;
   p.wait_ns = wait_limit_ns();
   cudaLaunchConfig_t cfg = {};
