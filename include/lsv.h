@@ -312,10 +312,12 @@ typedef struct {
  * (optional) the last u.  ctx_len [B] int32 (device) is read, not written;
  * ctx_len[b] + K <= L.  Supported: 0 <= B <= 256, H % 64 == 0, H <= 16384,
  * H/nh in {64, 128}, I % 64 == 0, I <= 16384, 1 <= K <= 63.  Per step, 11
- * launches: the block input's norms, the projections as the few-row products of
+ * launches and no copies: the block input's norms (step i > 1 reads its token
+ * from column i - 1 of drafts), the projections as the few-row products of
  * dense_matmul / dense_swiglu (q, k and v in one launch), the cache append, the
- * attention of spec_verify_attention at one query, and the output layer fused
- * with the greedy search of spec_verify_lmhead.
+ * attention of spec_verify_attention at one query (two launches), and the
+ * output layer fused with the greedy search of spec_verify_lmhead (two
+ * launches), which writes the step's token into column i of drafts.
  * ws: spec_draft_workspace_size(B, H, nh, I, V, L) bytes, zero before the first
  * use; calls that raise no device error leave it fit for the next call. */
 size_t spec_draft_workspace_size(int32_t B, int32_t H, int32_t nh, int32_t I, int32_t V, int32_t L);
@@ -334,8 +336,8 @@ lsv_status spec_draft_loop(const lsv_draft_weights *weights, const void *h0, con
  *   The argmax partials live in one fixed device array of 128 KiB (16,384
  *   (max, index) pairs), held by every device that loads the library until
  *   the process exits.  A call needs B*(K+1) rows times the chunks per row
- *   (on a 152-SM GB300: 3 chunks per row at 128 rows of 129,280 logits, 1
- *   chunk per row from 456 rows on), so up to 16,384 rows; a larger problem
+ *   (on a 152-SM GB300: 4 chunks per row at 128 rows of 129,280 logits, 1
+ *   chunk per row from 305 rows on), so up to 16,384 rows; a larger problem
  *   returns LSV_ERR_UNSUPPORTED before any launch.
  *   The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  *   routine.  The first call on each device looks up the array's device

@@ -136,13 +136,18 @@ __global__ void __launch_bounds__(kAccThreads) argmax_partial_bulk_kernel(const 
   float bv = -INFINITY;
   int bi = begin;  // a chunk of -inf gives its first index, so a row of -inf gives 0
   bool ok = true;
+  int q_fail = npieces;
   for (int q = 0; q < npieces; ++q) {
     const int slot = q % kRingSlots;
     if (!mbar_wait(&bar[slot], (q / kRingSlots) & 1, wait_ns)) {
       set_error(err, kErrTimeout);
       ok = false;
     }
-    if (__syncthreads_or(!ok)) break;
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      q_fail = q;
+      break;
+    }
     const int n = min(kPiece, bytes - q * kPiece);
     const uint4* v = reinterpret_cast<const uint4*>(ring + slot * kPiece);
     const int e0 = begin + q * (kPiece / 2);
@@ -177,16 +182,23 @@ __global__ void __launch_bounds__(kAccThreads) argmax_partial_bulk_kernel(const 
       bulk_load(ring + slot * kPiece, src + (size_t)qn * kPiece, nn, &bar[slot]);
     }
   }
+  if (!ok && threadIdx.x == 0) {
+    // a wait gave up at piece q_fail: let the copies still in flight into this CTA's ring land
+    // (again with a limit) before the CTA exits
+    for (int q = q_fail; q < npieces && q < q_fail + kRingSlots; ++q)
+      mbar_wait(&bar[q % kRingSlots], (q / kRingSlots) & 1, wait_ns);
+  }
   block_reduce_store(bv, bi, pv, pi, (size_t)r * nchunk + c);
 }
 
 // One CTA per sequence, one warp per verified row: each warp reduces its row's
-// chunk partials; then one thread applies the acceptance rule.
+// chunk partials; then one thread applies the acceptance rule.  argmax rows of
+// sequence b start at b * argmax_ld; accept_len and committed may be null.
 constexpr int kFinWarps = 32;
 
 __global__ void __launch_bounds__(kFinWarps * 32) accept_finalize_kernel(
     const float* __restrict__ pv, const int* __restrict__ pi, int nchunk, const int32_t* __restrict__ drafts,
-    int B, int K, int32_t* __restrict__ argmax, int32_t* __restrict__ accept_len,
+    int B, int K, int32_t* __restrict__ argmax, int argmax_ld, int32_t* __restrict__ accept_len,
     int32_t* __restrict__ committed) {
   pdl_wait();
   pdl_trigger();
@@ -206,11 +218,11 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finalize_kernel(
     }
     if (lane == 0) {
       g[j] = bi;
-      if (argmax) argmax[r] = bi;
+      if (argmax) argmax[(size_t)b * argmax_ld + j] = bi;
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && accept_len && committed) {
     int L = 0;
     while (L < K && drafts[(size_t)b * K + L] == g[L]) ++L;
     accept_len[b] = L;
@@ -274,10 +286,11 @@ cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int 
 }
 
 cudaError_t launch_accept_finalize(const float* pv, const int* pi, int nchunk, const int32_t* drafts, int B, int K,
-                                   int32_t* argmax, int32_t* accept_len, int32_t* committed, cudaStream_t s) {
+                                   int32_t* argmax, int32_t* accept_len, int32_t* committed, cudaStream_t s,
+                                   int argmax_ld) {
   if (B == 0) return cudaSuccess;
   return launch_pdl(accept_finalize_kernel, dim3(B), dim3(32 * min(K + 1, kFinWarps)), 0, s, pv, pi, nchunk, drafts,
-                    B, K, argmax, accept_len, committed);
+                    B, K, argmax, argmax_ld > 0 ? argmax_ld : K + 1, accept_len, committed);
 }
 
 }  // namespace lsv

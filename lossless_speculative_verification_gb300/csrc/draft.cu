@@ -16,10 +16,12 @@
 // Kernels of this file: the row normalisation that also gathers embedding
 // rows, the append of a step's keys and values to the caches, and a dense
 // bf16 product y = x W^T on tcgen05 (TMA-fed, TMEM accumulators, bf16 store)
-// for the projections.  The rest reuses the library's own kernels: the
-// verify-attention kernel at one query per sequence, the expert kernel's
-// shared-expert path for the dense SwiGLU, the residual + RMSNorm kernel, and
-// the output layer fused with the greedy search.
+// for products of more than 256 rows.  The rest reuses the library's own
+// kernels: the few-row split-K product (skinny.cu) for the projections, with
+// the RMSNorms of u folded into the q/k/v and gate/up products and the
+// residual adds into the W_o and down epilogues, the verify-attention kernel
+// at one query per sequence, and the output layer fused with the greedy
+// search, which writes each step's token straight into the drafts.
 #include <math.h>
 
 #include "internal.h"
@@ -247,12 +249,12 @@ __global__ void __launch_bounds__(kDgThreads, 1) dense_gemm_kernel(const __grid_
 constexpr int kDnThreads = 256;
 
 // Row b of blockIdx.y == 0: y[b, 0:H] = bf16(RMSNorm(a[b, :])).  Of blockIdx.y == 1 (the block's
-// input): y[b, H:2H] = bf16(RMSNorm(e[rows[b], :])), an embedding row; a row index outside
-// [0, nsrc) writes zeros and raises LSV_ERR_DEVICE_INDEX.
+// input): y[b, H:2H] = bf16(RMSNorm(e[rows[b * rows_ld], :])), an embedding row; a row index
+// outside [0, nsrc) writes zeros and raises LSV_ERR_DEVICE_INDEX.
 __global__ void __launch_bounds__(kDnThreads) draft_norm_kernel(const bf16* __restrict__ a,
                                                                 const bf16* __restrict__ e, const int32_t* rows,
-                                                                int nsrc, bf16* __restrict__ y, int ldy, int H,
-                                                                float eps, int* err) {
+                                                                int rows_ld, int nsrc, bf16* __restrict__ y,
+                                                                int ldy, int H, float eps, int* err) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(kDnThreads) draft_norm_kernel(const bf16* __re
   bf16* yr = y + (size_t)b * ldy;
   if (blockIdx.y == 1) {
     yr += H;
-    const int src = __ldcg(rows + b);
+    const int src = __ldcg(rows + (size_t)b * rows_ld);
     if (src < 0 || src >= nsrc) {
       if (threadIdx.x == 0) set_error(err, kErrDeviceIndex);
       for (int c = threadIdx.x; c < H; c += kDnThreads) yr[c] = __float2bfloat16_rn(0.f);
@@ -342,7 +344,7 @@ cudaError_t launch_dense_gemm(const bf16* x, const bf16* w, bf16* y, int M, int 
 // Workspace of the draft loop: activations, the lengths, and the sub-workspaces of the
 // kernels it uses (each of which needs zero on first use and leaves its counters zero).
 struct DraftWs {
-  size_t inp, u, a, q, k, v, attn, y, f, hn, act, z, tok, alen, comm, len0, len1, attn_ws, lm_ws, total;
+  size_t inp, u, a, q, k, v, attn, y, f, hn, act, z, len0, len1, attn_ws, lm_ws, total;
   size_t attn_bytes, lm_bytes;
 };
 
@@ -367,9 +369,6 @@ DraftWs draft_ws_layout(int B, int H, int nh, int I, int V, int L) {
   w.hn = take(act);
   w.act = take((size_t)B * I * 2);
   w.z = take(act);
-  w.tok = take((size_t)B * 4);
-  w.alen = take((size_t)B * 4);
-  w.comm = take((size_t)B * 4);
   w.len0 = take((size_t)B * 4);
   w.len1 = take((size_t)B * 4);
   w.attn_bytes = spec_verify_attention_workspace_size(B, 1, L, nh, H / nh);
@@ -452,10 +451,12 @@ lsv_status spec_draft_loop(const lsv_draft_weights* wt, const void* h0, const in
   for (int i = 0; i < K && e == cudaSuccess; ++i) {
     int32_t* len_next = i32((i & 1) ? L8.len1 : L8.len0);
     const bf16* h_prev = i == 0 ? static_cast<const bf16*>(h0) : act(L8.u);
-    const int32_t* t_prev = i == 0 ? t0 : i32(L8.tok);
+    // the previous token: t0, then the last step's draft (column i - 1 of drafts)
+    const int32_t* t_prev = i == 0 ? t0 : drafts + (i - 1);
+    const int t_ld = i == 0 ? 1 : K;
     // the block's input [RMSNorm(h); RMSNorm(E[t])], one launch for both halves
-    e = launch_pdl(draft_norm_kernel, dim3(B, 2), dim3(kDnThreads), 0, s, h_prev, emb, t_prev, V, act(L8.inp), 2 * H,
-                   H, eps, dc->err);
+    e = launch_pdl(draft_norm_kernel, dim3(B, 2), dim3(kDnThreads), 0, s, h_prev, emb, t_prev, t_ld, V, act(L8.inp),
+                   2 * H, H, eps, dc->err);
     auto sk1 = [&](const bf16* x, int K_, const bf16* wm, int n, bf16* y, int ldy, bool swiglu) {
       return launch_skinny(x, B, K_, &wm, &n, &y, &ldy, 1, swiglu, *dc, s);
     };
@@ -488,12 +489,10 @@ lsv_status spec_draft_loop(const lsv_draft_weights* wt, const void* h0, const in
       e = launch_skinny(act(L8.act), B, I, &wd, &nH, &yu, &ldH, 1, false, *dc, s, 0.0f, &res_u);
     }
     // the draft token: the greedy token of W_vocab RMSNorm(u), which is the greedy token of W_vocab u
-    // (the norm scales a row's logits by one positive factor)
+    // (the norm scales a row's logits by one positive factor), written to column i of drafts
     if (e == cudaSuccess)
-      e = launch_lmhead_accept(act(L8.u), wgt(wt->w_vocab), nullptr, B, 0, V, H, i32(L8.tok), i32(L8.alen),
-                               i32(L8.comm), w + L8.lm_ws, *dc, s);
-    if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(drafts + i, (size_t)K * 4, i32(L8.tok), 4, 4, B, cudaMemcpyDeviceToDevice, s);
+      e = launch_lmhead_accept(act(L8.u), wgt(wt->w_vocab), nullptr, B, 0, V, H, drafts + i, nullptr, nullptr,
+                               w + L8.lm_ws, *dc, s, K);
     len_cur = len_next;
   }
   if (e == cudaSuccess && h_out) e = cudaMemcpyAsync(h_out, act(L8.u), (size_t)B * H * 2, cudaMemcpyDeviceToDevice, s);

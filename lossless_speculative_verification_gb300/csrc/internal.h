@@ -164,9 +164,11 @@ cudaError_t launch_rmsnorm_residual(bf16* x, const bf16* y, bf16* h, int T, int 
 
 size_t accept_ws_bytes(int B, int K, int V, int num_sms);
 // Reduce per-(row, chunk) (max, first index) partials [B*(K+1), nchunk] to greedy tokens and apply
-// the acceptance rule (one CTA per sequence).
+// the acceptance rule (one CTA per sequence).  argmax rows of sequence b start at b * argmax_ld
+// (0: K + 1); accept_len and committed both null: the greedy tokens alone.
 cudaError_t launch_accept_finalize(const float* pv, const int* pi, int nchunk, const int32_t* drafts, int B, int K,
-                                   int32_t* argmax, int32_t* accept_len, int32_t* committed, cudaStream_t s);
+                                   int32_t* argmax, int32_t* accept_len, int32_t* committed, cudaStream_t s,
+                                   int argmax_ld = 0);
 // Causal attention of Q verified positions per sequence over the cache.
 int attention_splits(int L);
 size_t attention_ws_bytes(int B, int Q, int L, int nh, int d);
@@ -189,11 +191,13 @@ cudaError_t launch_dense_gemm(const bf16* x, const bf16* w, bf16* y, int M, int 
 // Counts of the accepted lengths of a batch into hist [K+1].
 cudaError_t launch_accept_histogram(const int32_t* accept_len, int B, int K, int64_t* hist, int* err,
                                     cudaStream_t s);
-// The verifier's output layer fused with the greedy-token search, then acceptance.
+// The verifier's output layer fused with the greedy-token search, then acceptance.  argmax_ld: the
+// stride between sequences in argmax (0: K + 1); argmax may be null, and accept_len and committed
+// may both be null (no rule: the greedy tokens alone).
 size_t lmhead_ws_bytes(int B, int K, int V);
 cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const int32_t* drafts, int B, int K,
                                  int V, int H, int32_t* argmax, int32_t* accept_len, int32_t* committed, void* ws,
-                                 const DeviceCtx& dc, cudaStream_t s);
+                                 const DeviceCtx& dc, cudaStream_t s, int argmax_ld = 0);
 cudaError_t launch_accept(const bf16* logits, const int32_t* drafts, int B, int K, int V, int32_t* argmax,
                           int32_t* accept_len, int32_t* committed, void* ws, const DeviceCtx& dc,
                           cudaStream_t s);

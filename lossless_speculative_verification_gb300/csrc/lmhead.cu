@@ -11,7 +11,7 @@
 // review, Section 3.1 / Eq. 2).
 //
 // Orientation: the MMA's M side is 128 hidden rows (the verified positions) and
-// its N side 128 vocabulary rows, so that one TMEM lane holds one position's
+// its N side 176 vocabulary rows, so that one TMEM lane holds one position's
 // logits of the tile and its thread finds the tile maximum without talking to
 // other threads.  Both operands are K-major with the 128-byte swizzle, loaded
 // by TMA; the weights stream from HBM once (evict-first), the hidden rows stay
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lmhead_argmax_kernel(const __gr
       if (tr != cur_tr) {
         flush();
         best = -INFINITY;
-        bi = INT_MAX;
+        bi = tv * kLhN;  // a row of -inf keeps the first index this CTA saw (0 over the grid)
         cur_tr = tr;
       }
       cur_tv = tv;
@@ -293,7 +293,7 @@ size_t lmhead_ws_bytes(int B, int K, int V) {
 
 cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const int32_t* drafts, int B, int K,
                                  int V, int H, int32_t* argmax, int32_t* accept_len, int32_t* committed, void* ws,
-                                 const DeviceCtx& dc, cudaStream_t s) {
+                                 const DeviceCtx& dc, cudaStream_t s, int argmax_ld) {
   const int R = B * (K + 1);
   if (R == 0) return cudaSuccess;
   const cudaError_t ea =
@@ -333,7 +333,7 @@ cudaError_t launch_lmhead_accept(const bf16* hidden, const bf16* w_vocab, const 
       launch_pdl(lmhead_argmax_kernel, dim3(grid), dim3(kLhThreads), LhSmem::kTotal, s, hmap, hmap_last, wmap,
                  wmap_last, p);
   if (e != cudaSuccess) return e;
-  return launch_accept_finalize(p.pv, p.pi, p.nslot, drafts, B, K, argmax, accept_len, committed, s);
+  return launch_accept_finalize(p.pv, p.pi, p.nslot, drafts, B, K, argmax, accept_len, committed, s, argmax_ld);
 }
 
 }  // namespace lsv

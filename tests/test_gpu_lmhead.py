@@ -113,3 +113,38 @@ def test_lmhead_is_deterministic():
     b = run(p.hidden, p.w_vocab, p.drafts, p.K)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+def test_lmhead_zero_hidden_rows_give_token_zero():
+    # a hidden row of zeros makes every logit of its row +0 or -0 (the weights' signs vary), which
+    # are equal: the greedy token is 0, the first index, however the CTAs' results combine
+    B, K, V, H = 3, 1, 4099, 128
+    p = problem(B, K, V, H, 91)
+    hid = p.hidden.copy()
+    hid[1] = 0
+    hid[4] = 0x8000                              # -0 everywhere
+    g, _ = oracle.lmhead_argmax(hid, p.w_vocab)
+    assert g[1] == 0 and g[4] == 0
+    drafts = synth.draft_tokens(g.reshape(B, K + 1).astype(np.int32), V, [0.5], 5)
+    ga, alen, comm = run(hid, p.w_vocab, drafts, K)
+    np.testing.assert_array_equal(ga.reshape(-1), g)
+    ralen, rcomm = oracle.accept_from_greedy(g.reshape(B, K + 1), drafts)
+    np.testing.assert_array_equal(alen, ralen)
+    np.testing.assert_array_equal(comm, rcomm)
+
+
+def test_lmhead_workspace_reuse():
+    # one workspace across calls of different shapes: whatever a call leaves in it, the next call's
+    # results do not depend on it
+    ws = api.spec_verify_lmhead_workspace(64, 7, 4099, 192)
+    for B, K, V, H, seed in [(64, 7, 4099, 192, 1), (3, 0, 1000, 128, 2), (40, 3, 5000, 256, 3),
+                             (64, 7, 4099, 192, 4), (1, 1, 2000, 128, 5)]:
+        p = problem(B, K, V, H, seed)
+        argmax = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+        alen, comm = api.spec_verify_lmhead(to_dev(p.hidden), to_dev(p.w_vocab), torch.from_numpy(p.drafts).cuda(),
+                                            ws, K, argmax=argmax)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(argmax.cpu().numpy(), p.greedy)
+        ralen, rcomm = oracle.accept_from_greedy(p.greedy, p.drafts)
+        np.testing.assert_array_equal(alen.cpu().numpy(), ralen)
+        np.testing.assert_array_equal(comm.cpu().numpy(), rcomm)

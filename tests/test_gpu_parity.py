@@ -346,7 +346,8 @@ def test_accept_parity_sweep(B, K):
 
 
 @pytest.mark.parametrize("B,K,V", [(4, 3, 1024), (3, 2, 1023), (5, 1, 7), (2, 0, 100), (1, 7, 129_281),
-                                   (2, 63, 64), (600, 3, 4096), (4100, 1, 1024)])
+                                   (2, 63, 64), (600, 3, 4096), (4100, 1, 1024),
+                                   (4096, 0, 1001), (4096, 2, 2048)])
 def test_accept_edge_shapes(B, K, V):
     logits, planted = synth.verify_logits(B, K, V, seed=V + K)
     drafts = synth.draft_tokens(planted, V, [0.9] * K, seed=B)
