@@ -281,6 +281,28 @@ def test_layer_parity_smallest_batches(B, K):
     assert_layer_close(bf16_f64(from_dev_bf16(out)), ref, "T=%d" % d.T)
 
 
+@pytest.mark.parametrize("extra,H,E,k,S,I", [(0, 1280, 64, 6, 2, 896), (1, 1280, 64, 6, 2, 896),
+                                              (-115, 512, 256, 8, 1, 128)])
+def test_layer_routing_selection_and_counts(extra, H, E, k, S, I):
+    # the layer's selection for every token and its per-expert row counts, at one token per SM, one
+    # more (both the per-token router) and 37 tokens over 256 experts (the cluster router)
+    T = torch.cuda.get_device_properties(0).multi_processor_count + extra
+    d = synth.MoeDims(T, H, E, k, S, I)
+    prob = synth.moe_problem(d, seed=T + E, hidden="sphere", row_ok=oracle.gap_ok(k))
+    P = DevProblem(prob)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    out = api.moe_verify_layer(P.x, P.wts, P.sh, P.ws, topk_idx=idx, counts=counts)
+    torch.cuda.synchronize()
+    ridx, _ = oracle.route(prob.x, prob.w_router, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_array_equal(counts.cpu().numpy(), np.bincount(ridx.reshape(-1), minlength=E))
+    toks = sample_rows(T, 24, 3)
+    ref, _, _ = oracle.moe_layer(prob.x, prob.w_router, prob.w_gate_up, prob.w_down, prob.ws_gate_up,
+                                 prob.ws_down, k, S, tokens=toks)
+    assert_layer_close(bf16_f64(from_dev_bf16(out))[toks], ref, "T=%d E=%d" % (T, E))
+
+
 def test_layer_workspace_reuse_across_shapes():
     # one workspace for calls of different shapes and paths: every call must leave the counter
     # block at zero for the next one
